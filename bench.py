@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the BF16 optimizer step on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch of synthetic input: GAS
+accumulates of bf16 micro-batch gradients into the FP32 accumulator (the norm
+partials fused into the last one), the global-norm finish and the fused
+clip + AdamW + bf16-cast pass, on the scaled-down BLOOM shard (1,722,408,960
+elements in one flat buffer, 293 tensors, decay/no-decay groups, GAS 4).
+
+Prints ONE JSON line (rank 0).  `value` is elements/s over all ranks with
+inputs resident in HBM; `e2e` is the same metric with every micro-batch
+gradient copied from pinned host memory inside the timed region and the norm
+read back; `roofline` is the dominant kernel (the fused step) against the
+measured HBM copy peak; `cpu_baseline` is the CPU oracle on a bounded sample.
+`--impl reference` times that oracle instead, as the reference arm.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the shard
+(no collective on the data path: replicas only), timing is max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step elements/s and achieved HBM GB/s (% of peak) on 1 GB300"
+UNIT = "elements/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_step_scaled_bloom_1p72b.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "mixed_precision_optimizer_bf16_gb300", "csrc", f)
+                  for f in ("kernels.cuh", "bf16opt.cu")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--no-defer", action="store_true", help="store the last micro-batch into acc (no deferral)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time of the CPU baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the step kernel from the committed ncu summary,
+    or None when it is missing or was taken from other kernel sources."""
+    try:
+        txt = open(PROFILE_SUMMARY, encoding="utf-8").read()
+    except OSError:
+        return None
+    mh = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", txt)
+    mt = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    if not mh or not mt or mh.group(1) != kernel_hash():
+        return None
+    return float(mt.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, enabled=True):
+        self.p = None
+        self.enabled = enabled
+        self.gpu = gpu_index
+        if enabled:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x.strip().split()[0])
+            except (ValueError, IndexError):
+                return None
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        pw = [num(r[3]) for r in rows]
+        load = [s for s, p in zip(sm, pw) if s is not None and p is not None and p > 300.0] or [s for s in sm if s]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max([m for m in mx if m] or [0]) or None,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max([p for p in pw if p] or [0])}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
+    from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat
+    from synth import gpu as sgpu, workloads
+
+    rank, world, local = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    C.load()
+
+    wl = workloads.workload(args.workload)
+    assert wl.mode == "flat", "the timed workload is a flat shard"
+    n, G = wl.n, wl.gas
+    defer = not args.no_defer
+    flat = alloc_flat(n, dev, wl.misalign)
+    sgpu.fill_master(wl, flat["master"])
+    for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+        flat[k].zero_()
+    grads = []
+    for k in range(G):
+        g = torch.empty(n + wl.misalign + 64, dtype=torch.int16, device=dev)[wl.misalign:wl.misalign + n]
+        sgpu.fill_grad(wl, 0, k, g)
+        grads.append(g)
+    opt = BF16Optimizer(wl.groups, flat=flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        for k in range(G):
+            opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=defer and k == G - 1, stream=stream)
+            if ev is not None:
+                ev[1 + k].record(stream)
+        opt.grad_norm(stream=stream)
+        if ev is not None:
+            ev[G + 1].record(stream)
+        opt.step(stream=stream)
+        if ev is not None:
+            ev[G + 2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(G + 3)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local, enabled=(not args.no_clocks) and rank == 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0.record(stream)
+    for s in range(K):
+        one_step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # per-kernel device times (events on the launching stream)
+    names = [f"accumulate_{k}" for k in range(G)] + ["norm_final", "step"]
+    per = {nm: [] for nm in names}
+    for e in evs:
+        for i, nm in enumerate(names):
+            per[nm].append(e[i].elapsed_time(e[i + 1]))
+    bpe = {}
+    for k in range(G):
+        if k == 0:
+            bpe[f"accumulate_{k}"] = 2 if (defer and G == 1) else 6
+        elif k == G - 1 and defer:
+            bpe[f"accumulate_{k}"] = 6
+        else:
+            bpe[f"accumulate_{k}"] = 10
+    bpe["norm_final"] = 0
+    bpe["step"] = (32 if G > 1 else 30) if defer else 30
+    peak, peak_src = measured_peak()
+    kern = {}
+    for nm in names:
+        ms = statistics.mean(per[nm])
+        gbs = bpe[nm] * n / (ms * 1e-3) / 1e9 if bpe[nm] else None
+        kern[nm] = {"ms": round(ms, 4), "bytes_per_elem": bpe[nm],
+                    "gbs": round(gbs, 1) if gbs else None, "frac": round(gbs / peak, 4) if gbs else None}
+    step_ms = statistics.mean(per["step"])
+    achieved = bpe["step"] * n / (step_ms * 1e-3) / 1e9
+    step_bytes = sum(bpe.values()) * n
+    ms_per_step = total_ms / K
+    value = n * K * world / (total_ms * 1e-3)
+
+    # e2e: gradients from pinned host memory each step, norm read back
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = run_e2e(args, opt, grads, G, defer, dev, world, n)
+
+    opt.close()
+    del grads, flat
+    torch.cuda.empty_cache()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_oracle(wl, args.cpu_seconds, steps=1)
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded counter-based bf16 grads ~N(0,1e-4) (Irwin-Hall), masters N(0,0.02)/LN 1/0",
+        "config": {"workload": wl.name, "elements": n, "tensors": len(wl.tensors), "groups": 2, "gas": G,
+                   "mode": "flat; last micro-batch deferred into the fused step" if defer else "flat; norm fused into last accumulate",
+                   "bytes_per_elem_per_step": sum(bpe.values()), "hbm_gbs_per_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+                   "l2": "inputs larger than L2 (every buffer >= 3.4 GB), no flush", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "k_step (fused clip+AdamW+master+bf16)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": bpe["step"] * n},
+        "kernels": kern,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": K * (G + 2),
+    }
+    print(json.dumps(line))
+    sys.stdout.flush()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, opt, grads, G, defer, dev, world, n):
+    """Same step through the C ABI with every gradient copied from pinned host
+    memory (copy of micro-batch k+1 overlapping accumulate k on a second
+    stream) and the global norm read back to the host each step."""
+    import torch
+    import torch.distributed as dist
+
+    host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(G)]
+    for k in range(G):
+        host[k].copy_(grads[k])
+    torch.cuda.synchronize(dev)
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    free = [None] * G
+
+    def one():
+        norm = None
+        for k in range(G):
+            with torch.cuda.stream(copy):
+                if free[k] is not None:
+                    copy.wait_event(free[k])
+                grads[k].copy_(host[k], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy)
+            comp.wait_event(ev)
+            opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=defer and k == G - 1, stream=comp)
+            if not (defer and k == G - 1):
+                free[k] = torch.cuda.Event()
+                free[k].record(comp)
+        norm = opt.grad_norm(stream=comp, sync=True)
+        opt.step(stream=comp)
+        if defer:
+            free[G - 1] = torch.cuda.Event()
+            free[G - 1].record(comp)
+        return norm
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    torch.cuda.synchronize(dev)
+    dt = time.perf_counter() - t
+    if world > 1:
+        tt = torch.tensor([dt], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dt = float(tt.item())
+    del host
+    return {"value": round(n * args.e2e_steps * world / dt, 1), "unit": UNIT,
+            "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
+            "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps}
+
+
+# ------------------------------------------------------------ CPU oracle arm
+
+def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
+    """The CPU oracle, as it stands, on a bounded contiguous sample of the
+    workload: `steps` whole optimizer steps (GAS accumulates, norm, clip,
+    AdamW per group) over S elements, S sized from a pilot to about `seconds`."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    threads = oracle.nthreads()
+    G = [oracle.group(*(float(np.float32(g[k])) for k in ("lr", "beta1", "beta2", "eps", "weight_decay")))
+         for g in wl.groups]
+    off0 = wl.offsets[1] - (1 << 20) if len(wl.offsets) > 1 else 0
+
+    def ranges_for(lo, hi):
+        out = []
+        for b, e, gi in wl.ranges():
+            b2, e2 = max(b, lo), min(e, hi)
+            if b2 < e2:
+                out.append((b2 - lo, e2 - lo, gi))
+        return out
+
+    def make(S):
+        p = synth.fill_master(wl, np.empty(S, np.float32), off0)
+        gr = [[synth.fill_grad(wl, s, k, np.empty(S, np.uint16), off0) for k in range(wl.gas)]
+              for s in range(min(2, max(1, steps + warmup)))]
+        return p, gr
+
+    def timed(S, p, gr, nsteps, t0=0):
+        m = np.zeros(S, np.float32)
+        v = np.zeros(S, np.float32)
+        pb = np.zeros(S, np.uint16)
+        acc = np.zeros(S, np.float32)
+        rg = ranges_for(off0, off0 + S)
+        t = time.perf_counter()
+        for s in range(nsteps):
+            for k in range(wl.gas):
+                oracle.accumulate(acc, gr[s % len(gr)][k], first=k == 0, threads=threads)
+            c = oracle.clip_coef(oracle.sumsq(acc, threads=threads), wl.max_norm)
+            for b, e, gi in rg:
+                oracle.adamw(p[b:e], m[b:e], v[b:e], pb[b:e], acc[b:e], c, G[gi], t0 + s + 1, threads=threads)
+        return time.perf_counter() - t
+
+    S0 = 1 << 22
+    p, gr = make(S0)
+    dt0 = timed(S0, p, gr, 1)
+    per_elem = dt0 / S0
+    S = int(min(max(seconds / max(steps, 1) / per_elem, S0), 1 << 28, wl.n - off0))
+    S -= S % 4096
+    p, gr = make(S)
+    if warmup:
+        timed(S, p.copy(), gr, warmup)
+    dt = timed(S, p, gr, steps)
+    val = S * steps / dt
+    return {"value": round(val, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{S} contiguous elements of the {wl.n}-element shard from element {off0} "
+                      f"(spans the embedding tail and the first layers, both groups), {steps} whole step(s) of "
+                      f"GAS {wl.gas}; input generation untimed", "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    from synth import workloads
+    wl = workloads.workload(args.workload)
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    cpu = cpu_oracle(wl, per_step * args.steps, steps=args.steps, warmup=args.warmup)
+    line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(cpu["seconds"] * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generators)",
+            "config": {"workload": wl.name, "elements": wl.n, "gas": wl.gas,
+                       "note": "reference arm = the FP64 CPU oracle on a bounded sample per step"},
+            "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cpu["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

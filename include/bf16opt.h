@@ -1,0 +1,179 @@
+/*
+ * bf16opt.h -- C ABI of the BF16 mixed-precision optimizer step for one GPU.
+ *
+ * What the library computes, per optimizer step over one rank's parameter
+ * shard (the BF16Optimizer of BLOOM-176B training):
+ *   1. the bf16 gradients of the GAS micro-batches are summed into an FP32
+ *      accumulator, in micro-batch order, stored as FP32 after every add
+ *      ("BLOOM 176B 训练技术概览", section "BF16 优化器": all accumulation in
+ *      FP32, gradients accumulated in FP32 across pipeline micro-batches);
+ *   2. the global L2 norm of the accumulated gradient is reduced
+ *      deterministically and the gradient is clipped to max_grad_norm
+ *      ("企业官网建设流程全解析" (cf-1.com), section 4.3: global-norm threshold 1.0;
+ *      "单机多卡实战：Megatron-DeepSpeed训练类BLOOM模型全流程解析", section 3: clip_grad 1.0);
+ *   3. AdamW with decoupled, lr-scaled weight decay and bias correction
+ *      updates the FP32 master weights and the FP32 first/second moments
+ *      ("企业官网建设流程全解析", section 1: FP32 master, momentum and variance;
+ *      section 3.3: AdamW lr 6e-5, weight_decay 0.01) and the bf16 working
+ *      parameters are written as the round-to-nearest-even bf16 of the FP32
+ *      master, all in one pass.
+ *
+ * Conventions.
+ *   - Every buffer is caller-owned device memory (e.g. from PyTorch) that must
+ *     outlive the handle; buffers must not overlap.  The library owns only
+ *     its scratch (segment/chunk tables, norm partials, norm scalars).
+ *   - FP32 buffers must be 4-byte aligned and bf16 buffers 2-byte aligned
+ *     (BF16OPT_ERR_ALIGNMENT otherwise).  Any offset modulo 16 bytes works;
+ *     full speed needs every buffer of a tensor to share the same element
+ *     offset modulo 16 bytes.
+ *   - Elements are counted in uint64_t; a tensor or shard may exceed 2^32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work is enqueued on it; no call synchronises
+ *     except bf16opt_grad_norm with a non-NULL host_norm.
+ *   - Every call returns 0 on success, a positive warning, or a negative
+ *     error code; no C++ exception crosses the ABI.  On an error nothing is
+ *     enqueued and the handle's sequence state is unchanged.
+ *     bf16opt_last_error() gives a one-line message.
+ *   - A handle is bound to the device that was current at bf16opt_create and
+ *     is not thread-safe: use one handle from one host thread at a time.
+ *
+ * Sequence per optimizer step (checked on the host; BF16OPT_ERR_SEQUENCE):
+ *   accumulate(FIRST) ... accumulate(LAST) -> grad_norm -> step
+ *   FIRST marks the first micro-batch (the accumulator is overwritten, not
+ *   added to); LAST marks the last one (the norm's partial sums are fused
+ *   into that pass).  FIRST|LAST is a single micro-batch.  grad_norm may also
+ *   follow a non-LAST accumulate; it then reads the accumulator once more.
+ */
+#ifndef BF16OPT_H
+#define BF16OPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define BF16OPT_OK 0
+#define BF16OPT_WARN_NONFINITE 1       /* grad_norm: the norm is Inf or NaN */
+#define BF16OPT_ERR_INVALID_ARG (-1)   /* NULL handle/pointer, bad size, bad hyper-parameter, overlap */
+#define BF16OPT_ERR_ALIGNMENT (-2)     /* FP32 pointer not 4-B aligned or bf16 pointer not 2-B aligned */
+#define BF16OPT_ERR_SEQUENCE (-3)      /* call out of the accumulate -> grad_norm -> step order */
+#define BF16OPT_ERR_OOM (-4)           /* the library's scratch could not be allocated */
+#define BF16OPT_ERR_CUDA (-5)          /* a CUDA runtime call or kernel launch failed */
+#define BF16OPT_ERR_UNSUPPORTED (-6)   /* e.g. no usable CUDA device */
+
+/* ---- modes and flags --------------------------------------------------- */
+#define BF16OPT_FLAT 0   /* one contiguous shard: five flat buffers + group ranges */
+#define BF16OPT_LIST 1   /* ragged list: five buffers per tensor (separate allocations) */
+
+#define BF16OPT_FIRST 1u /* first micro-batch of the step: acc = fp32(g) */
+#define BF16OPT_LAST 2u  /* last micro-batch: fuse the norm's partial sums into this pass */
+#define BF16OPT_DEFER 4u /* with LAST: do not store acc + g; the step kernel re-reads this
+                            micro-batch's gradient, which must stay valid and unchanged
+                            until bf16opt_step has run on the stream */
+
+#define BF16OPT_MAX_GROUPS 16
+
+/* ---- descriptors (host memory; copied by bf16opt_create) ---------------- */
+
+/* FLAT mode: elements [begin, end) of the shard belong to parameter group `group`. */
+typedef struct {
+    uint64_t begin, end;
+    uint32_t group;
+    uint32_t reserved;     /* must be 0 */
+} bf16opt_range_t;
+
+/* LIST mode: one tensor; every pointer is device memory of `numel` elements. */
+typedef struct {
+    float *master;         /* FP32 master weights */
+    float *exp_avg;        /* FP32 first moment m */
+    float *exp_avg_sq;     /* FP32 second moment v */
+    float *grad_accum;     /* FP32 gradient accumulator */
+    uint16_t *param_bf16;  /* bf16 working parameters (bit patterns) */
+    uint64_t numel;
+    uint32_t group;
+    uint32_t reserved;     /* must be 0 */
+} bf16opt_tensor_t;
+
+/* AdamW hyper-parameters of one parameter group. */
+typedef struct {
+    float lr;              /* >= 0 */
+    float beta1, beta2;    /* in [0, 1) */
+    float eps;             /* > 0 */
+    float weight_decay;    /* >= 0; decoupled: p -= lr * weight_decay * p */
+} bf16opt_group_t;
+
+typedef struct {
+    int32_t mode;                    /* BF16OPT_FLAT or BF16OPT_LIST */
+    uint32_t n_groups;               /* 1 .. BF16OPT_MAX_GROUPS */
+    const bf16opt_group_t *groups;   /* n_groups entries */
+    /* FLAT */
+    uint64_t n;                      /* shard elements (0 allowed) */
+    float *master, *exp_avg, *exp_avg_sq, *grad_accum;
+    uint16_t *param_bf16;
+    const bf16opt_range_t *ranges;   /* must tile [0, n) in order; NULL/0 = one range, group 0 */
+    uint32_t n_ranges;
+    /* LIST */
+    uint32_t n_tensors;
+    const bf16opt_tensor_t *tensors;
+    /* clipping */
+    float max_grad_norm;             /* global L2 clip threshold; <= 0 disables clipping */
+    float grad_scale;                /* multiplies the accumulated gradient before norm and
+                                        update (rounded to FP32); 1 = none; finite, != 0 */
+} bf16opt_desc_t;
+
+typedef struct bf16opt bf16opt_t;    /* opaque handle */
+
+/* ---- entry points ------------------------------------------------------- */
+
+/* Validates `d`, copies its host arrays, builds the segment and chunk tables
+ * on the device and allocates the norm scratch.  *out receives the handle
+ * (NULL on error).  The step counter starts at 0. */
+int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out);
+
+/* Adds one micro-batch of bf16 gradients into the FP32 accumulator
+ * ("BLOOM 176B 训练技术概览", "BF16 优化器").
+ *   FLAT: grad_flat = device bf16 buffer of n elements, grad_list = NULL.
+ *   LIST: grad_flat = NULL, grad_list = HOST array of n_tensors device
+ *         pointers (read during the call only).
+ *   flags: BF16OPT_FIRST / BF16OPT_LAST / BF16OPT_DEFER (see above).
+ * The gradient buffer is read on `stream`; it may be reused after the work
+ * on `stream` is done, except under BF16OPT_DEFER (until bf16opt_step). */
+int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list,
+                       unsigned flags, void *stream);
+
+/* Finishes the deterministic global L2 norm of the accumulated gradient
+ * (times grad_scale) and the clip coefficient c = max_grad_norm / norm if
+ * norm > max_grad_norm, else 1 ("企业官网建设流程全解析", section 4.3).  Both stay
+ * on the device for bf16opt_step.  host_norm == NULL: fully asynchronous.
+ * host_norm != NULL: waits for `stream` and stores the norm (FP64); returns
+ * BF16OPT_WARN_NONFINITE if it is Inf or NaN (the caller decides whether to
+ * call bf16opt_step; the library does not skip steps). */
+int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
+
+/* One fused pass: clip, AdamW (t = t + 1, bias-corrected, decoupled
+ * weight decay), FP32 master/moment update and bf16 parameter write
+ * ("企业官网建设流程全解析", sections 1 and 3.3).
+ * lr_override: NULL, or a HOST array of n_groups learning rates that
+ * replaces the groups' lr for this step only (for an LR schedule). */
+int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream);
+
+/* Frees the library's scratch (waits for the device); the caller's buffers
+ * are untouched.  NULL is accepted. */
+int bf16opt_destroy(bf16opt_t *h);
+
+/* Step counter t (number of completed bf16opt_step calls), for checkpoint
+ * and resume: restore the caller's buffers and set_step(t) to continue. */
+int bf16opt_get_step(const bf16opt_t *h, int64_t *t);
+int bf16opt_set_step(bf16opt_t *h, int64_t t);
+
+/* Static message of a status code; one-line message of the handle's last error. */
+const char *bf16opt_error_string(int code);
+const char *bf16opt_last_error(const bf16opt_t *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BF16OPT_H */

@@ -1,0 +1,35 @@
+"""Builds libbf16opt.so (the C-ABI library and its sm_103a kernels) in place."""
+import os
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+LIB_PATH = os.path.join(HERE, "libbf16opt.so")
+SOURCES = [os.path.join(HERE, "csrc", "bf16opt.cu")]
+DEPS = SOURCES + [os.path.join(HERE, "csrc", "kernels.cuh"), os.path.join(ROOT, "include", "bf16opt.h")]
+
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
+              "-Xcompiler", "-fPIC", "-shared"]
+
+
+def nvcc():
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _stale(out, deps):
+    if not os.path.exists(out):
+        return True
+    t = os.path.getmtime(out)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build_cmd(extra=()):
+    return [nvcc()] + NVCC_FLAGS + list(extra) + ["-I", os.path.join(ROOT, "include"), "-o", LIB_PATH] + SOURCES
+
+
+def build(force=False, extra=()):
+    """Compile libbf16opt.so for sm_103a if missing or older than its sources."""
+    if force or _stale(LIB_PATH, DEPS):
+        subprocess.run(build_cmd(extra), check=True)
+    return LIB_PATH

@@ -1,0 +1,522 @@
+// bf16opt.cu -- host side of the C ABI declared in include/bf16opt.h.
+//
+// Validates descriptors, builds the segment and chunk tables once on the
+// device, keeps the accumulate -> grad_norm -> step sequence, computes the
+// per-step AdamW scalars in FP64 on the host and launches the kernels of
+// kernels.cuh on the caller's stream.  No CPU fallback: every element of the
+// path is computed by those kernels.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <algorithm>
+#include <vector>
+
+#include "../../include/bf16opt.h"
+#include "kernels.cuh"
+
+using namespace bf16k;
+
+namespace {
+
+enum State { S_IDLE = 0, S_ACC, S_ACC_DONE, S_ACC_DEFERRED, S_NORMED };
+
+struct Batch {
+    uint32_t c0, c1;          // chunk range
+    uint32_t slot0, nslots;   // LIST: tensors [slot0, slot0 + nslots)
+};
+
+thread_local std::string g_create_error;
+
+}  // namespace
+
+struct bf16opt {
+    int device = 0;
+    int mode = BF16OPT_FLAT;
+    uint64_t n = 0;
+    uint32_t n_tensors = 0;
+    std::vector<Seg> segs;
+    std::vector<Batch> batches;
+    uint32_t n_chunks = 0;
+    Seg *segs_d = nullptr;
+    Chunk *chunks_d = nullptr;
+    double *partials_d = nullptr;
+    NormState *norm_d = nullptr;
+    std::vector<bf16opt_group_t> groups;
+    float max_norm = 1.0f;
+    float gscale = 1.0f;
+    int64_t t = 0;
+    State state = S_IDLE;
+    bool deferred = false;               // LAST|DEFER: the step re-reads the last micro-batch
+    bool defer_with_acc = false;         // ... and adds it to acc (micro-batches 0..G-2)
+    bool partials_ready = false;
+    const uint16_t *defer_flat = nullptr;
+    std::vector<const uint16_t *> defer_list;
+    int sm_count = 0;
+    std::string last_error;
+};
+
+namespace {
+
+int fail(bf16opt_t *h, int code, const std::string &msg) {
+    if (h) h->last_error = msg;
+    else g_create_error = msg;
+    return code;
+}
+
+int cuda_fail(bf16opt_t *h, cudaError_t e, const char *what) {
+    return fail(h, BF16OPT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+int check_group(const bf16opt_group_t &g, uint32_t i, std::string &msg) {
+    char buf[160];
+    if (!finite_f(g.lr) || g.lr < 0.f) { snprintf(buf, sizeof buf, "group %u: lr must be finite and >= 0", i); msg = buf; return -1; }
+    if (!(g.beta1 >= 0.f && g.beta1 < 1.f) || !(g.beta2 >= 0.f && g.beta2 < 1.f)) {
+        snprintf(buf, sizeof buf, "group %u: betas must lie in [0, 1)", i); msg = buf; return -1;
+    }
+    if (!finite_f(g.eps) || !(g.eps > 0.f)) { snprintf(buf, sizeof buf, "group %u: eps must be finite and > 0", i); msg = buf; return -1; }
+    if (!finite_f(g.weight_decay) || g.weight_decay < 0.f) {
+        snprintf(buf, sizeof buf, "group %u: weight_decay must be finite and >= 0", i); msg = buf; return -1;
+    }
+    return 0;
+}
+
+struct Interval {
+    uintptr_t lo, hi;
+};
+
+bool overlaps(std::vector<Interval> &iv) {
+    std::sort(iv.begin(), iv.end(), [](const Interval &a, const Interval &b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].lo < iv[i - 1].hi) return true;
+    return false;
+}
+
+bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
+bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
+
+template <class K>
+int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
+    return (int)std::max<uint64_t>(1, std::min<uint64_t>(g, nchunks));
+}
+
+// Launch one accumulate-family pass over every batch.
+template <int SRC, bool WRITE, bool NORM>
+int launch_accum(bf16opt_t *h, const uint16_t *gflat, const uint16_t *const *glist, cudaStream_t st) {
+    constexpr int U = 8;
+    if (h->n_chunks == 0) return 0;
+    if (h->mode == BF16OPT_FLAT) {
+        auto k = k_accum<SRC, WRITE, NORM, FlatGrads, U>;
+        FlatGrads gt{gflat};
+        k<<<grid_for(h, k, h->n_chunks), kThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks, gt,
+                                                               h->partials_d, h->gscale);
+    } else {
+        auto k = k_accum<SRC, WRITE, NORM, ListGrads, U>;
+        for (const Batch &b : h->batches) {
+            if (b.c1 == b.c0) continue;
+            ListGrads gt;
+            gt.slot_base = b.slot0;
+            gt.pad = 0;
+            for (uint32_t i = 0; i < (uint32_t)kListSlots; ++i)
+                gt.ptr[i] = (glist && i < b.nslots) ? glist[b.slot0 + i] : nullptr;
+            k<<<grid_for(h, k, b.c1 - b.c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1, gt,
+                                                                   h->partials_d, h->gscale);
+        }
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : cuda_fail(h, e, "accumulate kernel launch");
+}
+
+template <int SRC>
+int launch_step(bf16opt_t *h, const GroupTable &gtab, cudaStream_t st) {
+    constexpr int U = 4;
+    if (h->n_chunks == 0) return 0;
+    if (h->mode == BF16OPT_FLAT) {
+        auto k = k_step<SRC, FlatGrads, U>;
+        FlatGrads gt{h->defer_flat};
+        k<<<grid_for(h, k, h->n_chunks), kThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks, gt, gtab,
+                                                               h->norm_d, h->gscale);
+    } else {
+        auto k = k_step<SRC, ListGrads, U>;
+        for (const Batch &b : h->batches) {
+            if (b.c1 == b.c0) continue;
+            ListGrads gt;
+            gt.slot_base = b.slot0;
+            gt.pad = 0;
+            for (uint32_t i = 0; i < (uint32_t)kListSlots; ++i)
+                gt.ptr[i] = (!h->defer_list.empty() && i < b.nslots) ? h->defer_list[b.slot0 + i] : nullptr;
+            k<<<grid_for(h, k, b.c1 - b.c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1, gt, gtab,
+                                                                   h->norm_d, h->gscale);
+        }
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : cuda_fail(h, e, "step kernel launch");
+}
+
+void free_scratch(bf16opt_t *h) {
+    if (h->segs_d) cudaFree(h->segs_d);
+    if (h->chunks_d) cudaFree(h->chunks_d);
+    if (h->partials_d) cudaFree(h->partials_d);
+    if (h->norm_d) cudaFree(h->norm_d);
+    h->segs_d = nullptr;
+    h->chunks_d = nullptr;
+    h->partials_d = nullptr;
+    h->norm_d = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bf16opt_error_string(int code) {
+    switch (code) {
+    case BF16OPT_OK: return "ok";
+    case BF16OPT_WARN_NONFINITE: return "gradient norm is not finite";
+    case BF16OPT_ERR_INVALID_ARG: return "invalid argument";
+    case BF16OPT_ERR_ALIGNMENT: return "misaligned pointer";
+    case BF16OPT_ERR_SEQUENCE: return "call out of sequence (accumulate FIRST..LAST -> grad_norm -> step)";
+    case BF16OPT_ERR_OOM: return "out of device memory";
+    case BF16OPT_ERR_CUDA: return "CUDA error";
+    case BF16OPT_ERR_UNSUPPORTED: return "unsupported (no usable CUDA device)";
+    default: return "unknown status";
+    }
+}
+
+const char *bf16opt_last_error(const bf16opt_t *h) {
+    return h ? h->last_error.c_str() : g_create_error.c_str();
+}
+
+int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
+    if (out) *out = nullptr;
+    if (!d || !out) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "desc and out must be non-NULL");
+    if (d->mode != BF16OPT_FLAT && d->mode != BF16OPT_LIST)
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "mode must be BF16OPT_FLAT or BF16OPT_LIST");
+    if (d->n_groups < 1 || d->n_groups > (uint32_t)kMaxGroups || !d->groups)
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "n_groups must be in [1, 16] with a groups array");
+    std::string msg;
+    for (uint32_t i = 0; i < d->n_groups; ++i)
+        if (check_group(d->groups[i], i, msg)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, msg);
+    if (!finite_f(d->max_grad_norm)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "max_grad_norm must be finite");
+    if (!finite_f(d->grad_scale) || d->grad_scale == 0.f)
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "grad_scale must be finite and non-zero");
+
+    std::vector<Seg> segs;
+    std::vector<Interval> iv;
+    uint32_t n_slots = 0;
+    if (d->mode == BF16OPT_FLAT) {
+        const uint64_t n = d->n;
+        if (n > 0) {
+            if (!d->master || !d->exp_avg || !d->exp_avg_sq || !d->grad_accum || !d->param_bf16)
+                return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "FLAT: all five buffers must be non-NULL");
+            if (mis4(d->master) || mis4(d->exp_avg) || mis4(d->exp_avg_sq) || mis4(d->grad_accum) || mis2(d->param_bf16))
+                return fail(nullptr, BF16OPT_ERR_ALIGNMENT, "FLAT: FP32 buffers need 4-B and bf16 2-B alignment");
+            if (n > (UINT64_MAX / 8)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "FLAT: n too large");
+            iv.push_back({(uintptr_t)d->master, (uintptr_t)d->master + 4 * n});
+            iv.push_back({(uintptr_t)d->exp_avg, (uintptr_t)d->exp_avg + 4 * n});
+            iv.push_back({(uintptr_t)d->exp_avg_sq, (uintptr_t)d->exp_avg_sq + 4 * n});
+            iv.push_back({(uintptr_t)d->grad_accum, (uintptr_t)d->grad_accum + 4 * n});
+            iv.push_back({(uintptr_t)d->param_bf16, (uintptr_t)d->param_bf16 + 2 * n});
+        }
+        std::vector<bf16opt_range_t> ranges;
+        if (d->n_ranges == 0 || !d->ranges) {
+            if (d->n_ranges != 0) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "FLAT: n_ranges > 0 with NULL ranges");
+            ranges.push_back({0, n, 0, 0});
+        } else {
+            ranges.assign(d->ranges, d->ranges + d->n_ranges);
+        }
+        uint64_t expect = 0;
+        for (size_t i = 0; i < ranges.size(); ++i) {
+            const bf16opt_range_t &r = ranges[i];
+            if (r.begin != expect || r.end < r.begin || r.end > n || r.group >= d->n_groups || r.reserved != 0)
+                return fail(nullptr, BF16OPT_ERR_INVALID_ARG,
+                            "FLAT: ranges must tile [0, n) in order with valid groups (range " + std::to_string(i) + ")");
+            expect = r.end;
+            if (r.end > r.begin) {
+                Seg s;
+                s.acc = d->grad_accum + r.begin;
+                s.p = d->master + r.begin;
+                s.m = d->exp_avg + r.begin;
+                s.v = d->exp_avg_sq + r.begin;
+                s.bf = d->param_bf16 + r.begin;
+                s.numel = r.end - r.begin;
+                s.grad_off = r.begin;
+                s.grad_slot = 0;
+                s.group = r.group;
+                segs.push_back(s);
+            }
+        }
+        if (expect != n) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "FLAT: ranges do not cover [0, n)");
+        n_slots = 1;
+    } else {
+        if (d->n_tensors > 0 && !d->tensors) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "LIST: tensors is NULL");
+        for (uint32_t i = 0; i < d->n_tensors; ++i) {
+            const bf16opt_tensor_t &t = d->tensors[i];
+            const std::string at = "LIST: tensor " + std::to_string(i);
+            if (t.group >= d->n_groups || t.reserved != 0) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, at + ": bad group");
+            if (t.numel == 0) continue;
+            if (t.numel > (UINT64_MAX / 8)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, at + ": numel too large");
+            if (!t.master || !t.exp_avg || !t.exp_avg_sq || !t.grad_accum || !t.param_bf16)
+                return fail(nullptr, BF16OPT_ERR_INVALID_ARG, at + ": NULL buffer");
+            if (mis4(t.master) || mis4(t.exp_avg) || mis4(t.exp_avg_sq) || mis4(t.grad_accum) || mis2(t.param_bf16))
+                return fail(nullptr, BF16OPT_ERR_ALIGNMENT, at + ": FP32 buffers need 4-B and bf16 2-B alignment");
+            iv.push_back({(uintptr_t)t.master, (uintptr_t)t.master + 4 * t.numel});
+            iv.push_back({(uintptr_t)t.exp_avg, (uintptr_t)t.exp_avg + 4 * t.numel});
+            iv.push_back({(uintptr_t)t.exp_avg_sq, (uintptr_t)t.exp_avg_sq + 4 * t.numel});
+            iv.push_back({(uintptr_t)t.grad_accum, (uintptr_t)t.grad_accum + 4 * t.numel});
+            iv.push_back({(uintptr_t)t.param_bf16, (uintptr_t)t.param_bf16 + 2 * t.numel});
+            Seg s;
+            s.acc = t.grad_accum;
+            s.p = t.master;
+            s.m = t.exp_avg;
+            s.v = t.exp_avg_sq;
+            s.bf = t.param_bf16;
+            s.numel = t.numel;
+            s.grad_off = 0;
+            s.grad_slot = i;
+            s.group = t.group;
+            segs.push_back(s);
+        }
+        n_slots = d->n_tensors;
+    }
+    if (overlaps(iv)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "state buffers overlap");
+
+    // Chunk table and launch batches (LIST: at most kListSlots tensors per launch).
+    std::vector<Chunk> chunks;
+    std::vector<Batch> batches;
+    {
+        Batch cur{0, 0, 0, 0};
+        for (uint32_t si = 0; si < segs.size(); ++si) {
+            const Seg &s = segs[si];
+            if (d->mode == BF16OPT_LIST && s.grad_slot - cur.slot0 >= (uint32_t)kListSlots) {
+                cur.c1 = (uint32_t)chunks.size();
+                cur.nslots = s.grad_slot - cur.slot0;
+                batches.push_back(cur);
+                cur = Batch{(uint32_t)chunks.size(), 0, s.grad_slot, 0};
+            }
+            for (uint64_t off = 0; off < s.numel; off += kChunk) {
+                if (chunks.size() >= 0xffffffffull)
+                    return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
+                chunks.push_back({off, si, (uint32_t)std::min<uint64_t>(kChunk, s.numel - off)});
+            }
+        }
+        cur.c1 = (uint32_t)chunks.size();
+        cur.nslots = n_slots - cur.slot0;
+        batches.push_back(cur);
+    }
+
+    // Device and scratch.
+    int dev = 0, ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+        cudaGetLastError();
+        return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "no CUDA device");
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "cudaGetDevice failed");
+
+    bf16opt_t *h = new (std::nothrow) bf16opt_t();
+    if (!h) return fail(nullptr, BF16OPT_ERR_OOM, "host allocation failed");
+    h->device = dev;
+    h->mode = d->mode;
+    h->n = d->mode == BF16OPT_FLAT ? d->n : 0;
+    h->n_tensors = d->mode == BF16OPT_LIST ? d->n_tensors : 0;
+    h->segs = segs;
+    h->batches = batches;
+    h->n_chunks = (uint32_t)chunks.size();
+    h->groups.assign(d->groups, d->groups + d->n_groups);
+    h->max_norm = d->max_grad_norm;
+    h->gscale = d->grad_scale;
+    if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || h->sm_count < 1)
+        h->sm_count = 1;
+
+    cudaError_t e = cudaSuccess;
+    const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());
+    if ((e = cudaMalloc(&h->segs_d, nseg * sizeof(Seg))) != cudaSuccess ||
+        (e = cudaMalloc(&h->chunks_d, nch * sizeof(Chunk))) != cudaSuccess ||
+        (e = cudaMalloc(&h->partials_d, nch * sizeof(double))) != cudaSuccess ||
+        (e = cudaMalloc(&h->norm_d, sizeof(NormState))) != cudaSuccess) {
+        free_scratch(h);
+        delete h;
+        cudaGetLastError();
+        return fail(nullptr, e == cudaErrorMemoryAllocation ? BF16OPT_ERR_OOM : BF16OPT_ERR_CUDA,
+                    std::string("scratch allocation: ") + cudaGetErrorString(e));
+    }
+    if ((!segs.empty() && (e = cudaMemcpy(h->segs_d, segs.data(), segs.size() * sizeof(Seg), cudaMemcpyHostToDevice)) != cudaSuccess) ||
+        (!chunks.empty() && (e = cudaMemcpy(h->chunks_d, chunks.data(), chunks.size() * sizeof(Chunk), cudaMemcpyHostToDevice)) != cudaSuccess) ||
+        (e = cudaMemset(h->norm_d, 0, sizeof(NormState))) != cudaSuccess) {
+        free_scratch(h);
+        delete h;
+        return fail(nullptr, BF16OPT_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
+    }
+    g_create_error.clear();
+    *out = h;
+    return BF16OPT_OK;
+}
+
+int bf16opt_destroy(bf16opt_t *h) {
+    if (!h) return BF16OPT_OK;
+    DeviceGuard dg(h->device);
+    cudaDeviceSynchronize();
+    free_scratch(h);
+    delete h;
+    return BF16OPT_OK;
+}
+
+int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
+    if (!h || !t) return BF16OPT_ERR_INVALID_ARG;
+    *t = h->t;
+    return BF16OPT_OK;
+}
+
+int bf16opt_set_step(bf16opt_t *h, int64_t t) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (t < 0) return fail(h, BF16OPT_ERR_INVALID_ARG, "step must be >= 0");
+    h->t = t;
+    return BF16OPT_OK;
+}
+
+int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list, unsigned flags,
+                       void *stream) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    const bool first = flags & BF16OPT_FIRST, last = flags & BF16OPT_LAST, defer = flags & BF16OPT_DEFER;
+    if (flags & ~(BF16OPT_FIRST | BF16OPT_LAST | BF16OPT_DEFER)) return fail(h, BF16OPT_ERR_INVALID_ARG, "unknown flag");
+    if (defer && !last) return fail(h, BF16OPT_ERR_INVALID_ARG, "BF16OPT_DEFER needs BF16OPT_LAST");
+    if (!first && h->state != S_ACC) return fail(h, BF16OPT_ERR_SEQUENCE, "accumulate without FIRST outside an accumulation");
+    if (h->mode == BF16OPT_FLAT) {
+        if (grad_list) return fail(h, BF16OPT_ERR_INVALID_ARG, "FLAT: grad_list must be NULL");
+        if (h->n > 0 && !grad_flat) return fail(h, BF16OPT_ERR_INVALID_ARG, "FLAT: grad_flat is NULL");
+        if (mis2(grad_flat)) return fail(h, BF16OPT_ERR_ALIGNMENT, "grad_flat must be 2-B aligned");
+    } else {
+        if (grad_flat) return fail(h, BF16OPT_ERR_INVALID_ARG, "LIST: grad_flat must be NULL");
+        if (h->n_tensors > 0 && !grad_list) return fail(h, BF16OPT_ERR_INVALID_ARG, "LIST: grad_list is NULL");
+        for (const Seg &s : h->segs) {
+            const uint16_t *g = grad_list[s.grad_slot];
+            if (!g) return fail(h, BF16OPT_ERR_INVALID_ARG, "LIST: NULL gradient pointer for tensor " + std::to_string(s.grad_slot));
+            if (mis2(g)) return fail(h, BF16OPT_ERR_ALIGNMENT, "LIST: gradient pointers must be 2-B aligned");
+        }
+    }
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc = 0;
+    if (!last) {
+        rc = first ? launch_accum<SRC_G, true, false>(h, grad_flat, grad_list, st)
+                   : launch_accum<SRC_AG, true, false>(h, grad_flat, grad_list, st);
+    } else if (!defer) {
+        rc = first ? launch_accum<SRC_G, true, true>(h, grad_flat, grad_list, st)
+                   : launch_accum<SRC_AG, true, true>(h, grad_flat, grad_list, st);
+    } else {
+        rc = first ? launch_accum<SRC_G, false, true>(h, grad_flat, grad_list, st)
+                   : launch_accum<SRC_AG, false, true>(h, grad_flat, grad_list, st);
+    }
+    if (rc) return rc;
+    h->deferred = false;
+    h->defer_flat = nullptr;
+    h->defer_list.clear();
+    if (!last) {
+        h->state = S_ACC;
+        h->partials_ready = false;
+    } else if (!defer) {
+        h->state = S_ACC_DONE;
+        h->partials_ready = true;
+    } else {
+        h->state = S_ACC_DEFERRED;
+        h->partials_ready = true;
+        h->deferred = true;
+        h->defer_with_acc = !first;
+        h->defer_flat = grad_flat;
+        if (h->mode == BF16OPT_LIST) h->defer_list.assign(grad_list, grad_list + h->n_tensors);
+    }
+    return BF16OPT_OK;
+}
+
+int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
+        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm needs a completed accumulation");
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!h->partials_ready) {
+        int rc = launch_accum<SRC_A, false, true>(h, nullptr, nullptr, st);
+        if (rc) return rc;
+    }
+    k_norm_final<<<1, kFinalThreads, 0, st>>>(h->partials_d, h->n_chunks, h->max_norm, h->norm_d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");
+    h->partials_ready = true;
+    h->state = S_NORMED;
+    if (host_norm) {
+        double nrm = 0.0;
+        if ((e = cudaMemcpyAsync(&nrm, &h->norm_d->norm, sizeof(double), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+            (e = cudaStreamSynchronize(st)) != cudaSuccess)
+            return cuda_fail(h, e, "reading the norm");
+        *host_norm = nrm;
+        if (!std::isfinite(nrm)) {
+            h->last_error = "gradient norm is not finite";
+            return BF16OPT_WARN_NONFINITE;
+        }
+    }
+    return BF16OPT_OK;
+}
+
+int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (h->state != S_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "step needs grad_norm first");
+    const int64_t t = h->t + 1;
+    GroupTable gtab;
+    memset(&gtab, 0, sizeof gtab);
+    for (size_t i = 0; i < h->groups.size(); ++i) {
+        const bf16opt_group_t &g = h->groups[i];
+        const double lr = lr_override ? (double)lr_override[i] : (double)g.lr;
+        if (!std::isfinite(lr) || lr < 0.0) return fail(h, BF16OPT_ERR_INVALID_ARG, "lr_override must be finite and >= 0");
+        const double b1 = g.beta1, b2 = g.beta2;
+        const double bc1 = 1.0 - std::pow(b1, (double)t);
+        const double bc2 = 1.0 - std::pow(b2, (double)t);
+        GroupK &k = gtab.g[i];
+        k.b1 = (float)b1;
+        k.omb1 = (float)(1.0 - b1);
+        k.b2 = (float)b2;
+        k.omb2 = (float)(1.0 - b2);
+        k.eps = g.eps;
+        k.decay = (float)(lr * (double)g.weight_decay);
+        k.step_size = (float)(lr / bc1);
+        k.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    }
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc;
+    if (h->deferred) {
+        rc = h->defer_with_acc ? launch_step<SRC_AG>(h, gtab, st) : launch_step<SRC_G>(h, gtab, st);
+    } else {
+        rc = launch_step<SRC_A>(h, gtab, st);
+    }
+    if (rc) return rc;
+    h->t = t;
+    h->state = S_IDLE;
+    h->deferred = false;
+    h->defer_flat = nullptr;
+    h->defer_list.clear();
+    h->partials_ready = false;
+    return BF16OPT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,368 @@
+// kernels.cuh -- sm_103a kernels of the BF16 mixed-precision optimizer step.
+//
+// Three bandwidth-bound kernels (no tensor cores: nothing here is a
+// contraction) over a table of chunks:
+//   k_accum        bf16 micro-batch gradient -> FP32 accumulator, optionally with
+//                  the per-chunk partial sums of squares of the global norm fused in
+//                  ("BLOOM 176B 训练技术概览", section "BF16 优化器": FP32 accumulation of
+//                  gradients across pipeline micro-batches);
+//   k_norm_final   fixed-order FP64 sum of the chunk partials, norm and clip
+//                  coefficient ("企业官网建设流程全解析" (cf-1.com), section 4.3: global
+//                  norm clipped at 1.0);
+//   k_step         clip x AdamW x FP32 master/moment update x bf16 cast in one pass
+//                  ("企业官网建设流程全解析", sections 1 and 3.3).
+//
+// Work decomposition.  A segment is one run of elements with one parameter
+// group and one set of base pointers (a flat range or a list tensor).  Each
+// segment is cut into chunks of kChunk elements; a persistent grid strides over
+// the chunks.  Inside a chunk, thread t handles 4-element quads t, t+T, ...
+// so that every warp-wide access is contiguous: FP32 as 16-byte and bf16 as
+// 8-byte vectors.  Leading elements up to the first 16-byte-aligned FP32
+// address, and the ragged tail, are done one element at a time.  If the
+// buffers of a segment do not share their offset modulo 16 bytes the whole
+// chunk runs element-wise (correct, slower).
+//
+// Determinism.  The norm's partial of chunk c depends only on the chunk's
+// data and on the fixed thread->element map, so the result does not depend
+// on the grid size or on scheduling; the final sum runs in chunk order.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bf16k {
+
+constexpr int kThreads = 256;        // threads per CTA
+constexpr uint32_t kChunk = 16384;   // elements per chunk (multiple of 4)
+constexpr int kMaxGroups = 16;
+constexpr int kListSlots = 1024;     // gradient pointers per LIST-mode launch
+constexpr int kFinalThreads = 1024;
+
+struct Seg {
+    float *acc, *p, *m, *v;   // already offset to the segment's first element
+    uint16_t *bf;
+    uint64_t numel;
+    uint64_t grad_off;        // element offset of the segment in its gradient buffer
+    uint32_t grad_slot;       // which per-call gradient pointer
+    uint32_t group;
+};
+
+struct Chunk {
+    uint64_t start;           // first element, relative to the segment
+    uint32_t seg;
+    uint32_t len;
+};
+
+struct NormState {
+    double sumsq;             // sum of squares of the (scaled) accumulated gradient
+    double norm;              // sqrt(sumsq)
+    float c_hi, c_lo;         // clip coefficient c = c_hi + c_lo (float-float)
+    int32_t finite;
+    int32_t pad;
+};
+
+// Per-group scalars of one step, FP32, precomputed on the host in FP64.
+struct GroupK {
+    float b1, omb1, b2, omb2;
+    float eps;
+    float decay;              // lr * weight_decay
+    float step_size;          // lr / (1 - b1^t)
+    float inv_sqrt_bc2;       // 1 / sqrt(1 - b2^t)
+};
+struct GroupTable {
+    GroupK g[kMaxGroups];
+};
+
+// Gradient sources passed by value as kernel parameters.
+struct FlatGrads {
+    const uint16_t *base;
+    __device__ __forceinline__ const uint16_t *get(uint32_t) const { return base; }
+};
+struct ListGrads {
+    uint32_t slot_base;
+    uint32_t pad;
+    const uint16_t *ptr[kListSlots];
+    __device__ __forceinline__ const uint16_t *get(uint32_t s) const { return ptr[s - slot_base]; }
+};
+
+enum Src { SRC_G = 0, SRC_AG = 1, SRC_A = 2 };  // value = g | acc + g | acc
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Compensated sum of squares in FP32: x*x split exactly into p + e (fma), p
+// added by TwoSum (Knuth; Ogita, Rump & Oishi, "Accurate sum and dot
+// product", SIAM J. Sci. Comput. 26(6), 2005).  The _rn intrinsics keep
+// the compiler from contracting the error-free transformations into FMAs.
+struct Comp {
+    float s, c;
+};
+__device__ __forceinline__ void comp_add_sq(Comp &a, float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);
+    const float t = __fadd_rn(a.s, p);
+    const float bp = __fsub_rn(t, a.s);
+    const float err = __fadd_rn(__fsub_rn(a.s, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    a.s = t;
+    a.c = __fadd_rn(a.c, __fadd_rn(err, e));
+}
+
+// Deterministic CTA sum of one double per thread; result valid in thread 0.
+__device__ __forceinline__ double cta_sum(double x, double *sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) sh[w] = x;
+    __syncthreads();
+    double r = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) r += sh[i];
+    }
+    __syncthreads();
+    return r;
+}
+
+// Leading element count until a pointer's FP32/bf16 element index is a
+// multiple of 4 (16-byte FP32 / 8-byte bf16 boundary).
+__device__ __forceinline__ uint32_t phase4_f32(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) & 3u); }
+__device__ __forceinline__ uint32_t phase4_b16(const void *p) { return (uint32_t)(((uintptr_t)p >> 1) & 3u); }
+
+// ---------------------------------------------------------------- accumulate
+
+// One pass over chunks [c0, c1): value = g | acc + g | acc (SRC), stored back
+// to acc if WRITE, and its per-chunk sum of squares (times gscale, rounded to
+// FP32 first) written to partials[c] if NORM.
+template <int SRC, bool WRITE, bool NORM, class GT, int U>
+__global__ void __launch_bounds__(kThreads)
+k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
+        double *__restrict__ partials, float gscale) {
+    __shared__ double sh[kThreads / 32];
+    constexpr bool kReadG = SRC != SRC_A;
+    constexpr bool kReadA = SRC != SRC_G;
+    constexpr bool kUseA = kReadA || WRITE;
+    for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        const Seg s = segs[ch.seg];
+        float *a = s.acc + ch.start;
+        const uint16_t *g = kReadG ? gt.get(s.grad_slot) + s.grad_off + ch.start : nullptr;
+        const uint32_t len = ch.len;
+
+        uint32_t ph = 0;
+        bool vec = true;
+        if (kReadG) ph = phase4_b16(g);
+        if (kUseA) {
+            const uint32_t pa = phase4_f32(a);
+            if (kReadG && pa != ph) vec = false;
+            ph = pa;
+        }
+        uint32_t head = vec ? ((4u - ph) & 3u) : len;
+        if (head > len) head = len;
+        const uint32_t nq = (len - head) >> 2;
+        const uint32_t tail0 = head + (nq << 2);
+
+        Comp cs = {0.f, 0.f};
+        auto scalar = [&](uint32_t i) {
+            float val;
+            if (SRC == SRC_G) val = __uint_as_float((uint32_t)g[i] << 16);
+            else if (SRC == SRC_AG) val = __fadd_rn(a[i], __uint_as_float((uint32_t)g[i] << 16));
+            else val = a[i];
+            if (WRITE) a[i] = val;
+            if (NORM) comp_add_sq(cs, __fmul_rn(val, gscale));
+        };
+        for (uint32_t i = threadIdx.x; i < head; i += kThreads) scalar(i);
+        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) scalar(i);
+
+        const uint2 *g4 = reinterpret_cast<const uint2 *>(g + head);
+        float4 *a4 = reinterpret_cast<float4 *>(a + head);
+        for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
+            uint2 gv[U];
+            float4 av[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) {
+                    if (kReadG) gv[u] = __ldcs(g4 + j);
+                    if (kReadA) av[u] = __ldcs(a4 + j);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) {
+                    float4 r;
+                    if (SRC == SRC_G) {
+                        r = make_float4(bf_lo(gv[u].x), bf_hi(gv[u].x), bf_lo(gv[u].y), bf_hi(gv[u].y));
+                    } else if (SRC == SRC_AG) {
+                        r = make_float4(__fadd_rn(av[u].x, bf_lo(gv[u].x)), __fadd_rn(av[u].y, bf_hi(gv[u].x)),
+                                        __fadd_rn(av[u].z, bf_lo(gv[u].y)), __fadd_rn(av[u].w, bf_hi(gv[u].y)));
+                    } else {
+                        r = av[u];
+                    }
+                    if (WRITE) __stcs(a4 + j, r);
+                    if (NORM) {
+                        comp_add_sq(cs, __fmul_rn(r.x, gscale));
+                        comp_add_sq(cs, __fmul_rn(r.y, gscale));
+                        comp_add_sq(cs, __fmul_rn(r.z, gscale));
+                        comp_add_sq(cs, __fmul_rn(r.w, gscale));
+                    }
+                }
+            }
+        }
+        if (NORM) {
+            const double tot = cta_sum((double)cs.s + (double)cs.c, sh);
+            if (threadIdx.x == 0) partials[c] = tot;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- norm final
+
+// Sum of the chunk partials in a fixed order, then norm = sqrt(S) and
+// c = max_norm / norm if norm > max_norm (max_norm > 0), else 1.
+__global__ void __launch_bounds__(kFinalThreads)
+k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out) {
+    __shared__ double sh[kFinalThreads];
+    double s = 0.0;
+    for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) s += partials[i];
+    sh[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = kFinalThreads / 2; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double S = sh[0];
+        const double norm = sqrt(S);
+        double c = 1.0;
+        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
+        const float hi = __double2float_rn(c);
+        out->sumsq = S;
+        out->norm = norm;
+        out->c_hi = hi;
+        out->c_lo = __double2float_rn(c - (double)hi);
+        out->finite = isfinite(S) ? 1 : 0;
+        out->pad = 0;
+    }
+}
+
+// ---------------------------------------------------------------------- step
+
+struct AdamOut {
+    float p, m, v;
+};
+
+__device__ __forceinline__ AdamOut adam_elem(float e, float p, float m, float v, float c_hi, float c_lo,
+                                             const GroupK &G) {
+    const float gc = fmaf(e, c_hi, e * c_lo);                 // clipped gradient
+    const float m1 = fmaf(G.b1, m, G.omb1 * gc);
+    const float v1 = fmaf(G.b2, v, G.omb2 * gc * gc);
+    const float den = fmaf(sqrtf(v1), G.inv_sqrt_bc2, G.eps); // sqrt(v_hat) + eps
+    const float upd = __fdiv_rn(m1, den);
+    float p1 = fmaf(-G.decay, p, p);                          // decoupled weight decay
+    p1 = fmaf(-G.step_size, upd, p1);
+    return {p1, m1, v1};
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Fused clip + AdamW + master update + bf16 cast over chunks [c0, c1).
+// SRC_A: the gradient is the stored accumulator; SRC_AG: accumulator plus a
+// deferred last micro-batch g; SRC_G: a single deferred micro-batch.
+template <int SRC, class GT, int U>
+__global__ void __launch_bounds__(kThreads)
+k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
+       GroupTable gtab, const NormState *__restrict__ ns, float gscale) {
+    constexpr bool kReadG = SRC != SRC_A;
+    constexpr bool kReadA = SRC != SRC_G;
+    const float c_hi = ns->c_hi, c_lo = ns->c_lo;
+    for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        const Seg s = segs[ch.seg];
+        const GroupK G = gtab.g[s.group];
+        const float *a = s.acc + ch.start;
+        const uint16_t *g = kReadG ? gt.get(s.grad_slot) + s.grad_off + ch.start : nullptr;
+        float *p = s.p + ch.start;
+        float *m = s.m + ch.start;
+        float *v = s.v + ch.start;
+        uint16_t *bf = s.bf + ch.start;
+        const uint32_t len = ch.len;
+
+        const uint32_t ph = phase4_f32(p);
+        bool vec = phase4_f32(m) == ph && phase4_f32(v) == ph && phase4_b16(bf) == ph;
+        if (kReadA) vec = vec && phase4_f32(a) == ph;
+        if (kReadG) vec = vec && phase4_b16(g) == ph;
+        uint32_t head = vec ? ((4u - ph) & 3u) : len;
+        if (head > len) head = len;
+        const uint32_t nq = (len - head) >> 2;
+        const uint32_t tail0 = head + (nq << 2);
+
+        auto scalar = [&](uint32_t i) {
+            float e;
+            if (SRC == SRC_G) e = __uint_as_float((uint32_t)g[i] << 16);
+            else if (SRC == SRC_AG) e = __fadd_rn(a[i], __uint_as_float((uint32_t)g[i] << 16));
+            else e = a[i];
+            e = __fmul_rn(e, gscale);
+            const AdamOut o = adam_elem(e, p[i], m[i], v[i], c_hi, c_lo, G);
+            p[i] = o.p;
+            m[i] = o.m;
+            v[i] = o.v;
+            bf[i] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
+        };
+        for (uint32_t i = threadIdx.x; i < head; i += kThreads) scalar(i);
+        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) scalar(i);
+
+        const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
+        const uint2 *g4 = reinterpret_cast<const uint2 *>(g + head);
+        float4 *p4 = reinterpret_cast<float4 *>(p + head);
+        float4 *m4 = reinterpret_cast<float4 *>(m + head);
+        float4 *v4 = reinterpret_cast<float4 *>(v + head);
+        uint2 *b4 = reinterpret_cast<uint2 *>(bf + head);
+        for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
+            float4 av[U], pv[U], mv[U], vv[U];
+            uint2 gv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) {
+                    if (kReadA) av[u] = __ldcs(a4 + j);
+                    if (kReadG) gv[u] = __ldcs(g4 + j);
+                    pv[u] = __ldcs(p4 + j);
+                    mv[u] = __ldcs(m4 + j);
+                    vv[u] = __ldcs(v4 + j);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) {
+                    float e[4];
+                    if (SRC == SRC_G) {
+                        e[0] = bf_lo(gv[u].x); e[1] = bf_hi(gv[u].x); e[2] = bf_lo(gv[u].y); e[3] = bf_hi(gv[u].y);
+                    } else if (SRC == SRC_AG) {
+                        e[0] = __fadd_rn(av[u].x, bf_lo(gv[u].x)); e[1] = __fadd_rn(av[u].y, bf_hi(gv[u].x));
+                        e[2] = __fadd_rn(av[u].z, bf_lo(gv[u].y)); e[3] = __fadd_rn(av[u].w, bf_hi(gv[u].y));
+                    } else {
+                        e[0] = av[u].x; e[1] = av[u].y; e[2] = av[u].z; e[3] = av[u].w;
+                    }
+                    const AdamOut o0 = adam_elem(__fmul_rn(e[0], gscale), pv[u].x, mv[u].x, vv[u].x, c_hi, c_lo, G);
+                    const AdamOut o1 = adam_elem(__fmul_rn(e[1], gscale), pv[u].y, mv[u].y, vv[u].y, c_hi, c_lo, G);
+                    const AdamOut o2 = adam_elem(__fmul_rn(e[2], gscale), pv[u].z, mv[u].z, vv[u].z, c_hi, c_lo, G);
+                    const AdamOut o3 = adam_elem(__fmul_rn(e[3], gscale), pv[u].w, mv[u].w, vv[u].w, c_hi, c_lo, G);
+                    __stcs(p4 + j, make_float4(o0.p, o1.p, o2.p, o3.p));
+                    __stcs(m4 + j, make_float4(o0.m, o1.m, o2.m, o3.m));
+                    __stcs(v4 + j, make_float4(o0.v, o1.v, o2.v, o3.v));
+                    __stcs(b4 + j, make_uint2(pack_bf16x2(o0.p, o1.p), pack_bf16x2(o2.p, o3.p)));
+                }
+            }
+        }
+    }
+}
+
+}  // namespace bf16k

@@ -1,0 +1,95 @@
+"""BF16Optimizer: drives the bf16opt C ABI from torch device tensors.
+
+Marshalling only (data_ptr()s, stream handles, status -> exception); all
+arithmetic is in libbf16opt.so.  State layout for one rank's shard:
+
+  FLAT: master, exp_avg, exp_avg_sq, grad_accum (FP32) and param_bf16 (bf16)
+        as five contiguous buffers of n elements, plus group ranges;
+  LIST: the same five buffers per tensor (separate allocations).
+"""
+import torch
+
+from . import bf16opt as C
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else 0
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def alloc_flat(n, device="cuda", misalign=0):
+    """Five state buffers of n elements; each starts `misalign` elements past
+    a 256-byte boundary (the allocator's own alignment is at least that)."""
+    def one(dtype):
+        base = torch.empty(n + misalign + 64, dtype=dtype, device=device)
+        assert base.data_ptr() % 256 == 0
+        return base[misalign:misalign + n]
+    return dict(master=one(torch.float32), exp_avg=one(torch.float32), exp_avg_sq=one(torch.float32),
+                grad_accum=one(torch.float32), param_bf16=one(torch.int16))
+
+
+class BF16Optimizer:
+    """One handle over a FLAT shard (`flat` = dict of the five tensors, `ranges`)
+    or a LIST of tensors (`tensors` = list of such dicts with a "group" key)."""
+
+    def __init__(self, groups, flat=None, ranges=None, tensors=None, max_grad_norm=1.0, grad_scale=1.0):
+        if (flat is None) == (tensors is None):
+            raise ValueError("give exactly one of flat= or tensors=")
+        self.groups = [dict(g) for g in groups]
+        if flat is not None:
+            n = flat["master"].numel()
+            self.desc = C.flat_desc(n, _ptr(flat["master"]), _ptr(flat["exp_avg"]), _ptr(flat["exp_avg_sq"]),
+                                    _ptr(flat["grad_accum"]), _ptr(flat["param_bf16"]), self.groups, ranges,
+                                    max_grad_norm, grad_scale)
+            self.mode = C.BF16OPT_FLAT
+        else:
+            tl = [(_ptr(t["master"]), _ptr(t["exp_avg"]), _ptr(t["exp_avg_sq"]), _ptr(t["grad_accum"]),
+                   _ptr(t["param_bf16"]), t["master"].numel(), int(t.get("group", 0))) for t in tensors]
+            self.desc = C.list_desc(tl, self.groups, max_grad_norm, grad_scale)
+            self.mode = C.BF16OPT_LIST
+        rc, self.h = C.bf16opt_create(self.desc)
+        C.check(rc, None)
+
+    def accumulate(self, grad, first=False, last=False, defer=False, stream=None):
+        """grad: bf16 (int16-viewed) tensor (FLAT) or list of them (LIST)."""
+        flags = (C.BF16OPT_FIRST if first else 0) | (C.BF16OPT_LAST if last else 0) | (C.BF16OPT_DEFER if defer else 0)
+        if self.mode == C.BF16OPT_FLAT:
+            rc = C.bf16opt_accumulate(self.h, _ptr(grad), None, flags, _stream_handle(stream))
+        else:
+            rc = C.bf16opt_accumulate(self.h, 0, [_ptr(g) for g in grad], flags, _stream_handle(stream))
+        return C.check(rc, self.h)
+
+    def grad_norm(self, stream=None, sync=False):
+        rc, norm = C.bf16opt_grad_norm(self.h, _stream_handle(stream), want_norm=sync)
+        C.check(rc, self.h)
+        return norm
+
+    def step(self, lr=None, stream=None):
+        lrs = None if lr is None else ([float(lr)] * len(self.groups) if not hasattr(lr, "__len__") else list(lr))
+        return C.check(C.bf16opt_step(self.h, lrs, _stream_handle(stream)), self.h)
+
+    @property
+    def t(self):
+        rc, t = C.bf16opt_get_step(self.h)
+        C.check(rc, self.h)
+        return t
+
+    @t.setter
+    def t(self, value):
+        C.check(C.bf16opt_set_step(self.h, value), self.h)
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            C.bf16opt_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

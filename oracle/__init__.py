@@ -137,7 +137,7 @@ def run_dense(p, grads_fn, ranges, groups, steps, gas, max_norm, grad_scale=1.0,
     """Full oracle run over materialised host arrays.
 
     p: FP32 masters (updated in place); grads_fn(step, micro) -> uint16 array of
-    the whole buffer; ranges: [(begin, end, group index)] tiling [0, n);
+    the whole buffer, step counted from 0 (step index t0 + s has step number t0 + s + 1); ranges: [(begin, end, group index)] tiling [0, n);
     groups: list of Group.  Returns dict with p, m, v, p_bf16, acc (last step)
     and per-step sumsq / clip lists.
     """
@@ -149,7 +149,7 @@ def run_dense(p, grads_fn, ranges, groups, steps, gas, max_norm, grad_scale=1.0,
     sums, clips = [], []
     for s in range(steps):
         for k in range(gas):
-            accumulate(acc, grads_fn(s, k), first=(k == 0), threads=threads)
+            accumulate(acc, grads_fn(t0 + s, k), first=(k == 0), threads=threads)
         S = sumsq(acc, grad_scale, threads)
         c = clip_coef(S, max_norm)
         sums.append(S)

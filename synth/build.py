@@ -1,10 +1,12 @@
-"""Builds libsynth.so (host C, seeded input generators) in place."""
+"""Builds libsynth.so (host C) and libsynth_gpu.so (sm_103a) in place."""
 import os
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsynth.so")
+GPU_LIB_PATH = os.path.join(HERE, "libsynth_gpu.so")
 SOURCES = [os.path.join(HERE, "synth.c")]
+GPU_SOURCES = [os.path.join(HERE, "synth_gpu.cu")]
 HEADERS = [os.path.join(HERE, "synth.h")]
 
 
@@ -20,8 +22,22 @@ def build_cmd():
             "-o", LIB_PATH] + SOURCES + ["-lm"]
 
 
+def build_gpu_cmd():
+    nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    nvcc = nvcc if os.path.exists(nvcc) else "nvcc"
+    return [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-fmad=false",
+            "-Xcompiler", "-fPIC", "-shared", "-o", GPU_LIB_PATH] + GPU_SOURCES
+
+
 def build(force=False):
     """Compile libsynth.so if missing or older than its sources."""
     if force or _stale(LIB_PATH, SOURCES + HEADERS):
         subprocess.run(build_cmd(), check=True)
     return LIB_PATH
+
+
+def build_gpu(force=False):
+    """Compile libsynth_gpu.so if missing or older than its sources."""
+    if force or _stale(GPU_LIB_PATH, GPU_SOURCES + HEADERS):
+        subprocess.run(build_gpu_cmd(), check=True)
+    return GPU_LIB_PATH

@@ -22,24 +22,30 @@
 #include <stdint.h>
 #include <string.h>
 
+#ifdef __CUDACC__
+#define SYNTH_HD __host__ __device__
+#else
+#define SYNTH_HD
+#endif
+
 #define SYNTH_GAMMA 0x9e3779b97f4a7c15ULL
 
 /* Buffer kinds of a stream key. */
 enum { SYNTH_KIND_GRAD = 1, SYNTH_KIND_MASTER = 2, SYNTH_KIND_ZERO_MASK = 3 };
 
-static inline uint64_t synth_mix64(uint64_t z) {
+static inline SYNTH_HD uint64_t synth_mix64(uint64_t z) {
     z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
     z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
     return z ^ (z >> 31);
 }
 
 /* The i-th 64-bit output of the stream keyed by `key`. */
-static inline uint64_t synth_bits(uint64_t key, uint64_t i) {
+static inline SYNTH_HD uint64_t synth_bits(uint64_t key, uint64_t i) {
     return synth_mix64(key + (i + 1) * SYNTH_GAMMA);
 }
 
 /* Stream key of one buffer: (seed, workload id, kind, step, micro-batch). */
-static inline uint64_t synth_key(uint64_t seed, uint32_t workload, uint32_t kind,
+static inline SYNTH_HD uint64_t synth_key(uint64_t seed, uint32_t workload, uint32_t kind,
                                  uint32_t step, uint32_t micro) {
     uint64_t k = synth_mix64(seed + SYNTH_GAMMA);
     k = synth_mix64(k ^ ((uint64_t)workload << 32 | kind));
@@ -48,7 +54,7 @@ static inline uint64_t synth_key(uint64_t seed, uint32_t workload, uint32_t kind
 }
 
 /* Irwin-Hall(4) integer in [-131070, 131070], mean 0. */
-static inline int32_t synth_ih4(uint64_t h) {
+static inline SYNTH_HD int32_t synth_ih4(uint64_t h) {
     int32_t s = (int32_t)(h & 0xffff) + (int32_t)((h >> 16) & 0xffff) +
                 (int32_t)((h >> 32) & 0xffff) + (int32_t)(h >> 48);
     return s - 131070;
@@ -60,11 +66,11 @@ static inline int32_t synth_ih4(uint64_t h) {
 /* Multiplier that maps synth_ih4 to standard deviation sigma. */
 static inline double synth_scale_for_sigma(double sigma) { return sigma / SYNTH_IH4_STD; }
 
-static inline uint32_t synth_f32_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
-static inline float synth_bits_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static inline SYNTH_HD uint32_t synth_f32_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static inline SYNTH_HD float synth_bits_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
 
 /* ~N(0, sigma) FP32 value: (float)(ih4 * scale), scale = synth_scale_for_sigma(sigma). */
-static inline float synth_normal_f32(uint64_t key, uint64_t i, double scale) {
+static inline SYNTH_HD float synth_normal_f32(uint64_t key, uint64_t i, double scale) {
     return (float)((double)synth_ih4(synth_bits(key, i)) * scale);
 }
 
@@ -73,7 +79,7 @@ static inline float synth_normal_f32(uint64_t key, uint64_t i, double scale) {
  * If zero_thresh != 0, element i is exactly +0 whenever
  * synth_bits(zero_key, i) < zero_thresh (zero_thresh = frac * 2^64), i.e. the
  * same positions are zero in every stream that shares zero_key. */
-static inline uint16_t synth_grad_bf16(uint64_t key, uint64_t i, double scale,
+static inline SYNTH_HD uint16_t synth_grad_bf16(uint64_t key, uint64_t i, double scale,
                                        uint64_t zero_key, uint64_t zero_thresh) {
     if (zero_thresh != 0 && synth_bits(zero_key, i) < zero_thresh) return 0;
     return (uint16_t)(synth_f32_bits(synth_normal_f32(key, i, scale)) >> 16);
@@ -82,7 +88,7 @@ static inline uint16_t synth_grad_bf16(uint64_t key, uint64_t i, double scale,
 /* Log-uniform over binary octaves with random sign: |x| = (1 + f) * 2^e with
  * e uniform in [e_lo, e_hi] and f a uniform 23-bit fraction, built directly
  * as an FP32 bit pattern.  e in [-26, 9] spans [1.49e-8, 1024). */
-static inline float synth_loguniform_f32(uint64_t key, uint64_t i, int e_lo, int e_hi) {
+static inline SYNTH_HD float synth_loguniform_f32(uint64_t key, uint64_t i, int e_lo, int e_hi) {
     uint64_t h = synth_bits(key, i);
     uint32_t n_oct = (uint32_t)(e_hi - e_lo + 1);
     uint32_t e = (uint32_t)((((h >> 32) & 0xffffffffULL) * n_oct) >> 32);   /* [0, n_oct) */

@@ -1,0 +1,241 @@
+"""Parity harness: the CUDA path (through the C ABI) against the CPU oracle.
+
+GPU side: a workload's shard lives in torch device buffers; seeded inputs are
+written by the device generator (synth.gpu, bit-identical to the host one);
+every optimizer call goes through libbf16opt.so.
+Oracle side: the same inputs regenerated on the host; either a dense run over
+the whole shard, or (for shards too large to materialise) the global norm of
+every step streamed from the counters plus whole-run replays of sampled
+elements.
+
+Tolerances (the workload definitions' bar, plainest reading where silent):
+  accumulator    bit-exact;
+  global norm    |n_gpu - n_ref| <= 1e-6 n_ref;
+  m, v, master   |x_gpu - x_ref| <= 1e-6 * max(|x_ref|, s), with the operand
+                 scale s = b1 |m_prev| + (1 - b1) |gc| for m, |v_ref| for v and
+                 max(|p_prev|, lr |m_hat / (sqrt(v_hat) + eps)|) for the master;
+  bf16 param     bit-exact, except <= 1 bf16 ulp where the oracle's FP32 master
+                 lies within 1e-6 (relative) of a bf16 rounding midpoint.
+"""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from synth import gpu as sgpu
+from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat
+
+REL = 1e-6
+
+
+def ogroups(wl):
+    """Oracle groups carry the FP32-rounded hyper-parameters the C ABI receives."""
+    f = lambda x: float(np.float32(x))
+    return [oracle.group(f(g["lr"]), f(g["beta1"]), f(g["beta2"]), f(g["eps"]), f(g["weight_decay"]))
+            for g in wl.groups]
+
+
+def _alloc(n, dtype, misalign, device="cuda"):
+    base = torch.empty(n + misalign + 64, dtype=dtype, device=device)
+    return base[misalign:misalign + n]
+
+
+class GpuShard:
+    """Device state of a workload + its bf16opt handle."""
+
+    def __init__(self, wl, grad_scale=1.0, defer=False):
+        self.wl, self.defer = wl, defer
+        self.norms = []
+        if wl.mode == "flat":
+            self.flat = alloc_flat(wl.n, "cuda", wl.misalign)
+            sgpu.fill_master(wl, self.flat["master"])
+            for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+                self.flat[k].zero_()
+            self.opt = BF16Optimizer(wl.groups, flat=self.flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm,
+                                     grad_scale=grad_scale)
+        else:
+            self.tensors = []
+            master = _alloc(wl.n, torch.float32, 0)
+            sgpu.fill_master(wl, master)
+            for i, (t, off) in enumerate(zip(wl.tensors, wl.offsets)):
+                d = dict(master=_alloc(t.numel, torch.float32, wl.misalign),
+                         exp_avg=_alloc(t.numel, torch.float32, wl.misalign),
+                         exp_avg_sq=_alloc(t.numel, torch.float32, wl.misalign),
+                         grad_accum=_alloc(t.numel, torch.float32, wl.misalign),
+                         param_bf16=_alloc(t.numel, torch.int16, wl.misalign), group=wl.group_of_tensor(i))
+                d["master"].copy_(master[off:off + t.numel])
+                for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+                    d[k].zero_()
+                self.tensors.append(d)
+            del master
+            self.opt = BF16Optimizer(wl.groups, tensors=self.tensors, max_grad_norm=wl.max_norm,
+                                     grad_scale=grad_scale)
+        self.gbuf = _alloc(wl.n, torch.int16, wl.misalign)
+
+    def grads_arg(self):
+        if self.wl.mode == "flat":
+            return self.gbuf
+        return [self.gbuf[off:off + t.numel] for t, off in zip(self.wl.tensors, self.wl.offsets)]
+
+    def run_step(self, step):
+        wl = self.wl
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, step, k, self.gbuf)
+            self.opt.accumulate(self.grads_arg(), first=(k == 0), last=(k == wl.gas - 1),
+                                defer=self.defer and k == wl.gas - 1)
+        norm = self.opt.grad_norm(sync=True)
+        self.opt.step()
+        self.norms.append(norm)
+        return norm
+
+    def run(self, steps):
+        for s in range(steps):
+            self.run_step(s)
+        torch.cuda.synchronize()
+
+    # ---- read back
+    def full(self, name):
+        if self.wl.mode == "flat":
+            t = self.flat[name]
+            return t.cpu().numpy()
+        return np.concatenate([d[name].cpu().numpy() for d in self.tensors])
+
+    def gather(self, name, idx):
+        idx = np.asarray(idx, dtype=np.int64)
+        if self.wl.mode == "flat":
+            t = self.flat[name]
+            return t[torch.from_numpy(idx).to(t.device)].cpu().numpy()
+        tid = self.wl.tensor_of(idx)
+        out = None
+        for ti in np.unique(tid):
+            sel = np.nonzero(tid == ti)[0]
+            loc = idx[sel] - self.wl.offsets[ti]
+            t = self.tensors[ti][name]
+            vals = t[torch.from_numpy(loc).to(t.device)].cpu().numpy()
+            if out is None:
+                out = np.empty(idx.size, vals.dtype)
+            out[sel] = vals
+        return out
+
+    def states(self, idx=None):
+        get = (lambda k: self.full(k)) if idx is None else (lambda k: self.gather(k, idx))
+        return dict(p=get("master"), m=get("exp_avg"), v=get("exp_avg_sq"), acc=get("grad_accum"),
+                    p_bf16=get("param_bf16").view(np.uint16))
+
+    def close(self):
+        self.opt.close()
+
+
+# ------------------------------------------------------------------ oracle side
+
+def oracle_dense(wl, steps, grad_scale=1.0):
+    """Dense oracle run; returns (final, prev) state dicts (prev = after steps-1)."""
+    n = wl.n
+    p0 = synth.fill_master(wl, np.empty(n, np.float32))
+    G = ogroups(wl)
+    gfn = lambda s, k: synth.fill_grad(wl, s, k, np.empty(n, np.uint16))
+    prev = oracle.run_dense(p0.copy(), gfn, wl.ranges(), G, steps - 1, wl.gas, wl.max_norm, grad_scale)
+    prev = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in prev.items()}
+    fin = oracle.run_dense(prev["p"].copy(), gfn, wl.ranges(), G, 1, wl.gas, wl.max_norm, grad_scale,
+                           t0=steps - 1, m=prev["m"].copy(), v=prev["v"].copy())
+    fin["sumsq"] = prev["sumsq"] + fin["sumsq"]
+    fin["clip"] = prev["clip"] + fin["clip"]
+    return fin, prev
+
+
+def oracle_sampled(wl, steps, idx, grad_scale=1.0):
+    """Streamed norms of every step + sampled whole-run replays."""
+    st = oracle.stream(wl.id, wl.gas, synth.sigma_scale(wl.grad_sigma), synth.zero_thresh(wl.zero_frac),
+                       grad_scale)
+    sums = [oracle.stream_sumsq(st, s, wl.n) for s in range(steps)]
+    clips = [oracle.clip_coef(S, wl.max_norm) for S in sums]
+    idx = np.asarray(idx, dtype=np.uint64)
+    p0 = synth.gather_master(wl, idx)
+    G = ogroups(wl)
+    gof = wl.group_of(idx)
+    p, m, v, pb, acc = oracle.sample_run(st, idx, p0, G, gof, clips)
+    if steps > 1:
+        pp, mp, vp, _, _ = oracle.sample_run(st, idx, p0, G, gof, clips[:steps - 1])
+    else:
+        pp, mp, vp = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    fin = dict(p=p, m=m, v=v, p_bf16=pb, acc=acc, sumsq=sums, clip=clips)
+    prev = dict(p=pp, m=mp, v=vp)
+    return fin, prev
+
+
+def sample_indices(wl, k=1 << 15, seed=0):
+    """Random elements plus every tensor's first/last element and chunk edges."""
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, wl.n, size=min(k, wl.n), dtype=np.int64)]
+    edges = []
+    for t, off in zip(wl.tensors, wl.offsets):
+        edges += [off, off + 1, off + t.numel - 1, off + t.numel - 2, off + min(t.numel - 1, 16383),
+                  off + min(t.numel - 1, 16384)]
+    edges += [0, wl.n - 1]
+    idx.append(np.array([e for e in edges if 0 <= e < wl.n], np.int64))
+    return np.unique(np.concatenate(idx))
+
+
+# ------------------------------------------------------------------ comparison
+
+def _bf16_midpoint_close(p_ref):
+    """True where the FP32 value lies within 1e-6 (relative) of a bf16 rounding midpoint."""
+    u = p_ref.view(np.uint32)
+    mid = ((u & 0xFFFF0000) | 0x8000).view(np.float32).astype(np.float64)
+    x = p_ref.astype(np.float64)
+    return np.abs(x - mid) <= REL * np.abs(x)
+
+
+def compare(gpu, ref, prev, wl, t_last, grad_scale=1.0, check_acc=True, gof=None):
+    """Element-wise parity; returns a stats dict, raises AssertionError on a breach."""
+    G = ogroups(wl)
+    n = ref["p"].size
+    gof = np.zeros(n, np.uint32) if gof is None else np.asarray(gof)
+    b1 = np.array([g.beta1 for g in G])[gof]
+    b2 = np.array([g.beta2 for g in G])[gof]
+    lr = np.array([g.lr for g in G])[gof]
+    eps = np.array([g.eps for g in G])[gof]
+    c = ref["clip"][-1]
+    stats = {}
+    if check_acc:
+        bad = np.nonzero(gpu["acc"].view(np.uint32) != ref["acc"].view(np.uint32))[0]
+        # +0 and -0 compare equal
+        bad = bad[~((gpu["acc"][bad] == 0) & (ref["acc"][bad] == 0))]
+        assert bad.size == 0, f"accumulator differs at {bad[:8]}: {gpu['acc'][bad[:8]]} vs {ref['acc'][bad[:8]]}"
+    acc_ref = ref["acc"].astype(np.float64)
+    if grad_scale != 1.0:
+        acc_ref = (ref["acc"] * np.float32(grad_scale)).astype(np.float32).astype(np.float64)
+    gc = acc_ref * c
+    m_ref, v_ref, p_ref = (ref[k].astype(np.float64) for k in ("m", "v", "p"))
+    s_m = np.maximum(np.abs(m_ref), b1 * np.abs(prev["m"].astype(np.float64)) + (1 - b1) * np.abs(gc))
+    s_v = np.abs(v_ref)
+    bc1, bc2 = 1 - b1 ** t_last, 1 - b2 ** t_last
+    u = np.abs(m_ref / bc1) / (np.sqrt(v_ref / bc2) + eps)
+    s_p = np.maximum(np.abs(prev["p"].astype(np.float64)), lr * u)
+    for name, s in (("m", s_m), ("v", s_v), ("p", s_p)):
+        x, y = gpu[name].astype(np.float64), ref[name].astype(np.float64)
+        err = np.abs(x - y)
+        lim = REL * np.maximum(np.abs(y), s)
+        bad = np.nonzero(~(err <= lim))[0]
+        assert bad.size == 0, (f"{name} out of tolerance at {bad[:8]}: gpu {x[bad[:8]]} ref {y[bad[:8]]} "
+                               f"lim {lim[bad[:8]]}")
+        strict = np.count_nonzero(err > REL * np.abs(y))
+        stats[name + "_max_scaled_err"] = float(np.max(err / np.maximum(np.maximum(np.abs(y), s), 1e-45)))
+        stats[name + "_strict_rel_fail"] = int(strict)
+    bg, br = gpu["p_bf16"].astype(np.int64), ref["p_bf16"].astype(np.int64)
+    diff = np.abs(bg - br)
+    near = _bf16_midpoint_close(ref["p"])
+    bad = np.nonzero((diff != 0) & ~((diff == 1) & near))[0]
+    bad = bad[~(((bg[bad] & 0x7FFF) == 0) & ((br[bad] & 0x7FFF) == 0))]
+    assert bad.size == 0, f"bf16 params differ at {bad[:8]}: {bg[bad[:8]]} vs {br[bad[:8]]}"
+    stats["bf16_ulp_diffs"] = int(np.count_nonzero(diff))
+    return stats
+
+
+def check_norms(gpu_norms, ref_sums):
+    for g, S in zip(gpu_norms, ref_sums):
+        r = math.sqrt(S)
+        assert abs(g - r) <= REL * r, f"norm {g} vs {r}"
+    return max((abs(g - math.sqrt(S)) / math.sqrt(S) if S > 0 else abs(g)) for g, S in zip(gpu_norms, ref_sums))

@@ -1,0 +1,147 @@
+"""The C ABI without a GPU: build, exported symbols, struct layout, validation.
+
+bf16opt_create validates its descriptor before touching CUDA, so every
+argument error is reported the same way with or without a device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
+from mixed_precision_optimizer_bf16_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bf16opt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return C.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bf16opt_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(C.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True)
+    syms = set(re.findall(r"\bT (bf16opt_\w+)", out.stdout))
+    for name in declared_functions():
+        assert name in syms, name
+        assert hasattr(lib, name)
+
+
+def test_struct_layout_matches_header(tmp_path):
+    probe = tmp_path / "probe.c"
+    probe.write_text("""
+#include <stdio.h>
+#include <stddef.h>
+#include "bf16opt.h"
+int main(void) {
+  printf("%zu %zu %zu %zu\\n", sizeof(bf16opt_desc_t), sizeof(bf16opt_tensor_t), sizeof(bf16opt_range_t), sizeof(bf16opt_group_t));
+  printf("%zu %zu %zu %zu %zu %zu %zu\\n", offsetof(bf16opt_desc_t, groups), offsetof(bf16opt_desc_t, n),
+         offsetof(bf16opt_desc_t, param_bf16), offsetof(bf16opt_desc_t, ranges), offsetof(bf16opt_desc_t, n_tensors),
+         offsetof(bf16opt_desc_t, tensors), offsetof(bf16opt_desc_t, grad_scale));
+  printf("%zu %zu\\n", offsetof(bf16opt_tensor_t, numel), offsetof(bf16opt_tensor_t, group));
+  return 0;
+}
+""")
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(probe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    sizes = [int(x) for x in lines[0].split()]
+    assert sizes == [ctypes.sizeof(C.bf16opt_desc_t), ctypes.sizeof(C.bf16opt_tensor_t),
+                     ctypes.sizeof(C.bf16opt_range_t), ctypes.sizeof(C.bf16opt_group_t)]
+    offs = [int(x) for x in lines[1].split()]
+    D = C.bf16opt_desc_t
+    assert offs == [D.groups.offset, D.n.offset, D.param_bf16.offset, D.ranges.offset, D.n_tensors.offset,
+                    D.tensors.offset, D.grad_scale.offset]
+    T = C.bf16opt_tensor_t
+    assert [int(x) for x in lines[2].split()] == [T.numel.offset, T.group.offset]
+
+
+G = [dict(lr=6e-5, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.01),
+     dict(lr=6e-5, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)]
+BASE = 0x7f0000000000  # fake device addresses: validation never dereferences them
+
+
+def flat(n=1000, **kw):
+    args = dict(master=BASE, exp_avg=BASE + 0x100000, exp_avg_sq=BASE + 0x200000, grad_accum=BASE + 0x300000,
+                param_bf16=BASE + 0x400000)
+    args.update({k: v for k, v in kw.items() if k in args})
+    other = {k: v for k, v in kw.items() if k not in args}
+    return C.flat_desc(n, args["master"], args["exp_avg"], args["exp_avg_sq"], args["grad_accum"],
+                       args["param_bf16"], other.pop("groups", G), **other)
+
+
+@pytest.mark.parametrize("desc,code", [
+    (lambda: flat(groups=[dict(G[0], beta1=1.0)]), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(groups=[dict(G[0], eps=0.0)]), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(groups=[dict(G[0], lr=float("nan"))]), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(groups=[dict(G[0], weight_decay=-1.0)]), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(groups=G * 9), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(master=0), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(master=BASE + 2), C.BF16OPT_ERR_ALIGNMENT),
+    (lambda: flat(param_bf16=BASE + 0x400001), C.BF16OPT_ERR_ALIGNMENT),
+    (lambda: flat(exp_avg=BASE + 3996), C.BF16OPT_ERR_INVALID_ARG),          # overlaps master
+    (lambda: flat(ranges=[(0, 500, 0), (600, 1000, 1)]), C.BF16OPT_ERR_INVALID_ARG),  # gap
+    (lambda: flat(ranges=[(0, 500, 0), (400, 1000, 1)]), C.BF16OPT_ERR_INVALID_ARG),  # overlap
+    (lambda: flat(ranges=[(0, 500, 0), (500, 999, 1)]), C.BF16OPT_ERR_INVALID_ARG),   # short
+    (lambda: flat(ranges=[(0, 1000, 2)]), C.BF16OPT_ERR_INVALID_ARG),                # bad group
+    (lambda: flat(max_grad_norm=float("inf")), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: flat(grad_scale=0.0), C.BF16OPT_ERR_INVALID_ARG),
+    (lambda: C.list_desc([(BASE, BASE + 4096, BASE + 8192, BASE + 12288, BASE + 16384, 1000, 0),
+                          (BASE + 2000, BASE + 0x10000, BASE + 0x20000, BASE + 0x30000, BASE + 0x40000, 10, 1)], G),
+     C.BF16OPT_ERR_INVALID_ARG),                                                     # tensor 1 overlaps tensor 0
+    (lambda: C.list_desc([(BASE, BASE + 4096, BASE + 8192, BASE + 12288, BASE + 16385, 1000, 0)], G),
+     C.BF16OPT_ERR_ALIGNMENT),
+    (lambda: C.list_desc([(BASE, BASE + 4096, BASE + 8192, BASE + 12288, BASE + 16384, 1000, 5)], G),
+     C.BF16OPT_ERR_INVALID_ARG),
+])
+def test_create_validation(lib, desc, code):
+    d = desc()
+    rc, h = C.bf16opt_create(d)
+    assert rc == code, C.bf16opt_last_error(None)
+    assert not h.value
+    assert C.bf16opt_last_error(None)
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.bf16opt_create(None, ctypes.byref(h)) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_accumulate(None, 0, None, C.BF16OPT_FIRST) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_grad_norm(None)[0] == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_step(None) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_destroy(None) == C.BF16OPT_OK
+    assert C.bf16opt_get_step(None)[0] == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_set_step(None, 3) == C.BF16OPT_ERR_INVALID_ARG
+
+
+def test_error_strings(lib):
+    for code in (0, 1, -1, -2, -3, -4, -5, -6):
+        assert C.bf16opt_error_string(code) not in ("", "unknown status")
+    assert C.bf16opt_error_string(-99) == "unknown status"
+
+
+def test_valid_descriptor_without_device_is_unsupported(lib):
+    """With no GPU visible a valid descriptor gets ERR_UNSUPPORTED, never a crash."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    rc, h = C.bf16opt_create(flat(ranges=[(0, 400, 0), (400, 1000, 1)]))
+    assert rc == C.BF16OPT_ERR_UNSUPPORTED and not h.value
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        C.load(str(tmp_path / "libbf16opt.so"))

@@ -1,0 +1,315 @@
+"""GPU parity: libbf16opt.so (through its C ABI) against the CPU oracle.
+
+Every test here needs a CUDA GPU and the built library; all are marked gpu.
+"""
+import ctypes
+import gc
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from synth import gpu as sgpu, workloads  # noqa: E402
+from mixed_precision_optimizer_bf16_gb300 import bf16opt as C  # noqa: E402
+from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat  # noqa: E402
+from harness import GpuShard, check_norms, compare, ogroups, oracle_dense, oracle_sampled, sample_indices  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+
+
+@pytest.fixture(autouse=True)
+def _cleanup():
+    yield
+    gc.collect()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def dense_parity(wl, defer=False, grad_scale=1.0):
+    sh = GpuShard(wl, grad_scale=grad_scale, defer=defer)
+    sh.run(wl.steps)
+    got = sh.states()
+    norms = list(sh.norms)
+    sh.close()
+    ref, prev = oracle_dense(wl, wl.steps, grad_scale)
+    check_norms(norms, ref["sumsq"])
+    gof = wl.group_of(np.arange(wl.n))
+    return compare(got, ref, prev, wl, wl.steps, grad_scale, check_acc=not defer, gof=gof)
+
+
+def sampled_parity(wl, defer=False, k=1 << 15):
+    sh = GpuShard(wl, defer=defer)
+    sh.run(wl.steps)
+    idx = sample_indices(wl, k)
+    got = sh.states(idx)
+    norms = list(sh.norms)
+    sh.close()
+    del sh
+    ref, prev = oracle_sampled(wl, wl.steps, idx)
+    err = check_norms(norms, ref["sumsq"])
+    st = compare(got, ref, prev, wl, wl.steps, check_acc=not defer, gof=wl.group_of(idx))
+    st["norm_rel_err"] = err
+    return st
+
+
+# ---------------------------------------------------------------- generators
+
+@needs_cuda
+def test_device_generator_matches_host():
+    for wl in (workloads.workload(5), workloads.workload(2)):
+        n = 1 << 20
+        first = wl.n - n if wl.id == 2 else 12345
+        d = torch.empty(n, dtype=torch.int16, device="cuda")
+        sgpu.fill_grad(wl, 1, 1, d, first)
+        h = synth.fill_grad(wl, 1, 1, np.empty(n, np.uint16), first)
+        assert np.array_equal(d.cpu().numpy().view(np.uint16), h)
+        f = torch.empty(n, dtype=torch.float32, device="cuda")
+        sgpu.fill_master(wl, f, first)
+        hm = synth.fill_master(wl, np.empty(n, np.float32), first)
+        assert np.array_equal(f.cpu().numpy().view(np.uint32), hm.view(np.uint32))
+
+
+# ------------------------------------------------------------- dense parity
+
+@needs_cuda
+@pytest.mark.parametrize("defer", [False, True])
+def test_tiny_workload_dense(defer):
+    st = dense_parity(workloads.workload(1), defer=defer)
+    print("tiny", defer, st)
+
+
+@needs_cuda
+@pytest.mark.parametrize("defer", [False, True])
+def test_clip_edge_workload_dense(defer):
+    """2^27+13 elements, every buffer 2 elements past a 256-B boundary, clip ~1/163,
+    1 % exact-zero gradients, masters log-uniform over 1e-8..1e3, 5 steps."""
+    wl = workloads.workload(5)
+    st = dense_parity(wl, defer=defer)
+    print("clip edge", defer, st)
+
+
+SMALL = [
+    # (sizes, misalign, gas, steps, sigma)
+    ([1], 0, 1, 2, 1e-3),
+    ([2], 1, 2, 2, 0.5),
+    ([3, 5], 3, 3, 2, 1e-3),
+    ([7, 8, 9], 2, 2, 3, 0.2),
+    ([31, 1000, 4096], 5, 2, 2, 1e-3),
+    ([16383, 1, 16384, 16385], 7, 3, 2, 0.05),
+    ([50001, 3], 6, 1, 3, 1e-2),
+    ([65536 * 3 + 17], 4, 2, 2, 1e-3),
+    ([4, 4, 4, 4], 0, 2, 2, 0.3),
+]
+
+
+@needs_cuda
+@pytest.mark.parametrize("case", range(len(SMALL)))
+@pytest.mark.parametrize("mode", ["flat", "list"])
+@pytest.mark.parametrize("defer", [False, True])
+def test_small_ragged_variants(case, mode, defer):
+    sizes, mis, gas, steps, sigma = SMALL[case]
+    decay = [(i % 3) != 1 for i in range(len(sizes))]
+    wl = workloads.custom(100 + case, sizes, decay=decay, gas=gas, steps=steps, grad_sigma=sigma, misalign=mis,
+                          mode=mode)
+    dense_parity(wl, defer=defer)
+
+
+@needs_cuda
+def test_list_more_tensors_than_one_launch():
+    """1100 tensors (> 1024 gradient pointers per launch): two launches per pass."""
+    rng = np.random.default_rng(5)
+    sizes = rng.integers(1, 700, 1100).tolist()
+    wl = workloads.custom(150, sizes, decay=[i % 2 == 0 for i in range(1100)], gas=2, steps=2,
+                          grad_sigma=0.05, misalign=3, mode="list")
+    dense_parity(wl)
+    dense_parity(wl, defer=True)
+
+
+@needs_cuda
+def test_grad_scale():
+    wl = workloads.custom(160, [70000, 333], decay=[True, False], gas=3, steps=2, grad_sigma=0.3)
+    dense_parity(wl, grad_scale=0.25)
+    dense_parity(wl, defer=True, grad_scale=0.25)
+
+
+# ----------------------------------------------------------- full-size sampled
+
+@needs_cuda
+@pytest.mark.parametrize("defer", [True, False])
+def test_scaled_bloom_full_size_sampled(defer):
+    """1,722,408,960 elements, 293 tensors in one flat buffer, decay/no-decay
+    ranges, GAS 4, 2 steps; the benchmark's launch configuration is defer=True."""
+    st = sampled_parity(workloads.workload(2), defer=defer)
+    print("scaled BLOOM", defer, st)
+
+
+@needs_cuda
+def test_large_partition_full_size_sampled():
+    """1.83e9 flat elements, GAS 32, 1 step."""
+    st = sampled_parity(workloads.workload(3), defer=True)
+    print("large partition", st)
+
+
+@needs_cuda
+def test_tp4_slice_full_size_sampled():
+    """72 separate tensors, 3,700,064,256 elements, GAS 8, 2 steps."""
+    st = sampled_parity(workloads.workload(4), defer=True)
+    print("TP4 slice", st)
+
+
+# ------------------------------------------------------------ behaviour
+
+@needs_cuda
+def test_determinism_bitwise():
+    wl = workloads.custom(170, [300_000, 5000, 77], decay=[True, False, True], gas=3, steps=2, grad_sigma=0.1,
+                          misalign=1)
+    outs = []
+    for _ in range(2):
+        sh = GpuShard(wl, defer=True)
+        sh.run(wl.steps)
+        outs.append((sh.states(), list(sh.norms)))
+        sh.close()
+    (a, na), (b, nb) = outs
+    assert na == nb
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8))
+
+
+def _raw_flat(n, groups=None):
+    wl = workloads.custom(180, [max(n, 1)])
+    flat = alloc_flat(n, "cuda")
+    for k in flat:
+        flat[k].zero_()
+    desc = C.flat_desc(n, *(flat[k].data_ptr() if n else 0 for k in
+                            ("master", "exp_avg", "exp_avg_sq", "grad_accum", "param_bf16")),
+                       groups or wl.groups)
+    rc, h = C.bf16opt_create(desc)
+    assert rc == 0, C.bf16opt_last_error(None)
+    return flat, h
+
+
+@needs_cuda
+def test_sequence_errors():
+    flat, h = _raw_flat(1000)
+    g = torch.zeros(1000, dtype=torch.int16, device="cuda")
+    assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_grad_norm(h)[0] == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, 0) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST) == 0
+    assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == 0
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == C.BF16OPT_ERR_SEQUENCE
+    rc, nrm = C.bf16opt_grad_norm(h, 0, True)
+    assert rc == 0 and nrm == 0.0
+    assert C.bf16opt_step(h) == 0
+    assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_get_step(h) == (0, 1)
+    assert C.bf16opt_accumulate(h, g.data_ptr() + 1, None, C.BF16OPT_FIRST) == C.BF16OPT_ERR_ALIGNMENT
+    assert "sequence" in C.bf16opt_error_string(C.BF16OPT_ERR_SEQUENCE)
+    C.bf16opt_destroy(h)
+
+
+@needs_cuda
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_nonfinite_gradient_warns(bad):
+    flat, h = _raw_flat(5000)
+    g = torch.zeros(5000, dtype=torch.float32, device="cuda")
+    g[1234] = bad
+    gb = g.to(torch.bfloat16).view(torch.int16)
+    assert C.bf16opt_accumulate(h, gb.data_ptr(), None, C.BF16OPT_FIRST | C.BF16OPT_LAST) == 0
+    rc, nrm = C.bf16opt_grad_norm(h, 0, True)
+    assert rc == C.BF16OPT_WARN_NONFINITE and not np.isfinite(nrm)
+    assert C.bf16opt_step(h) == 0  # the library does not skip; the caller decides
+    torch.cuda.synchronize()
+    C.bf16opt_destroy(h)
+
+
+@needs_cuda
+def test_empty_shard():
+    flat, h = _raw_flat(0)
+    assert C.bf16opt_accumulate(h, 0, None, C.BF16OPT_FIRST | C.BF16OPT_LAST) == 0
+    assert C.bf16opt_grad_norm(h, 0, True) == (0, 0.0)
+    assert C.bf16opt_step(h) == 0
+    assert C.bf16opt_get_step(h) == (0, 1)
+    C.bf16opt_destroy(h)
+
+
+@needs_cuda
+def test_lr_override_and_resume():
+    """lr_override replaces the groups' lr for one step; a new handle over the
+    same buffers with set_step(2) continues exactly like an uninterrupted run."""
+    wl = workloads.custom(190, [20000, 1000], decay=[True, False], gas=2, steps=3, grad_sigma=0.2)
+    # uninterrupted 3 steps with lr x0.5 on the last step
+    sh = GpuShard(wl)
+    sh.run_step(0)
+    sh.run_step(1)
+    for k in range(wl.gas):
+        sgpu.fill_grad(wl, 2, k, sh.gbuf)
+        sh.opt.accumulate(sh.gbuf, first=k == 0, last=k == wl.gas - 1)
+    sh.opt.grad_norm()
+    sh.opt.step(lr=[3e-5, 3e-5])
+    a = sh.states()
+    sh.close()
+    # interrupted: 2 steps, new handle, set_step(2), last step
+    sh2 = GpuShard(wl)
+    sh2.run_step(0)
+    sh2.run_step(1)
+    sh2.opt.close()
+    sh2.opt = BF16Optimizer(wl.groups, flat=sh2.flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
+    sh2.opt.t = 2
+    for k in range(wl.gas):
+        sgpu.fill_grad(wl, 2, k, sh2.gbuf)
+        sh2.opt.accumulate(sh2.gbuf, first=k == 0, last=k == wl.gas - 1)
+    sh2.opt.grad_norm()
+    sh2.opt.step(lr=[3e-5, 3e-5])
+    b = sh2.states()
+    assert sh2.opt.t == 3
+    sh2.close()
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8))
+    # and the oracle with lr 3e-5 on step 3
+    G = ogroups(wl)
+    n = wl.n
+    p = synth.fill_master(wl, np.empty(n, np.float32))
+    gfn = lambda s, k: synth.fill_grad(wl, s, k, np.empty(n, np.uint16))
+    r2 = oracle.run_dense(p, gfn, wl.ranges(), G, 2, wl.gas, wl.max_norm)
+    prev = {k: r2[k].copy() for k in ("p", "m", "v")}
+    G3 = [oracle.group(float(np.float32(3e-5)), g.beta1, g.beta2, g.eps, g.weight_decay) for g in G]
+    r3 = oracle.run_dense(r2["p"], gfn, wl.ranges(), G3, 1, wl.gas, wl.max_norm, t0=2, m=r2["m"], v=r2["v"])
+    wl.groups = [dict(g, lr=3e-5) for g in wl.groups]
+    compare(a, r3, prev, wl, 3, gof=wl.group_of(np.arange(n)))
+
+
+@needs_cuda
+def test_inconsistent_alignment_falls_back_correctly():
+    """Buffers with different offsets modulo 16 B take the element-wise path."""
+    wl = workloads.custom(195, [10007], gas=2, steps=2, grad_sigma=0.1)
+    n = wl.n
+    bufs = {}
+    for i, (k, dt) in enumerate((("master", torch.float32), ("exp_avg", torch.float32), ("exp_avg_sq", torch.float32),
+                                 ("grad_accum", torch.float32), ("param_bf16", torch.int16))):
+        base = torch.zeros(n + 64, dtype=dt, device="cuda")
+        bufs[k] = base[i % 4:i % 4 + n]
+    sgpu.fill_master(wl, bufs["master"])
+    opt = BF16Optimizer(wl.groups, flat=bufs, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
+    gb = torch.empty(n + 64, dtype=torch.int16, device="cuda")[3:3 + n]
+    norms = []
+    for s in range(wl.steps):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, gb)
+            opt.accumulate(gb, first=k == 0, last=k == wl.gas - 1)
+        norms.append(opt.grad_norm(sync=True))
+        opt.step()
+    got = dict(p=bufs["master"].cpu().numpy(), m=bufs["exp_avg"].cpu().numpy(), v=bufs["exp_avg_sq"].cpu().numpy(),
+               acc=bufs["grad_accum"].cpu().numpy(), p_bf16=bufs["param_bf16"].cpu().numpy().view(np.uint16))
+    opt.close()
+    ref, prev = oracle_dense(wl, wl.steps)
+    check_norms(norms, ref["sumsq"])
+    compare(got, ref, prev, wl, wl.steps, gof=wl.group_of(np.arange(n)))
