@@ -11,9 +11,14 @@ elements.
 Tolerances (the workload definitions' bar, plainest reading where silent):
   accumulator    bit-exact;
   global norm    |n_gpu - n_ref| <= 1e-6 n_ref;
-  m, v, master   |x_gpu - x_ref| <= 1e-6 * max(|x_ref|, s), with the operand
-                 scale s = b1 |m_prev| + (1 - b1) |gc| for m, |v_ref| for v and
-                 max(|p_prev|, lr |m_hat / (sqrt(v_hat) + eps)|) for the master;
+  m, v, master   |x_gpu - x_ref| <= 1e-6 * max(|x_ref|, s), with s the operand
+                 scale of the whole recurrence (the sum of the magnitudes of its
+                 terms, so that cancellation in any step is covered):
+                   m:      M_t = b1 M_{t-1} + (1 - b1) |gc_t|,           M_0 = 0
+                   v:      |v_ref| (all terms are positive)
+                   master: A_t = A_{t-1} (1 - lr wd) + lr |u_t|,           A_0 = |p_0|
+                 with gc_t the clipped gradient and u_t = m_hat_t / (sqrt(v_hat_t) + eps)
+                 of the oracle's step t;
   bf16 param     bit-exact, except <= 1 bf16 ulp where the oracle's FP32 master
                  lies within 1e-6 (relative) of a bf16 rounding midpoint.
 """
@@ -130,19 +135,40 @@ class GpuShard:
 
 # ------------------------------------------------------------------ oracle side
 
+def _gvec(wl, gof, attr):
+    return np.array([getattr(g, attr) for g in ogroups(wl)])[gof]
+
+
+def _update_scales(sc, wl, gof, acc, c, m, v, t, grad_scale):
+    """Advance the operand scales M (first moment) and A (master) by one step."""
+    b1, b2 = _gvec(wl, gof, "beta1"), _gvec(wl, gof, "beta2")
+    lr, wd, eps = _gvec(wl, gof, "lr"), _gvec(wl, gof, "weight_decay"), _gvec(wl, gof, "eps")
+    e = acc if grad_scale == 1.0 else (acc * np.float32(grad_scale)).astype(np.float32)
+    gc = np.abs(e.astype(np.float64)) * c
+    sc["M"] = b1 * sc["M"] + (1 - b1) * gc
+    u = np.abs(m.astype(np.float64) / (1 - b1 ** t)) / (np.sqrt(v.astype(np.float64) / (1 - b2 ** t)) + eps)
+    sc["A"] = sc["A"] * (1 - lr * wd) + lr * u
+
+
 def oracle_dense(wl, steps, grad_scale=1.0):
-    """Dense oracle run; returns (final, prev) state dicts (prev = after steps-1)."""
+    """Dense oracle run, one step at a time; returns (final states, operand scales)."""
     n = wl.n
-    p0 = synth.fill_master(wl, np.empty(n, np.float32))
+    p = synth.fill_master(wl, np.empty(n, np.float32))
     G = ogroups(wl)
+    gof = wl.group_of(np.arange(n))
     gfn = lambda s, k: synth.fill_grad(wl, s, k, np.empty(n, np.uint16))
-    prev = oracle.run_dense(p0.copy(), gfn, wl.ranges(), G, steps - 1, wl.gas, wl.max_norm, grad_scale)
-    prev = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in prev.items()}
-    fin = oracle.run_dense(prev["p"].copy(), gfn, wl.ranges(), G, 1, wl.gas, wl.max_norm, grad_scale,
-                           t0=steps - 1, m=prev["m"].copy(), v=prev["v"].copy())
-    fin["sumsq"] = prev["sumsq"] + fin["sumsq"]
-    fin["clip"] = prev["clip"] + fin["clip"]
-    return fin, prev
+    sc = {"M": np.zeros(n), "A": np.abs(p.astype(np.float64))}
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    sums, clips = [], []
+    r = None
+    for s in range(steps):
+        r = oracle.run_dense(p, gfn, wl.ranges(), G, 1, wl.gas, wl.max_norm, grad_scale, t0=s, m=m, v=v)
+        p, m, v = r["p"], r["m"], r["v"]
+        sums += r["sumsq"]
+        clips += r["clip"]
+        _update_scales(sc, wl, gof, r["acc"], r["clip"][0], m, v, s + 1, grad_scale)
+    r["sumsq"], r["clip"] = sums, clips
+    return r, sc
 
 
 def oracle_sampled(wl, steps, idx, grad_scale=1.0):
@@ -155,14 +181,12 @@ def oracle_sampled(wl, steps, idx, grad_scale=1.0):
     p0 = synth.gather_master(wl, idx)
     G = ogroups(wl)
     gof = wl.group_of(idx)
-    p, m, v, pb, acc = oracle.sample_run(st, idx, p0, G, gof, clips)
-    if steps > 1:
-        pp, mp, vp, _, _ = oracle.sample_run(st, idx, p0, G, gof, clips[:steps - 1])
-    else:
-        pp, mp, vp = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    sc = {"M": np.zeros(idx.size), "A": np.abs(p0.astype(np.float64))}
+    for s in range(steps):
+        p, m, v, pb, acc = oracle.sample_run(st, idx, p0, G, gof, clips[:s + 1])
+        _update_scales(sc, wl, gof, acc, clips[s], m, v, s + 1, grad_scale)
     fin = dict(p=p, m=m, v=v, p_bf16=pb, acc=acc, sumsq=sums, clip=clips)
-    prev = dict(p=pp, m=mp, v=vp)
-    return fin, prev
+    return fin, sc
 
 
 def sample_indices(wl, k=1 << 15, seed=0):
@@ -188,42 +212,23 @@ def _bf16_midpoint_close(p_ref):
     return np.abs(x - mid) <= REL * np.abs(x)
 
 
-def compare(gpu, ref, prev, wl, t_last, grad_scale=1.0, check_acc=True, gof=None):
+def compare(gpu, ref, scales, wl, grad_scale=1.0, check_acc=True):
     """Element-wise parity; returns a stats dict, raises AssertionError on a breach."""
-    G = ogroups(wl)
-    n = ref["p"].size
-    gof = np.zeros(n, np.uint32) if gof is None else np.asarray(gof)
-    b1 = np.array([g.beta1 for g in G])[gof]
-    b2 = np.array([g.beta2 for g in G])[gof]
-    lr = np.array([g.lr for g in G])[gof]
-    eps = np.array([g.eps for g in G])[gof]
-    c = ref["clip"][-1]
     stats = {}
     if check_acc:
         bad = np.nonzero(gpu["acc"].view(np.uint32) != ref["acc"].view(np.uint32))[0]
         # +0 and -0 compare equal
         bad = bad[~((gpu["acc"][bad] == 0) & (ref["acc"][bad] == 0))]
         assert bad.size == 0, f"accumulator differs at {bad[:8]}: {gpu['acc'][bad[:8]]} vs {ref['acc'][bad[:8]]}"
-    acc_ref = ref["acc"].astype(np.float64)
-    if grad_scale != 1.0:
-        acc_ref = (ref["acc"] * np.float32(grad_scale)).astype(np.float32).astype(np.float64)
-    gc = acc_ref * c
-    m_ref, v_ref, p_ref = (ref[k].astype(np.float64) for k in ("m", "v", "p"))
-    s_m = np.maximum(np.abs(m_ref), b1 * np.abs(prev["m"].astype(np.float64)) + (1 - b1) * np.abs(gc))
-    s_v = np.abs(v_ref)
-    bc1, bc2 = 1 - b1 ** t_last, 1 - b2 ** t_last
-    u = np.abs(m_ref / bc1) / (np.sqrt(v_ref / bc2) + eps)
-    s_p = np.maximum(np.abs(prev["p"].astype(np.float64)), lr * u)
-    for name, s in (("m", s_m), ("v", s_v), ("p", s_p)):
+    for name, s in (("m", scales["M"]), ("v", np.abs(ref["v"].astype(np.float64))), ("p", scales["A"])):
         x, y = gpu[name].astype(np.float64), ref[name].astype(np.float64)
         err = np.abs(x - y)
         lim = REL * np.maximum(np.abs(y), s)
         bad = np.nonzero(~(err <= lim))[0]
         assert bad.size == 0, (f"{name} out of tolerance at {bad[:8]}: gpu {x[bad[:8]]} ref {y[bad[:8]]} "
                                f"lim {lim[bad[:8]]}")
-        strict = np.count_nonzero(err > REL * np.abs(y))
         stats[name + "_max_scaled_err"] = float(np.max(err / np.maximum(np.maximum(np.abs(y), s), 1e-45)))
-        stats[name + "_strict_rel_fail"] = int(strict)
+        stats[name + "_strict_rel_fail"] = int(np.count_nonzero(err > REL * np.abs(y)))
     bg, br = gpu["p_bf16"].astype(np.int64), ref["p_bf16"].astype(np.int64)
     diff = np.abs(bg - br)
     near = _bf16_midpoint_close(ref["p"])

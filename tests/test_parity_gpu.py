@@ -37,10 +37,9 @@ def dense_parity(wl, defer=False, grad_scale=1.0):
     got = sh.states()
     norms = list(sh.norms)
     sh.close()
-    ref, prev = oracle_dense(wl, wl.steps, grad_scale)
+    ref, scales = oracle_dense(wl, wl.steps, grad_scale)
     check_norms(norms, ref["sumsq"])
-    gof = wl.group_of(np.arange(wl.n))
-    return compare(got, ref, prev, wl, wl.steps, grad_scale, check_acc=not defer, gof=gof)
+    return compare(got, ref, scales, wl, grad_scale, check_acc=not defer)
 
 
 def sampled_parity(wl, defer=False, k=1 << 15):
@@ -51,9 +50,9 @@ def sampled_parity(wl, defer=False, k=1 << 15):
     norms = list(sh.norms)
     sh.close()
     del sh
-    ref, prev = oracle_sampled(wl, wl.steps, idx)
+    ref, scales = oracle_sampled(wl, wl.steps, idx)
     err = check_norms(norms, ref["sumsq"])
-    st = compare(got, ref, prev, wl, wl.steps, check_acc=not defer, gof=wl.group_of(idx))
+    st = compare(got, ref, scales, wl, check_acc=not defer)
     st["norm_rel_err"] = err
     return st
 
@@ -275,16 +274,23 @@ def test_lr_override_and_resume():
     for k in ("p", "m", "v", "p_bf16"):
         assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8))
     # and the oracle with lr 3e-5 on step 3
+    import harness
     G = ogroups(wl)
     n = wl.n
+    gof = wl.group_of(np.arange(n))
     p = synth.fill_master(wl, np.empty(n, np.float32))
+    sc = {"M": np.zeros(n), "A": np.abs(p.astype(np.float64))}
     gfn = lambda s, k: synth.fill_grad(wl, s, k, np.empty(n, np.uint16))
-    r2 = oracle.run_dense(p, gfn, wl.ranges(), G, 2, wl.gas, wl.max_norm)
-    prev = {k: r2[k].copy() for k in ("p", "m", "v")}
-    G3 = [oracle.group(float(np.float32(3e-5)), g.beta1, g.beta2, g.eps, g.weight_decay) for g in G]
-    r3 = oracle.run_dense(r2["p"], gfn, wl.ranges(), G3, 1, wl.gas, wl.max_norm, t0=2, m=r2["m"], v=r2["v"])
-    wl.groups = [dict(g, lr=3e-5) for g in wl.groups]
-    compare(a, r3, prev, wl, 3, gof=wl.group_of(np.arange(n)))
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    lr3 = float(np.float32(3e-5))
+    for s in range(3):
+        Gs = G if s < 2 else [oracle.group(lr3, g.beta1, g.beta2, g.eps, g.weight_decay) for g in G]
+        r = oracle.run_dense(p, gfn, wl.ranges(), Gs, 1, wl.gas, wl.max_norm, t0=s, m=m, v=v)
+        p, m, v = r["p"], r["m"], r["v"]
+        if s == 2:
+            wl.groups = [dict(g, lr=3e-5) for g in wl.groups]
+        harness._update_scales(sc, wl, gof, r["acc"], r["clip"][0], m, v, s + 1, 1.0)
+    compare(a, r, sc, wl)
 
 
 @needs_cuda
@@ -310,6 +316,6 @@ def test_inconsistent_alignment_falls_back_correctly():
     got = dict(p=bufs["master"].cpu().numpy(), m=bufs["exp_avg"].cpu().numpy(), v=bufs["exp_avg_sq"].cpu().numpy(),
                acc=bufs["grad_accum"].cpu().numpy(), p_bf16=bufs["param_bf16"].cpu().numpy().view(np.uint16))
     opt.close()
-    ref, prev = oracle_dense(wl, wl.steps)
+    ref, scales = oracle_dense(wl, wl.steps)
     check_norms(norms, ref["sumsq"])
-    compare(got, ref, prev, wl, wl.steps, gof=wl.group_of(np.arange(n)))
+    compare(got, ref, scales, wl)
