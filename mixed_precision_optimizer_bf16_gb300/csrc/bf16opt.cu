@@ -110,11 +110,22 @@ bool overlaps(std::vector<Interval> &iv) {
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 
+#ifndef BF16K_ACC_U
+#define BF16K_ACC_U 8       // quads in flight per thread, accumulate family
+#endif
+#ifndef BF16K_STEP_U
+#define BF16K_STEP_U 4      // quads in flight per thread, fused step
+#endif
+#ifndef BF16K_MAX_CTAS_PER_SM
+#define BF16K_MAX_CTAS_PER_SM 64
+#endif
+
 template <class K>
 int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
         per_sm = 1;
+    if (per_sm > BF16K_MAX_CTAS_PER_SM) per_sm = BF16K_MAX_CTAS_PER_SM;
     const uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
     return (int)std::max<uint64_t>(1, std::min<uint64_t>(g, nchunks));
 }
@@ -122,7 +133,7 @@ int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks) {
 // Launch one accumulate-family pass over every batch.
 template <int SRC, bool WRITE, bool NORM>
 int launch_accum(bf16opt_t *h, const uint16_t *gflat, const uint16_t *const *glist, cudaStream_t st) {
-    constexpr int U = 8;
+    constexpr int U = BF16K_ACC_U;
     if (h->n_chunks == 0) return 0;
     if (h->mode == BF16OPT_FLAT) {
         auto k = k_accum<SRC, WRITE, NORM, FlatGrads, U>;
@@ -148,7 +159,7 @@ int launch_accum(bf16opt_t *h, const uint16_t *gflat, const uint16_t *const *gli
 
 template <int SRC>
 int launch_step(bf16opt_t *h, const GroupTable &gtab, cudaStream_t st) {
-    constexpr int U = 4;
+    constexpr int U = BF16K_STEP_U;
     if (h->n_chunks == 0) return 0;
     if (h->mode == BF16OPT_FLAT) {
         auto k = k_step<SRC, FlatGrads, U>;

@@ -33,8 +33,16 @@
 
 namespace bf16k {
 
-constexpr int kThreads = 256;        // threads per CTA
-constexpr uint32_t kChunk = 16384;   // elements per chunk (multiple of 4)
+// Launch shape; the defaults were chosen by measurement on GB300 and can be
+// overridden at build time (-DBF16K_THREADS=..., -DBF16K_CHUNK=...).
+#ifndef BF16K_THREADS
+#define BF16K_THREADS 256
+#endif
+#ifndef BF16K_CHUNK
+#define BF16K_CHUNK 16384
+#endif
+constexpr int kThreads = BF16K_THREADS;  // threads per CTA
+constexpr uint32_t kChunk = BF16K_CHUNK; // elements per chunk (multiple of 4)
 constexpr int kMaxGroups = 16;
 constexpr int kListSlots = 1024;     // gradient pointers per LIST-mode launch
 constexpr int kFinalThreads = 1024;
