@@ -169,6 +169,48 @@ int bf16opt_destroy(bf16opt_t *h);
 int bf16opt_get_step(const bf16opt_t *h, int64_t *t);
 int bf16opt_set_step(bf16opt_t *h, int64_t t);
 
+/* ---- allocation-free one-shot norm -----------------------------------------
+ * No counterpart in the paper: a service entry point for callers that cannot
+ * call cudaMalloc -- code inside another framework's launch path that is given
+ * only a stream and a pre-planned workspace (plugins, custom-op launchers),
+ * processes whose device memory is held by a caching allocator (a raw
+ * cudaMalloc can then fail), and latency-sensitive loops that cannot take the
+ * device synchronisation cudaMalloc/cudaFree imply.
+ *
+ * Computes, without a handle and without allocating anything, the global L2
+ * norm of a flat FP32 gradient accumulator `grad_accum` of n elements (each
+ * element times grad_scale, rounded to FP32), with the same deterministic
+ * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard, and the
+ * clip coefficient c = max_grad_norm / norm if norm > max_grad_norm (> 0),
+ * else 1.  `out` is device-accessible memory owned by the caller; the result
+ * is written there on `stream` (nothing is synchronised).
+ *
+ * Scratch: one FP64 partial per 16,384-element chunk, kept in a file-scope
+ * device array of 65,536 entries (512 KiB) that every GPU loading this
+ * library holds until the process exits; hence n is limited to
+ * BF16OPT_STATIC_NORM_MAX_ELEMS (2^30) elements and larger n is rejected with
+ * BF16OPT_ERR_INVALID_ARG before any work is enqueued.  Every call writes the
+ * partials it later reads, so nothing has to start at zero.  All calls on a
+ * device share that one array: calls whose work overlaps on the GPU (e.g. on
+ * two streams without ordering between them) race and give wrong results.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Errors: INVALID_ARG (NULL pointers, n too large,
+ * non-finite or zero grad_scale, non-finite max_grad_norm), ALIGNMENT
+ * (grad_accum not 4-B aligned, out not 8-B aligned), UNSUPPORTED (no device),
+ * CUDA (symbol lookup or launch failed); bf16opt_last_error(NULL) has the
+ * message. */
+#define BF16OPT_STATIC_NORM_MAX_ELEMS (((uint64_t)1) << 30)
+
+typedef struct {
+    double sumsq;      /* sum of squares of the (scaled) accumulated gradient */
+    double norm;       /* sqrt(sumsq) */
+    double clip_coef;  /* max_grad_norm / norm if norm > max_grad_norm, else 1 */
+} bf16opt_norm_result_t;
+
+int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, float grad_scale, float max_grad_norm,
+                             bf16opt_norm_result_t *out, void *stream);
+
 /* Static message of a status code; one-line message of the handle's last error. */
 const char *bf16opt_error_string(int code);
 const char *bf16opt_last_error(const bf16opt_t *h);

@@ -25,6 +25,7 @@ BF16OPT_FIRST = 1
 BF16OPT_LAST = 2
 BF16OPT_DEFER = 4
 BF16OPT_MAX_GROUPS = 16
+BF16OPT_STATIC_NORM_MAX_ELEMS = 1 << 30
 
 c_u64, c_u32, c_i32, c_f32, c_vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
 
@@ -50,9 +51,14 @@ class bf16opt_desc_t(ctypes.Structure):
                 ("max_grad_norm", c_f32), ("grad_scale", c_f32)]
 
 
+class bf16opt_norm_result_t(ctypes.Structure):
+    _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double), ("clip_coef", ctypes.c_double)]
+
+
 # Functions the header declares (the tests check the library exports them all).
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
-           "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error")
+           "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
+           "bf16opt_grad_norm_static")
 
 _lib = None
 
@@ -90,6 +96,8 @@ def load(path=None):
     L.bf16opt_error_string.argtypes = [ctypes.c_int]
     L.bf16opt_last_error.restype = ctypes.c_char_p
     L.bf16opt_last_error.argtypes = [hp]
+    L.bf16opt_grad_norm_static.restype = ctypes.c_int
+    L.bf16opt_grad_norm_static.argtypes = [c_vp, c_u64, c_f32, c_f32, c_vp, c_vp]
     if path == _build.LIB_PATH:
         _lib = L
     return L
@@ -137,6 +145,14 @@ def bf16opt_get_step(h):
 
 def bf16opt_set_step(h, t):
     return load().bf16opt_set_step(h, int(t))
+
+
+def bf16opt_grad_norm_static(grad_accum, n, grad_scale, max_grad_norm, out, stream=0):
+    """grad_accum, out: device addresses (ints); out receives a bf16opt_norm_result_t.
+    Allocates nothing (its scratch is a fixed static device array)."""
+    return load().bf16opt_grad_norm_static(c_vp(int(grad_accum)) if grad_accum else None, n, grad_scale,
+                                           max_grad_norm, c_vp(int(out)) if out else None,
+                                           c_vp(int(stream)) if stream else None)
 
 
 def bf16opt_error_string(code):

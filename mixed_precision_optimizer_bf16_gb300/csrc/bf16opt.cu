@@ -531,3 +531,152 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free one-shot norm (bf16opt_grad_norm_static).
+//
+// Some callers cannot call cudaMalloc: code running inside another
+// framework's launch path that is handed only a stream and a pre-planned
+// workspace (plugins, custom-op launchers), processes whose device memory is
+// already held by a caching allocator (a raw cudaMalloc can then fail), and
+// latency-sensitive loops that cannot take the device synchronisation that
+// cudaMalloc/cudaFree imply.  For them this entry point keeps its scratch --
+// one FP64 partial per 16,384-element chunk -- in a file-scope device array
+// of fixed size, so it never allocates.  The array exists once per GPU that
+// loads this library and stays allocated until the process exits.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+namespace {
+
+constexpr uint32_t kStaticMaxChunks = 65536;  // 512 KiB of FP64 partials
+constexpr int kStaticMaxDevices = 64;
+
+static __device__ __align__(256) double g_static_partials[kStaticMaxChunks];
+
+std::mutex g_static_mu;
+double *g_static_ptr[kStaticMaxDevices] = {};
+
+// Device address of g_static_partials on device `dev` (the current device),
+// looked up once per device.  In host code the array's name is only a host
+// stand-in, so the kernels must be given this address.
+int static_scratch(int dev, double **out, std::string &msg) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_partials);
+        if (e != cudaSuccess || !p) {
+            msg = std::string("cudaGetSymbolAddress of the static norm scratch failed: ") + cudaGetErrorString(e);
+            return BF16OPT_ERR_CUDA;
+        }
+        g_static_ptr[dev] = static_cast<double *>(p);
+    }
+    *out = g_static_ptr[dev];
+    return BF16OPT_OK;
+}
+
+// Partial sums of squares of implicit chunks [c*kChunk, min(n, (c+1)*kChunk)) of
+// a flat FP32 buffer: the same thread->element map, compensated sum and CTA tree
+// as the handle's norm pass over a one-range FLAT shard.
+template <int U>
+__global__ void __launch_bounds__(kThreads)
+k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, float gscale,
+                  double *__restrict__ partials) {
+    __shared__ double sh[kThreads / 32];
+    for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const uint64_t start = (uint64_t)c * kChunk;
+        const uint32_t len = (uint32_t)((n - start) < kChunk ? (n - start) : kChunk);
+        const float *a = acc + start;
+        uint32_t head = (4u - phase4_f32(a)) & 3u;
+        if (head > len) head = len;
+        const uint32_t nq = (len - head) >> 2;
+        const uint32_t tail0 = head + (nq << 2);
+        Comp cs = {0.f, 0.f};
+        for (uint32_t i = threadIdx.x; i < head; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
+        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
+        const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
+        for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
+            float4 av[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) av[u] = __ldcs(a4 + j);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = base + u * kThreads;
+                if (j < nq) {
+                    comp_add_sq(cs, __fmul_rn(av[u].x, gscale));
+                    comp_add_sq(cs, __fmul_rn(av[u].y, gscale));
+                    comp_add_sq(cs, __fmul_rn(av[u].z, gscale));
+                    comp_add_sq(cs, __fmul_rn(av[u].w, gscale));
+                }
+            }
+        }
+        const double tot = cta_sum((double)cs.s + (double)cs.c, sh);
+        if (threadIdx.x == 0) partials[c] = tot;
+    }
+}
+
+// Fixed-order sum of the partials, norm and clip coefficient into the caller's result.
+__global__ void __launch_bounds__(kFinalThreads)
+k_static_final(const double *__restrict__ partials, uint32_t n, float max_norm, bf16opt_norm_result_t *out) {
+    __shared__ double sh[kFinalThreads];
+    double s = 0.0;
+    for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) s += partials[i];
+    sh[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = kFinalThreads / 2; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double S = sh[0];
+        const double norm = sqrt(S);
+        double c = 1.0;
+        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
+        out->sumsq = S;
+        out->norm = norm;
+        out->clip_coef = c;
+    }
+}
+
+}  // namespace
+
+extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, float grad_scale, float max_grad_norm,
+                                        bf16opt_norm_result_t *out, void *stream) {
+    g_create_error.clear();
+    if (!out) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "grad_norm_static: out is NULL");
+    if (((uintptr_t)out & 7u) != 0) return fail(nullptr, BF16OPT_ERR_ALIGNMENT, "grad_norm_static: out must be 8-B aligned");
+    if (n > BF16OPT_STATIC_NORM_MAX_ELEMS)
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG,
+                    "grad_norm_static: n = " + std::to_string(n) + " exceeds the static scratch limit of " +
+                        std::to_string((unsigned long long)BF16OPT_STATIC_NORM_MAX_ELEMS) + " elements");
+    if (n > 0 && !grad_accum) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "grad_norm_static: grad_accum is NULL");
+    if (mis4(grad_accum)) return fail(nullptr, BF16OPT_ERR_ALIGNMENT, "grad_norm_static: grad_accum must be 4-B aligned");
+    if (!finite_f(grad_scale) || grad_scale == 0.f || !finite_f(max_grad_norm))
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "grad_norm_static: grad_scale and max_grad_norm must be finite, grad_scale != 0");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "grad_norm_static: no CUDA device");
+    }
+    if (dev < 0 || dev >= kStaticMaxDevices) return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "grad_norm_static: device ordinal too large");
+    double *partials = nullptr;
+    std::string msg;
+    int rc = static_scratch(dev, &partials, msg);
+    if (rc) return fail(nullptr, rc, msg);
+    int sms = 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+    const uint32_t nchunks = (uint32_t)((n + kChunk - 1) / kChunk);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (nchunks > 0) {
+        const uint32_t grid = std::min<uint32_t>(nchunks, (uint32_t)sms * 8u);
+        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, grad_scale, partials);
+    }
+    k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "grad_norm_static kernel launch");
+    return BF16OPT_OK;
+}

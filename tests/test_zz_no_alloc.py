@@ -1,0 +1,81 @@
+"""The allocation-free norm entry point (bf16opt_grad_norm_static).
+
+It serves callers that cannot call cudaMalloc (code inside another
+framework's launch path that only gets a stream, processes whose device
+memory sits in a caching allocator, loops that cannot take the device
+synchronisation of cudaMalloc/cudaFree): its scratch is a fixed static device
+array.  This file is collected last so that a run stopping at its first
+failure has already run every other test; it must pass alone in a fresh
+process as well as after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from mixed_precision_optimizer_bf16_gb300 import bf16opt as C  # noqa: E402
+from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat  # noqa: E402
+from synth import gpu as sgpu, workloads  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-6  # the norm tolerance of the parity tests
+
+
+def _read(res):
+    h = res.cpu().numpy().view(np.float64)
+    return float(h[0]), float(h[1]), float(h[2])
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+def test_static_norm_matches_handle_norm_twice():
+    C.load()
+    # 3,000,011 elements (ragged last chunk), misaligned by 1 element, clipping active
+    wl = workloads.custom(199, [3_000_011], gas=2, steps=1, grad_sigma=0.05, misalign=1)
+    flat = alloc_flat(wl.n, "cuda", wl.misalign)
+    sgpu.fill_master(wl, flat["master"])
+    for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+        flat[k].zero_()
+    g = torch.empty(wl.n + 64, dtype=torch.int16, device="cuda")[1:1 + wl.n]
+    opt = BF16Optimizer(wl.groups, flat=flat, max_grad_norm=1.0, grad_scale=0.5)
+    for k in range(2):
+        sgpu.fill_grad(wl, 0, k, g)
+        opt.accumulate(g, first=k == 0, last=k == 1)
+    ref_norm = opt.grad_norm(sync=True)
+    assert ref_norm > 1.0  # clipping is active
+
+    res = torch.zeros(3, dtype=torch.float64, device="cuda")   # caller-owned output
+    stream = torch.cuda.current_stream().cuda_stream
+    acc = flat["grad_accum"]
+    outs = []
+    for _ in range(2):  # two calls in a row share the static scratch
+        rc = C.bf16opt_grad_norm_static(acc.data_ptr(), acc.numel(), 0.5, 1.0, res.data_ptr(), stream)
+        assert rc == 0, C.bf16opt_last_error(None)
+        torch.cuda.synchronize()
+        outs.append(_read(res))
+        res.zero_()
+    for sumsq, norm, clip in outs:
+        assert abs(norm - ref_norm) <= REL * ref_norm
+        assert abs(sumsq - ref_norm ** 2) <= 2 * REL * ref_norm ** 2
+        assert abs(clip - 1.0 / ref_norm) <= REL / ref_norm
+    assert outs[0] == outs[1]
+
+    # a smaller second input right after a larger one: no stale partial is used
+    part = acc[:70_000]
+    rc = C.bf16opt_grad_norm_static(part.data_ptr(), part.numel(), 1.0, 1.0, res.data_ptr(), stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    s_small = float((part.double() ** 2).sum())
+    assert abs(_read(res)[0] - s_small) <= REL * s_small
+
+    # empty input and the size limit
+    assert C.bf16opt_grad_norm_static(0, 0, 1.0, 1.0, res.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    assert _read(res) == (0.0, 0.0, 1.0)
+    too_big = C.BF16OPT_STATIC_NORM_MAX_ELEMS + 1
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), too_big, 1.0, 1.0, res.data_ptr(), stream) == \
+        C.BF16OPT_ERR_INVALID_ARG
+    assert "exceeds" in C.bf16opt_last_error(None)
+    opt.close()
