@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--elements", type=int, default=0, help="time only the first N elements (profiling)")
     ap.add_argument("--no-defer", action="store_true", help="store the last micro-batch into acc (no deferral)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
@@ -166,6 +167,8 @@ def run_ours(args):
     C.load()
 
     wl = workloads.workload(args.workload)
+    if args.elements:
+        wl = workloads.prefix(wl, args.elements)
     assert wl.mode == "flat", "the timed workload is a flat shard"
     n, G = wl.n, wl.gas
     defer = not args.no_defer

@@ -114,16 +114,16 @@ bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 #define BF16K_ACC_U 8       // quads in flight per thread, accumulate family
 #endif
 #ifndef BF16K_STEP_U
-#define BF16K_STEP_U 4      // quads in flight per thread, fused step
+#define BF16K_STEP_U 2      // quads in flight per thread, fused step
 #endif
 #ifndef BF16K_MAX_CTAS_PER_SM
 #define BF16K_MAX_CTAS_PER_SM 64
 #endif
 
 template <class K>
-int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks) {
+int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
         per_sm = 1;
     if (per_sm > BF16K_MAX_CTAS_PER_SM) per_sm = BF16K_MAX_CTAS_PER_SM;
     const uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
@@ -164,8 +164,8 @@ int launch_step(bf16opt_t *h, const GroupTable &gtab, cudaStream_t st) {
     if (h->mode == BF16OPT_FLAT) {
         auto k = k_step<SRC, FlatGrads, U>;
         FlatGrads gt{h->defer_flat};
-        k<<<grid_for(h, k, h->n_chunks), kThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks, gt, gtab,
-                                                               h->norm_d, h->gscale);
+        k<<<grid_for(h, k, h->n_chunks, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks,
+                                                                                 gt, gtab, h->norm_d, h->gscale);
     } else {
         auto k = k_step<SRC, ListGrads, U>;
         for (const Batch &b : h->batches) {
@@ -175,8 +175,8 @@ int launch_step(bf16opt_t *h, const GroupTable &gtab, cudaStream_t st) {
             gt.pad = 0;
             for (uint32_t i = 0; i < (uint32_t)kListSlots; ++i)
                 gt.ptr[i] = (!h->defer_list.empty() && i < b.nslots) ? h->defer_list[b.slot0 + i] : nullptr;
-            k<<<grid_for(h, k, b.c1 - b.c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1, gt, gtab,
-                                                                   h->norm_d, h->gscale);
+            k<<<grid_for(h, k, b.c1 - b.c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1,
+                                                                                     gt, gtab, h->norm_d, h->gscale);
         }
     }
     cudaError_t e = cudaGetLastError();

@@ -34,15 +34,23 @@
 namespace bf16k {
 
 // Launch shape; the defaults were chosen by measurement on GB300 and can be
-// overridden at build time (-DBF16K_THREADS=..., -DBF16K_CHUNK=...).
-#ifndef BF16K_THREADS
-#define BF16K_THREADS 256
+// overridden at build time (-DBF16K_ACC_THREADS=..., -DBF16K_CHUNK=...).
+#ifndef BF16K_ACC_THREADS
+#define BF16K_ACC_THREADS 256
+#endif
+#ifndef BF16K_STEP_THREADS
+#define BF16K_STEP_THREADS 512
+#endif
+#ifndef BF16K_STEP_MIN_BLOCKS
+#define BF16K_STEP_MIN_BLOCKS 1
 #endif
 #ifndef BF16K_CHUNK
-#define BF16K_CHUNK 16384
+#define BF16K_CHUNK 32768
 #endif
-constexpr int kThreads = BF16K_THREADS;  // threads per CTA
-constexpr uint32_t kChunk = BF16K_CHUNK; // elements per chunk (multiple of 4)
+constexpr int kAccThreads = BF16K_ACC_THREADS;    // threads per CTA, accumulate / norm passes
+constexpr int kStepThreads = BF16K_STEP_THREADS;  // threads per CTA, fused step
+constexpr int kThreads = kAccThreads;
+constexpr uint32_t kChunk = BF16K_CHUNK;          // elements per chunk (multiple of 4)
 constexpr int kMaxGroups = 16;
 constexpr int kListSlots = 1024;     // gradient pointers per LIST-mode launch
 constexpr int kFinalThreads = 1024;
@@ -118,7 +126,7 @@ __device__ __forceinline__ void comp_add_sq(Comp &a, float x) {
     a.c = __fadd_rn(a.c, __fadd_rn(err, e));
 }
 
-// Deterministic CTA sum of one double per thread; result valid in thread 0.
+// Deterministic CTA sum of one double per thread (kThreads threads); result valid in thread 0.
 __device__ __forceinline__ double cta_sum(double x, double *sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -270,8 +278,10 @@ __device__ __forceinline__ AdamOut adam_elem(float e, float p, float m, float v,
     const float v1 = fmaf(G.b2, v, G.omb2 * gc * gc);
     const float den = fmaf(sqrtf(v1), G.inv_sqrt_bc2, G.eps); // sqrt(v_hat) + eps
     const float upd = __fdiv_rn(m1, den);
-    float p1 = fmaf(-G.decay, p, p);                          // decoupled weight decay
-    p1 = fmaf(-G.step_size, upd, p1);
+    // p - (lr wd p + step_size upd): the decay and the update are summed first
+    // (both are small next to p), so p itself is rounded once.
+    const float delta = fmaf(G.decay, p, G.step_size * upd);
+    const float p1 = __fsub_rn(p, delta);
     return {p1, m1, v1};
 }
 
@@ -284,7 +294,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // SRC_A: the gradient is the stored accumulator; SRC_AG: accumulator plus a
 // deferred last micro-batch g; SRC_G: a single deferred micro-batch.
 template <int SRC, class GT, int U>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
        GroupTable gtab, const NormState *__restrict__ ns, float gscale) {
     constexpr bool kReadG = SRC != SRC_A;
@@ -323,8 +333,8 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             v[i] = o.v;
             bf[i] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
         };
-        for (uint32_t i = threadIdx.x; i < head; i += kThreads) scalar(i);
-        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) scalar(i);
+        for (uint32_t i = threadIdx.x; i < head; i += kStepThreads) scalar(i);
+        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kStepThreads) scalar(i);
 
         const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
         const uint2 *g4 = reinterpret_cast<const uint2 *>(g + head);
@@ -332,12 +342,12 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
         float4 *m4 = reinterpret_cast<float4 *>(m + head);
         float4 *v4 = reinterpret_cast<float4 *>(v + head);
         uint2 *b4 = reinterpret_cast<uint2 *>(bf + head);
-        for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
+        for (uint32_t base = threadIdx.x; base < nq; base += kStepThreads * U) {
             float4 av[U], pv[U], mv[U], vv[U];
             uint2 gv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kThreads;
+                const uint32_t j = base + u * kStepThreads;
                 if (j < nq) {
                     if (kReadA) av[u] = __ldcs(a4 + j);
                     if (kReadG) gv[u] = __ldcs(g4 + j);
@@ -348,7 +358,7 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kThreads;
+                const uint32_t j = base + u * kStepThreads;
                 if (j < nq) {
                     float e[4];
                     if (SRC == SRC_G) {

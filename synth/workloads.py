@@ -140,6 +140,21 @@ def workload(i):
     return WORKLOADS[i]
 
 
+def prefix(wl, n):
+    """The first n elements of a flat workload (tensors cut at n), same ids and streams."""
+    ts, left = [], n
+    for t in wl.tensors:
+        if left <= 0:
+            break
+        k = min(t.numel, left)
+        ts.append(Tensor(t.name, k, t.decay, t.init))
+        left -= k
+    w = Workload(wl.id, f"{wl.name}, first {n} elements", ts, wl.mode, gas=wl.gas, steps=wl.steps,
+                 grad_sigma=wl.grad_sigma, zero_frac=wl.zero_frac, misalign=wl.misalign, max_norm=wl.max_norm)
+    w.groups = [dict(g) for g in wl.groups]
+    return w
+
+
 def custom(wl_id, sizes, decay=None, gas=2, steps=2, grad_sigma=1e-3, misalign=0, zero_frac=0.0,
            mode="flat", init=("normal", 0.02), max_norm=MAX_NORM):
     """Small ad-hoc workload for parity cases (ragged sizes, misalignment, GAS)."""
