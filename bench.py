@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "optimizer-step elements/s and achieved HBM GB/s (% of peak) on 1 GB300"
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_step_clip_edge_134m.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_step_scaled_bloom_prefix_134m.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "mixed_precision_optimizer_bf16_gb300", "csrc", f)
                   for f in ("kernels.cuh", "bf16opt.cu")]
 
