@@ -62,6 +62,18 @@ def rank_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value, device):
+    """Max of a float over all ranks of the default process group (the job's
+    time is its slowest rank's).  Plain value when there is no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -219,11 +231,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dev)
 
     # per-kernel device times (events on the launching stream)
     names = [f"accumulate_{k}" for k in range(G)] + ["norm_final", "step"]
@@ -340,11 +348,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     for _ in range(args.e2e_steps):
         one()
     torch.cuda.synchronize(dev)
-    dt = time.perf_counter() - t
-    if world > 1:
-        tt = torch.tensor([dt], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dt = float(tt.item())
+    dt = max_over_ranks(time.perf_counter() - t, dev)
     del host
     return {"value": round(n * args.e2e_steps * world / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,

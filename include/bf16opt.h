@@ -160,6 +160,33 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
  * replaces the groups' lr for this step only (for an LR schedule). */
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream);
 
+/* Learning-rate schedule of the training configuration ("单机多卡实战：
+ * Megatron-DeepSpeed训练类BLOOM模型全流程解析", section 3: lr 6e-5, min_lr 1e-6,
+ * lr_decay_style cosine, warmup_iters 500): linear warmup from 0 to the group's
+ * lr over warmup_steps, then cosine decay to min_lr_ratio * lr at decay_steps,
+ * then constant.  For the step number t >= 1 the factor on every group's lr is
+ *   t <= warmup_steps:                f = t / warmup_steps
+ *   warmup_steps < t <= decay_steps:  f = r + (1 - r) (1 + cos(pi (t - warmup_steps)
+ *                                              / (decay_steps - warmup_steps))) / 2
+ *   t > decay_steps:                  f = r                      (r = min_lr_ratio)
+ * evaluated in FP64. */
+typedef struct {
+    int64_t warmup_steps;  /* >= 0 */
+    int64_t decay_steps;   /* >= warmup_steps */
+    float min_lr_ratio;    /* in [0, 1] */
+    uint32_t reserved;     /* must be 0 */
+} bf16opt_lr_schedule_t;
+
+/* f(t) of the schedule above into *factor.  Host-only; needs no device or handle.
+ * Errors: INVALID_ARG for NULL pointers, t < 1 or an invalid schedule. */
+int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor);
+
+/* Attaches a copy of schedule `s` to the handle (NULL detaches it).  Every later
+ * bf16opt_step then uses lr = (lr_override[g] or the group's lr) * f(t) with t
+ * the step number of that step (the step counter plus one, so a resumed run
+ * that restored its counter with bf16opt_set_step continues the schedule). */
+int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
+
 /* Frees the library's scratch (waits for the device); the caller's buffers
  * are untouched.  NULL is accepted. */
 int bf16opt_destroy(bf16opt_t *h);

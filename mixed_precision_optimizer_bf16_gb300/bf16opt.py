@@ -51,6 +51,11 @@ class bf16opt_desc_t(ctypes.Structure):
                 ("max_grad_norm", c_f32), ("grad_scale", c_f32)]
 
 
+class bf16opt_lr_schedule_t(ctypes.Structure):
+    _fields_ = [("warmup_steps", ctypes.c_int64), ("decay_steps", ctypes.c_int64), ("min_lr_ratio", c_f32),
+                ("reserved", c_u32)]
+
+
 class bf16opt_norm_result_t(ctypes.Structure):
     _fields_ = [("sumsq", ctypes.c_double), ("norm", ctypes.c_double), ("clip_coef", ctypes.c_double)]
 
@@ -58,7 +63,7 @@ class bf16opt_norm_result_t(ctypes.Structure):
 # Functions the header declares (the tests check the library exports them all).
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
-           "bf16opt_grad_norm_static")
+           "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule")
 
 _lib = None
 
@@ -96,6 +101,11 @@ def load(path=None):
     L.bf16opt_error_string.argtypes = [ctypes.c_int]
     L.bf16opt_last_error.restype = ctypes.c_char_p
     L.bf16opt_last_error.argtypes = [hp]
+    L.bf16opt_lr_factor.restype = ctypes.c_int
+    L.bf16opt_lr_factor.argtypes = [ctypes.POINTER(bf16opt_lr_schedule_t), ctypes.c_int64,
+                                    ctypes.POINTER(ctypes.c_double)]
+    L.bf16opt_set_lr_schedule.restype = ctypes.c_int
+    L.bf16opt_set_lr_schedule.argtypes = [hp, ctypes.POINTER(bf16opt_lr_schedule_t)]
     L.bf16opt_grad_norm_static.restype = ctypes.c_int
     L.bf16opt_grad_norm_static.argtypes = [c_vp, c_u64, c_f32, c_f32, c_vp, c_vp]
     if path == _build.LIB_PATH:
@@ -145,6 +155,20 @@ def bf16opt_get_step(h):
 
 def bf16opt_set_step(h, t):
     return load().bf16opt_set_step(h, int(t))
+
+
+def bf16opt_lr_factor(sched, t):
+    f = ctypes.c_double(0.0)
+    rc = load().bf16opt_lr_factor(ctypes.byref(sched) if sched is not None else None, int(t), ctypes.byref(f))
+    return rc, f.value
+
+
+def bf16opt_set_lr_schedule(h, sched):
+    return load().bf16opt_set_lr_schedule(h, ctypes.byref(sched) if sched is not None else None)
+
+
+def lr_schedule(warmup_steps, decay_steps, min_lr_ratio):
+    return bf16opt_lr_schedule_t(int(warmup_steps), int(decay_steps), float(min_lr_ratio), 0)
 
 
 def bf16opt_grad_norm_static(grad_accum, n, grad_scale, max_grad_norm, out, stream=0):

@@ -53,6 +53,8 @@ struct bf16opt {
     const uint16_t *defer_flat = nullptr;
     std::vector<const uint16_t *> defer_list;
     int sm_count = 0;
+    bool has_sched = false;
+    bf16opt_lr_schedule_t sched{};
     std::string last_error;
 };
 
@@ -488,16 +490,51 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
     return BF16OPT_OK;
 }
 
+int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor) {
+    if (!s || !factor || t < 1) return BF16OPT_ERR_INVALID_ARG;
+    if (s->warmup_steps < 0 || s->decay_steps < s->warmup_steps || !(s->min_lr_ratio >= 0.f && s->min_lr_ratio <= 1.f) ||
+        s->reserved != 0)
+        return BF16OPT_ERR_INVALID_ARG;
+    const double r = (double)s->min_lr_ratio;
+    const int64_t w = s->warmup_steps, d = s->decay_steps;
+    if (t <= w) {
+        *factor = (double)t / (double)w;
+    } else if (t <= d) {
+        const double x = (double)(t - w) / (double)(d - w);
+        *factor = r + (1.0 - r) * 0.5 * (1.0 + std::cos(M_PI * x));
+    } else {
+        *factor = r;
+    }
+    return BF16OPT_OK;
+}
+
+int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!s) {
+        h->has_sched = false;
+        return BF16OPT_OK;
+    }
+    double f = 0.0;
+    if (bf16opt_lr_factor(s, 1, &f) != BF16OPT_OK)
+        return fail(h, BF16OPT_ERR_INVALID_ARG, "lr schedule: need 0 <= warmup_steps <= decay_steps, min_lr_ratio in [0, 1]");
+    h->sched = *s;
+    h->has_sched = true;
+    return BF16OPT_OK;
+}
+
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "step needs grad_norm first");
     const int64_t t = h->t + 1;
+    double sched_f = 1.0;
+    if (h->has_sched) bf16opt_lr_factor(&h->sched, t, &sched_f);
     GroupTable gtab;
     memset(&gtab, 0, sizeof gtab);
     for (size_t i = 0; i < h->groups.size(); ++i) {
         const bf16opt_group_t &g = h->groups[i];
-        const double lr = lr_override ? (double)lr_override[i] : (double)g.lr;
-        if (!std::isfinite(lr) || lr < 0.0) return fail(h, BF16OPT_ERR_INVALID_ARG, "lr_override must be finite and >= 0");
+        const double lr0 = lr_override ? (double)lr_override[i] : (double)g.lr;
+        if (!std::isfinite(lr0) || lr0 < 0.0) return fail(h, BF16OPT_ERR_INVALID_ARG, "lr_override must be finite and >= 0");
+        const double lr = lr0 * sched_f;
         const double b1 = g.beta1, b2 = g.beta2;
         const double bc1 = 1.0 - std::pow(b1, (double)t);
         const double bc2 = 1.0 - std::pow(b2, (double)t);

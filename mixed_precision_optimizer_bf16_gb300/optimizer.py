@@ -69,6 +69,11 @@ class BF16Optimizer:
         C.check(rc, self.h)
         return norm
 
+    def set_lr_schedule(self, warmup_steps, decay_steps, min_lr_ratio):
+        """Attach the warmup + cosine schedule (None detaches); see bf16opt_set_lr_schedule."""
+        self._sched = None if warmup_steps is None else C.lr_schedule(warmup_steps, decay_steps, min_lr_ratio)
+        return C.check(C.bf16opt_set_lr_schedule(self.h, self._sched), self.h)
+
     def step(self, lr=None, stream=None):
         lrs = None if lr is None else ([float(lr)] * len(self.groups) if not hasattr(lr, "__len__") else list(lr))
         return C.check(C.bf16opt_step(self.h, lrs, _stream_handle(stream)), self.h)

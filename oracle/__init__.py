@@ -52,6 +52,8 @@ def lib():
         L.orc_stream_sumsq.argtypes = [ctypes.POINTER(Stream), ctypes.c_uint32, u64, i32]
         L.orc_sample_run.argtypes = [ctypes.POINTER(Stream), vp, u64, vp, ctypes.POINTER(Group), vp,
                                      ctypes.c_uint32, vp, i64, vp, vp, vp, vp, vp]
+        L.orc_lr_at.restype = dbl
+        L.orc_lr_at.argtypes = [dbl, dbl, i64, i64, i64]
         for f in ("orc_f32_to_bf16_array", "orc_accumulate", "orc_adamw", "orc_sample_run"):
             getattr(L, f).restype = None
         _lib = L
@@ -157,3 +159,8 @@ def run_dense(p, grads_fn, ranges, groups, steps, gas, max_norm, grad_scale=1.0,
         for b, e, gi in ranges:
             adamw(p[b:e], m[b:e], v[b:e], pbf[b:e], acc[b:e], c, groups[gi], t0 + s + 1, grad_scale, threads)
     return dict(p=p, m=m, v=v, p_bf16=pbf, acc=acc, sumsq=sums, clip=clips)
+
+
+def lr_at(lr, min_lr, warmup, decay, t):
+    """Warmup + cosine learning rate at step number t >= 1."""
+    return lib().orc_lr_at(lr, min_lr, warmup, decay, t)

@@ -277,3 +277,15 @@ void orc_sample_run(const orc_stream_t *s, const uint64_t *idx, uint64_t k, cons
     }
     free(keys);
 }
+
+/* ------------------------------------------------------------- LR schedule */
+
+/* Warmup: lr grows linearly and reaches lr at step `warmup`.  Decay: the
+ * cosine half-wave from lr (just after warmup) to min_lr (at step `decay`):
+ * lr_t = min_lr + (lr - min_lr) (1 + cos(pi s)) / 2, s = (t - warmup)/(decay - warmup). */
+double orc_lr_at(double lr, double min_lr, int64_t warmup, int64_t decay, int64_t t) {
+    if (t <= warmup) return lr * (double)t / (double)warmup;
+    if (t > decay) return min_lr;
+    double s = (double)(t - warmup) / (double)(decay - warmup);
+    return min_lr + (lr - min_lr) * (1.0 + cos(3.14159265358979323846 * s)) / 2.0;
+}

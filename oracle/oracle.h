@@ -86,6 +86,12 @@ void orc_sample_run(const orc_stream_t *s, const uint64_t *idx, uint64_t k, cons
                     const double *clip, int64_t t0, float *p, float *m, float *v, uint16_t *p_bf16,
                     float *acc_out);
 
+/* Learning rate at step number t >= 1 ("单机多卡实战：Megatron-DeepSpeed训练类BLOOM
+ * 模型全流程解析", section 3: lr, min_lr, lr_decay_style cosine, warmup_iters):
+ * linear warmup 0 -> lr over `warmup` steps, cosine lr -> min_lr until step `decay`,
+ * then min_lr. */
+double orc_lr_at(double lr, double min_lr, int64_t warmup, int64_t decay, int64_t t);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,65 @@
+"""The benchmark's multi-rank path on CPU (gloo, world size 2).
+
+With N > 1 every rank runs an independent replica of the shard (no data-path
+collective); the job time is the maximum over ranks, rank 0 alone prints, and
+under --impl reference only rank 0 runs the CPU oracle.
+"""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
+    import bench
+    got = bench.max_over_ranks(10.0 + 5.0 * rank, "cpu")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        args = type("A", (), dict(steps=1, warmup=0, workload=1))()
+        if rank != 0:
+            bench.run_reference(args)   # non-zero ranks do no work and print nothing
+    dist.barrier()
+    q.put((rank, got, buf.getvalue(), bench.rank_info()))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_rank0_only_gloo():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [15.0, 15.0]          # both ranks see the slowest rank's time
+    assert res[1][2] == ""                               # rank 1 printed nothing
+    assert res[0][3] == (0, 2, 0) and res[1][3] == (1, 2, 1)
+
+
+def test_max_over_ranks_without_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5

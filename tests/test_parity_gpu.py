@@ -319,3 +319,68 @@ def test_inconsistent_alignment_falls_back_correctly():
     ref, scales = oracle_dense(wl, wl.steps)
     check_norms(norms, ref["sumsq"])
     compare(got, ref, scales, wl)
+
+
+# ------------------------------------------------------------ guard bands
+
+PAD = 256  # elements of canary on each side of every buffer
+
+
+def _guarded(n, dtype, mis):
+    """A buffer of n elements `mis` elements into an allocation whose 256-element
+    pads on both sides hold a NaN canary pattern."""
+    base = torch.empty(n + 2 * PAD + 8, dtype=dtype, device="cuda")
+    if dtype == torch.float32:
+        base.view(torch.int32).fill_(0x7FC00D0D)
+    else:
+        base.fill_(0x7FCD)
+    return base, base[PAD + mis:PAD + mis + n]
+
+
+def _pads_intact(base, n, mis):
+    a = base.view(torch.int32 if base.dtype == torch.float32 else torch.int16).cpu().numpy()
+    want = 0x7FC00D0D if base.dtype == torch.float32 else 0x7FCD
+    head, tail = a[:PAD + mis], a[PAD + mis + n:]
+    return bool((head == want).all() and (tail == want).all())
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_guard_bands_untouched(mode):
+    """No kernel writes outside its buffers and the gradients are only read."""
+    sizes = [16385, 3, 40001] if mode == "list" else [56389]
+    wl = workloads.custom(220, sizes, decay=[True, False, True][:len(sizes)], gas=3, steps=2, grad_sigma=0.1,
+                          misalign=3, mode=mode)
+    keys = ("master", "exp_avg", "exp_avg_sq", "grad_accum", "param_bf16")
+    bases, views = [], []
+    tensors = []
+    for t in wl.tensors:
+        d = {}
+        for k in keys:
+            b, v = _guarded(t.numel, torch.int16 if k == "param_bf16" else torch.float32, wl.misalign)
+            v.zero_()
+            bases.append((b, t.numel))
+            d[k] = v
+        sgpu.fill_master(workloads.custom(220, [t.numel]), d["master"])
+        d["group"] = 0
+        tensors.append(d)
+    gb, g = _guarded(wl.n, torch.int16, wl.misalign)
+    if mode == "flat":
+        opt = BF16Optimizer(wl.groups, flat=tensors[0], ranges=wl.ranges(), max_grad_norm=1.0)
+        garg = g
+    else:
+        opt = BF16Optimizer(wl.groups, tensors=tensors, max_grad_norm=1.0)
+        garg = [g[o:o + t.numel] for t, o in zip(wl.tensors, wl.offsets)]
+    for s in range(wl.steps):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, g)
+            before = g.clone()
+            opt.accumulate(garg, first=k == 0, last=k == wl.gas - 1, defer=(s == 1 and k == wl.gas - 1))
+        opt.grad_norm()
+        opt.step()
+        torch.cuda.synchronize()
+        assert torch.equal(g, before)                  # gradients are read-only
+    opt.close()
+    for b, n in bases:
+        assert _pads_intact(b, n, wl.misalign)
+    assert _pads_intact(gb, wl.n, wl.misalign)
