@@ -303,31 +303,37 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, opt, grads, G, defer, dev, world, n):
+def run_e2e(args, opt, grads, G, defer, dev, world, n, copy_streams=1):
     """Same step through the C ABI with every gradient copied from pinned host
-    memory (copy of micro-batch k+1 overlapping accumulate k on a second
-    stream) and the global norm read back to the host each step."""
+    memory inside the timed region -- on a copy stream, the copy of micro-batch
+    k+1 overlapping accumulate k (splitting a copy over several streams was
+    measured slower in steady state) -- and the global norm read back to the
+    host every step."""
     import torch
-    import torch.distributed as dist
 
     host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(G)]
     for k in range(G):
         host[k].copy_(grads[k])
     torch.cuda.synchronize(dev)
     comp = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
+    copies = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
+    bounds = [n * i // copy_streams for i in range(copy_streams + 1)]
     free = [None] * G
 
     def one():
-        norm = None
         for k in range(G):
-            with torch.cuda.stream(copy):
-                if free[k] is not None:
-                    copy.wait_event(free[k])
-                grads[k].copy_(host[k], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(copy)
-            comp.wait_event(ev)
+            done = []
+            for i, cs in enumerate(copies):
+                with torch.cuda.stream(cs):
+                    if free[k] is not None:
+                        cs.wait_event(free[k])
+                    lo, hi = bounds[i], bounds[i + 1]
+                    grads[k][lo:hi].copy_(host[k][lo:hi], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    done.append(ev)
+            for ev in done:
+                comp.wait_event(ev)
             opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=defer and k == G - 1, stream=comp)
             if not (defer and k == G - 1):
                 free[k] = torch.cuda.Event()
@@ -343,6 +349,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
         one()
     torch.cuda.synchronize(dev)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     t = time.perf_counter()
     for _ in range(args.e2e_steps):
@@ -352,7 +359,8 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     del host
     return {"value": round(n * args.e2e_steps * world / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
-            "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps}
+            "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps,
+            "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1), "copy_streams": copy_streams}
 
 
 # ------------------------------------------------------------ CPU oracle arm

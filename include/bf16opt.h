@@ -153,6 +153,24 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
  * call bf16opt_step; the library does not skip steps). */
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
 
+/* Multi-rank use.  Under ZeRO every rank owns one partition of the parameters
+ * and the clipping norm is global over all of them ("BLOOM 176B 训练技术概览",
+ * section 并行细节 / ZeRO: each GPU holds only its part; "企业官网建设流程全解析",
+ * section 4.3: the global norm).  The exchange is one FP64 scalar per rank and
+ * belongs to the caller's communication library:
+ *   1. bf16opt_grad_norm_local: in place of bf16opt_grad_norm, finishes this
+ *      rank's sum of squares, waits for `stream` and stores it in *local_sumsq;
+ *   2. the caller gathers every rank's value and sums them in rank order (the
+ *      same order on every rank, so every rank clips by the same bits);
+ *   3. bf16opt_set_global_sumsq: turns that sum into the norm and clip
+ *      coefficient on the device (enqueued on `stream`); bf16opt_step follows.
+ * Sequence: local needs a completed accumulation (as grad_norm); set_global
+ * needs local.  Errors: INVALID_ARG (NULL pointer), SEQUENCE (out of order),
+ * CUDA.  A non-finite local or global sum is passed through unchanged and
+ * reported as BF16OPT_WARN_NONFINITE (the caller decides whether to step). */
+int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq);
+int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream);
+
 /* One fused pass: clip, AdamW (t = t + 1, bias-corrected, decoupled
  * weight decay), FP32 master/moment update and bf16 parameter write
  * ("企业官网建设流程全解析", sections 1 and 3.3).

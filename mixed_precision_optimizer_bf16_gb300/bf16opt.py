@@ -63,7 +63,8 @@ class bf16opt_norm_result_t(ctypes.Structure):
 # Functions the header declares (the tests check the library exports them all).
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
-           "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule")
+           "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
+           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq")
 
 _lib = None
 
@@ -101,6 +102,10 @@ def load(path=None):
     L.bf16opt_error_string.argtypes = [ctypes.c_int]
     L.bf16opt_last_error.restype = ctypes.c_char_p
     L.bf16opt_last_error.argtypes = [hp]
+    L.bf16opt_grad_norm_local.restype = ctypes.c_int
+    L.bf16opt_grad_norm_local.argtypes = [hp, c_vp, ctypes.POINTER(ctypes.c_double)]
+    L.bf16opt_set_global_sumsq.restype = ctypes.c_int
+    L.bf16opt_set_global_sumsq.argtypes = [hp, ctypes.c_double, c_vp]
     L.bf16opt_lr_factor.restype = ctypes.c_int
     L.bf16opt_lr_factor.argtypes = [ctypes.POINTER(bf16opt_lr_schedule_t), ctypes.c_int64,
                                     ctypes.POINTER(ctypes.c_double)]
@@ -155,6 +160,16 @@ def bf16opt_get_step(h):
 
 def bf16opt_set_step(h, t):
     return load().bf16opt_set_step(h, int(t))
+
+
+def bf16opt_grad_norm_local(h, stream=0):
+    out = ctypes.c_double(0.0)
+    rc = load().bf16opt_grad_norm_local(h, c_vp(int(stream)) if stream else None, ctypes.byref(out))
+    return rc, out.value
+
+
+def bf16opt_set_global_sumsq(h, global_sumsq, stream=0):
+    return load().bf16opt_set_global_sumsq(h, float(global_sumsq), c_vp(int(stream)) if stream else None)
 
 
 def bf16opt_lr_factor(sched, t):

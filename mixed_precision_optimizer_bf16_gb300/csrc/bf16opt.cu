@@ -19,7 +19,7 @@ using namespace bf16k;
 
 namespace {
 
-enum State { S_IDLE = 0, S_ACC, S_ACC_DONE, S_ACC_DEFERRED, S_NORMED };
+enum State { S_IDLE = 0, S_ACC, S_ACC_DONE, S_ACC_DEFERRED, S_LOCAL_NORMED, S_NORMED };
 
 struct Batch {
     uint32_t c0, c1;          // chunk range
@@ -486,6 +486,40 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
             h->last_error = "gradient norm is not finite";
             return BF16OPT_WARN_NONFINITE;
         }
+    }
+    return BF16OPT_OK;
+}
+
+int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!local_sumsq) return fail(h, BF16OPT_ERR_INVALID_ARG, "grad_norm_local: local_sumsq is NULL");
+    if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
+        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm_local needs a completed accumulation");
+    double nrm = 0.0;
+    int rc = bf16opt_grad_norm(h, stream, &nrm);
+    if (rc < 0) return rc;
+    DeviceGuard dg(h->device);
+    double S = 0.0;
+    cudaError_t e;
+    if ((e = cudaMemcpy(&S, &h->norm_d->sumsq, sizeof(double), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(h, e, "reading the local sum of squares");
+    *local_sumsq = S;
+    h->state = S_LOCAL_NORMED;
+    return BF16OPT_OK;
+}
+
+int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_global_sumsq needs grad_norm_local first");
+    DeviceGuard dg(h->device);
+    if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
+    k_norm_from_sumsq<<<1, 32, 0, (cudaStream_t)stream>>>(global_sumsq, h->max_norm, h->norm_d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");
+    h->state = S_NORMED;
+    if (!std::isfinite(global_sumsq)) {
+        h->last_error = "global gradient norm is not finite";
+        return BF16OPT_WARN_NONFINITE;
     }
     return BF16OPT_OK;
 }

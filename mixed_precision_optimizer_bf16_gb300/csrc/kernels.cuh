@@ -265,6 +265,23 @@ k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, No
     }
 }
 
+// Norm and clip coefficient from a sum of squares given by the host (the
+// all-rank sum under ZeRO): same formula as k_norm_final.
+__global__ void k_norm_from_sumsq(double S, float max_norm, NormState *__restrict__ out) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const double norm = sqrt(S);
+        double c = 1.0;
+        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
+        const float hi = __double2float_rn(c);
+        out->sumsq = S;
+        out->norm = norm;
+        out->c_hi = hi;
+        out->c_lo = __double2float_rn(c - (double)hi);
+        out->finite = isfinite(S) ? 1 : 0;
+        out->pad = 0;
+    }
+}
+
 // ---------------------------------------------------------------------- step
 
 struct AdamOut {

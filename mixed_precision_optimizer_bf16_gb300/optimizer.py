@@ -33,6 +33,24 @@ def alloc_flat(n, device="cuda", misalign=0):
                 grad_accum=one(torch.float32), param_bf16=one(torch.int16))
 
 
+def global_sumsq(local, group=None):
+    """Sum of every rank's local sum of squares, in rank order (deterministic and
+    identical on all ranks); `local` when torch.distributed is not initialised."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(local)
+    world = dist.get_world_size(group)
+    backend = dist.get_backend(group)
+    dev = "cuda" if backend == "nccl" else "cpu"
+    mine = torch.tensor([float(local)], dtype=torch.float64, device=dev)
+    parts = [torch.empty_like(mine) for _ in range(world)]
+    dist.all_gather(parts, mine, group=group)
+    total = 0.0
+    for p in parts:
+        total += float(p.item())
+    return total
+
+
 class BF16Optimizer:
     """One handle over a FLAT shard (`flat` = dict of the five tensors, `ranges`)
     or a LIST of tensors (`tensors` = list of such dicts with a "group" key)."""
@@ -68,6 +86,16 @@ class BF16Optimizer:
         rc, norm = C.bf16opt_grad_norm(self.h, _stream_handle(stream), want_norm=sync)
         C.check(rc, self.h)
         return norm
+
+    def grad_norm_distributed(self, group=None, stream=None):
+        """Global norm over every rank's partition: this rank's FP64 sum of squares
+        is all-gathered and summed in rank order (identical on every rank), then
+        handed back to the library.  Returns the global norm."""
+        rc, local = C.bf16opt_grad_norm_local(self.h, _stream_handle(stream))
+        C.check(rc, self.h)
+        total = global_sumsq(local, group)
+        C.check(C.bf16opt_set_global_sumsq(self.h, total, _stream_handle(stream)), self.h)
+        return total ** 0.5
 
     def set_lr_schedule(self, warmup_steps, decay_steps, min_lr_ratio):
         """Attach the warmup + cosine schedule (None detaches); see bf16opt_set_lr_schedule."""

@@ -59,6 +59,35 @@ def test_max_over_ranks_and_rank0_only_gloo():
     assert res[0][3] == (0, 2, 0) and res[1][3] == (1, 2, 1)
 
 
+def _gather_worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
+    from mixed_precision_optimizer_bf16_gb300.optimizer import global_sumsq
+    # values whose sum depends on the order: rank order must be used on every rank
+    local = [1.0, 1e-16, -1.0][rank]
+    q.put((rank, global_sumsq(local)))
+    dist.destroy_process_group()
+
+
+def test_global_sumsq_rank_order_gloo():
+    """Each rank's local sum of squares is all-gathered and summed in rank order,
+    so every rank clips with the same bits."""
+    world = 3
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    want = (1.0 + 1e-16) + -1.0          # = 0.0 in rank order (1 + 1e-16 rounds to 1)
+    assert [r[1] for r in res] == [want] * world
+
+
 def test_max_over_ranks_without_group():
     sys.path.insert(0, ROOT)
     import bench

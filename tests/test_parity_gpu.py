@@ -384,3 +384,53 @@ def test_guard_bands_untouched(mode):
     for b, n in bases:
         assert _pads_intact(b, n, wl.misalign)
     assert _pads_intact(gb, wl.n, wl.misalign)
+
+
+# ------------------------------------------------------- multi-rank norm hooks
+
+@needs_cuda
+def test_two_partitions_share_the_global_norm():
+    """Two handles over the two halves of one shard stand for two ZeRO ranks
+    (their calls are sequenced on the host; no kernel waits on another).  Each
+    reports its local sum of squares, the sum in rank order is handed back to
+    both, and the two halves then step exactly like the whole shard would."""
+    wl = workloads.custom(230, [70_000, 333, 50_001], decay=[True, False, True], gas=3, steps=2, grad_sigma=0.2)
+    n, half = wl.n, 60_000
+    flat = alloc_flat(wl.n, "cuda")
+    sgpu.fill_master(wl, flat["master"])
+    for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+        flat[k].zero_()
+    parts = [{k: v[:half] for k, v in flat.items()}, {k: v[half:] for k, v in flat.items()}]
+
+    def local_ranges(lo, hi):
+        return [(max(b, lo) - lo, min(e, hi) - lo, g) for b, e, g in wl.ranges() if max(b, lo) < min(e, hi)]
+
+    opts = [BF16Optimizer(wl.groups, flat=parts[0], ranges=local_ranges(0, half)),
+            BF16Optimizer(wl.groups, flat=parts[1], ranges=local_ranges(half, n))]
+    g = torch.empty(n, dtype=torch.int16, device="cuda")
+    norms = []
+    for s in range(wl.steps):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, g)
+            opts[0].accumulate(g[:half], first=k == 0, last=k == wl.gas - 1)
+            opts[1].accumulate(g[half:], first=k == 0, last=k == wl.gas - 1)
+        locs = []
+        for o in opts:
+            rc, loc = C.bf16opt_grad_norm_local(o.h, torch.cuda.current_stream().cuda_stream)
+            assert rc == 0
+            locs.append(loc)
+        total = locs[0] + locs[1]
+        for o in opts:
+            assert C.bf16opt_set_global_sumsq(o.h, total, torch.cuda.current_stream().cuda_stream) == 0
+            o.step()
+        norms.append(total ** 0.5)
+    torch.cuda.synchronize()
+    got = dict(p=flat["master"].cpu().numpy(), m=flat["exp_avg"].cpu().numpy(),
+               v=flat["exp_avg_sq"].cpu().numpy(), acc=flat["grad_accum"].cpu().numpy(),
+               p_bf16=flat["param_bf16"].cpu().numpy().view(np.uint16))
+    for o in opts:
+        assert C.bf16opt_set_global_sumsq(o.h, 1.0) == C.BF16OPT_ERR_SEQUENCE
+        o.close()
+    ref, scales = oracle_dense(wl, wl.steps)
+    check_norms(norms, ref["sumsq"])
+    compare(got, ref, scales, wl)
