@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-variant", action="store_true", help="skip the all-deferred variant timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time of the CPU baseline")
     return ap.parse_args()
 
@@ -60,6 +61,26 @@ def parse():
 
 def rank_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def pass_bytes(pattern):
+    """Algorithmic HBM bytes per element of each accumulate call and of the fused
+    step for one step whose micro-batches are deferred per `pattern`: a stored
+    pass reads acc (if it holds earlier micro-batches) and every gradient it
+    folds (2 B each) and writes acc (4 B); a deferred LAST call reads the same
+    without writing (norm partials only); the step reads acc?, the pending
+    gradients and p, m, v (12 B) and writes p, m, v, bf16 (14 B)."""
+    acc_valid, pend, calls = False, 0, []
+    for k, d in enumerate(pattern):
+        last = k == len(pattern) - 1
+        if d:
+            pend += 1
+            calls.append(((4 if acc_valid else 0) + 2 * pend) if last else 0)
+        else:
+            calls.append((4 if acc_valid else 0) + 2 * (pend + 1) + 4)
+            acc_valid, pend = True, 0
+    step = (4 if acc_valid else 0) + 2 * pend + 12 + 14
+    return calls, step
 
 
 def max_over_ranks(value, device):
@@ -197,11 +218,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
-    def one_step(ev=None):
+    pattern = [False] * (G - 1) + [defer]
+
+    def one_step(ev=None, pat=pattern):
         if ev is not None:
             ev[0].record(stream)
         for k in range(G):
-            opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=defer and k == G - 1, stream=stream)
+            opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=pat[k], stream=stream)
             if ev is not None:
                 ev[1 + k].record(stream)
         opt.grad_norm(stream=stream)
@@ -239,17 +262,37 @@ def run_ours(args):
     for e in evs:
         for i, nm in enumerate(names):
             per[nm].append(e[i].elapsed_time(e[i + 1]))
-    bpe = {}
-    for k in range(G):
-        if k == 0:
-            bpe[f"accumulate_{k}"] = 2 if (defer and G == 1) else 6
-        elif k == G - 1 and defer:
-            bpe[f"accumulate_{k}"] = 6
-        else:
-            bpe[f"accumulate_{k}"] = 10
+    calls, step_b = pass_bytes(pattern)
+    bpe = {f"accumulate_{k}": calls[k] for k in range(G)}
     bpe["norm_final"] = 0
-    bpe["step"] = (32 if G > 1 else 30) if defer else 30
+    bpe["step"] = step_b
     peak, peak_src = measured_peak()
+
+    # variant: every micro-batch deferred (all GAS gradients stay resident; the
+    # accumulator is never stored; the norm pass and the step fold all of them)
+    variant = None
+    if G <= 8 and not args.no_variant:
+        vpat = [True] * G
+        for _ in range(2):
+            one_step(pat=vpat)
+        torch.cuda.synchronize(dev)
+        vk = max(1, min(K, 100))
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        v0.record(stream)
+        for _ in range(vk):
+            one_step(pat=vpat)
+        v1.record(stream)
+        torch.cuda.synchronize(dev)
+        vms = max_over_ranks(v0.elapsed_time(v1), dev) / vk
+        vcalls, vstep = pass_bytes(vpat)
+        vb = sum(vcalls) + vstep
+        variant = {"all_micro_batches_deferred": {
+            "value": round(n * world / (vms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(vms, 4), "steps": vk,
+            "bytes_per_elem_per_step": vb, "hbm_gbs": round(vb * n / (vms * 1e-3) / 1e9, 1),
+            "frac": round(vb * n / (vms * 1e-3) / 1e9 / peak, 4),
+            "note": "all GAS bf16 gradients stay resident until the step; same FP32 adds in the same order"}}
     kern = {}
     for nm in names:
         ms = statistics.mean(per[nm])
@@ -292,6 +335,7 @@ def run_ours(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes_per_launch": bpe["step"] * n},
         "kernels": kern,
+        "variants": variant,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
@@ -303,12 +347,12 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, opt, grads, G, defer, dev, world, n, copy_streams=1):
+def run_e2e(args, opt, grads, G, defer, dev, world, n):
     """Same step through the C ABI with every gradient copied from pinned host
-    memory inside the timed region -- on a copy stream, the copy of micro-batch
-    k+1 overlapping accumulate k (splitting a copy over several streams was
-    measured slower in steady state) -- and the global norm read back to the
-    host every step."""
+    memory inside the timed region -- whole-buffer copies on one copy stream
+    (copies of pinned slices, or one copy split over several streams, measured
+    slower), the copy of micro-batch k+1 overlapping accumulate k -- and the
+    global norm read back to the host every step."""
     import torch
 
     host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(G)]
@@ -316,24 +360,18 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n, copy_streams=1):
         host[k].copy_(grads[k])
     torch.cuda.synchronize(dev)
     comp = torch.cuda.current_stream(dev)
-    copies = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
-    bounds = [n * i // copy_streams for i in range(copy_streams + 1)]
+    copy = torch.cuda.Stream(dev)
     free = [None] * G
 
     def one():
         for k in range(G):
-            done = []
-            for i, cs in enumerate(copies):
-                with torch.cuda.stream(cs):
-                    if free[k] is not None:
-                        cs.wait_event(free[k])
-                    lo, hi = bounds[i], bounds[i + 1]
-                    grads[k][lo:hi].copy_(host[k][lo:hi], non_blocking=True)
-                    ev = torch.cuda.Event()
-                    ev.record(cs)
-                    done.append(ev)
-            for ev in done:
-                comp.wait_event(ev)
+            with torch.cuda.stream(copy):
+                if free[k] is not None:
+                    copy.wait_event(free[k])
+                grads[k].copy_(host[k], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy)
+            comp.wait_event(ev)
             opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=defer and k == G - 1, stream=comp)
             if not (defer and k == G - 1):
                 free[k] = torch.cuda.Event()
@@ -360,7 +398,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n, copy_streams=1):
     return {"value": round(n * args.e2e_steps * world / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
             "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps,
-            "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1), "copy_streams": copy_streams}
+            "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1)}
 
 
 # ------------------------------------------------------------ CPU oracle arm

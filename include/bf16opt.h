@@ -43,6 +43,8 @@
  *   added to); LAST marks the last one (the norm's partial sums are fused
  *   into that pass).  FIRST|LAST is a single micro-batch.  grad_norm may also
  *   follow a non-LAST accumulate; it then reads the accumulator once more.
+ *   Any micro-batch may carry BF16OPT_DEFER (see there); LAST|DEFER is the
+ *   plain "fuse the last micro-batch into the step" case.
  */
 #ifndef BF16OPT_H
 #define BF16OPT_H
@@ -70,9 +72,19 @@ extern "C" {
 
 #define BF16OPT_FIRST 1u /* first micro-batch of the step: acc = fp32(g) */
 #define BF16OPT_LAST 2u  /* last micro-batch: fuse the norm's partial sums into this pass */
-#define BF16OPT_DEFER 4u /* with LAST: do not store acc + g; the step kernel re-reads this
-                            micro-batch's gradient, which must stay valid and unchanged
-                            until bf16opt_step has run on the stream */
+#define BF16OPT_DEFER 4u /* keep this micro-batch's gradient instead of folding it into the
+                            FP32 accumulator now: it is folded (in micro-batch order) by
+                            the next pass that reads gradients -- the next accumulate
+                            without DEFER, or, if none follows before LAST, the norm and
+                            the step kernels, so the accumulator is never stored for it.
+                            The buffer must stay valid and unchanged until that pass has
+                            run on the stream (until bf16opt_step for deferred micro-
+                            batches of the last run).  At most BF16OPT_MAX_DEFERRED may be
+                            pending.  Same FP32 adds in the same order: bit-identical to
+                            not deferring; it trades 2 bytes/element of gradient memory
+                            per pending micro-batch for 8 bytes/element of HBM traffic */
+
+#define BF16OPT_MAX_DEFERRED 8
 
 #define BF16OPT_MAX_GROUPS 16
 
@@ -140,7 +152,8 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out);
  *         pointers (read during the call only).
  *   flags: BF16OPT_FIRST / BF16OPT_LAST / BF16OPT_DEFER (see above).
  * The gradient buffer is read on `stream`; it may be reused after the work
- * on `stream` is done, except under BF16OPT_DEFER (until bf16opt_step). */
+ * on `stream` is done, except under BF16OPT_DEFER (until the pass that folds
+ * it).  A DEFER beyond BF16OPT_MAX_DEFERRED pending is BF16OPT_ERR_INVALID_ARG. */
 int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list,
                        unsigned flags, void *stream);
 

@@ -25,6 +25,7 @@ BF16OPT_FIRST = 1
 BF16OPT_LAST = 2
 BF16OPT_DEFER = 4
 BF16OPT_MAX_GROUPS = 16
+BF16OPT_MAX_DEFERRED = 8
 BF16OPT_STATIC_NORM_MAX_ELEMS = 1 << 30
 
 c_u64, c_u32, c_i32, c_f32, c_vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p

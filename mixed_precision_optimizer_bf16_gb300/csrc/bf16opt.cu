@@ -10,6 +10,7 @@
 #include <cstring>
 #include <string>
 #include <algorithm>
+#include <type_traits>
 #include <vector>
 
 #include "../../include/bf16opt.h"
@@ -21,11 +22,6 @@ namespace {
 
 enum State { S_IDLE = 0, S_ACC, S_ACC_DONE, S_ACC_DEFERRED, S_LOCAL_NORMED, S_NORMED };
 
-struct Batch {
-    uint32_t c0, c1;          // chunk range
-    uint32_t slot0, nslots;   // LIST: tensors [slot0, slot0 + nslots)
-};
-
 thread_local std::string g_create_error;
 
 }  // namespace
@@ -36,7 +32,6 @@ struct bf16opt {
     uint64_t n = 0;
     uint32_t n_tensors = 0;
     std::vector<Seg> segs;
-    std::vector<Batch> batches;
     uint32_t n_chunks = 0;
     Seg *segs_d = nullptr;
     Chunk *chunks_d = nullptr;
@@ -47,11 +42,13 @@ struct bf16opt {
     float gscale = 1.0f;
     int64_t t = 0;
     State state = S_IDLE;
-    bool deferred = false;               // LAST|DEFER: the step re-reads the last micro-batch
-    bool defer_with_acc = false;         // ... and adds it to acc (micro-batches 0..G-2)
+    bool acc_valid = false;              // acc holds the fold of the micro-batches folded so far
     bool partials_ready = false;
-    const uint16_t *defer_flat = nullptr;
-    std::vector<const uint16_t *> defer_list;
+    // Deferred micro-batches not yet folded into acc, in micro-batch order:
+    // FLAT one pointer each, LIST one pointer per tensor each.
+    std::vector<const uint16_t *> pend_flat;
+    std::vector<std::vector<const uint16_t *>> pend_list;
+    std::vector<uint32_t> slot_chunk0;   // LIST: first chunk of tensor s (n_tensors + 1 entries)
     int sm_count = 0;
     bool has_sched = false;
     bf16opt_lr_schedule_t sched{};
@@ -132,57 +129,101 @@ int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThre
     return (int)std::max<uint64_t>(1, std::min<uint64_t>(g, nchunks));
 }
 
-// Launch one accumulate-family pass over every batch.
-template <int SRC, bool WRITE, bool NORM>
-int launch_accum(bf16opt_t *h, const uint16_t *gflat, const uint16_t *const *glist, cudaStream_t st) {
-    constexpr int U = BF16K_ACC_U;
+// Gradients a pass folds: K micro-batches (FLAT: one pointer each; LIST: one
+// per tensor each), in micro-batch order.
+struct FoldSet {
+    std::vector<const uint16_t *> flat;
+    std::vector<const std::vector<const uint16_t *> *> list;
+    size_t count() const { return flat.size() > list.size() ? flat.size() : list.size(); }
+};
+
+inline int kmax_for(size_t K) { return K <= 1 ? (int)K : (K <= 4 ? 4 : 8); }
+
+// Visit every launch of a pass: FLAT one launch over all chunks; LIST launches
+// of consecutive tensors such that K gradient pointers per tensor fit the
+// kernel parameter table.
+template <class F>
+int for_each_launch(bf16opt_t *h, const FoldSet &fs, F &&launch) {
+    const size_t K = fs.count();
+    if (K > (size_t)kMaxFold) return fail(h, BF16OPT_ERR_INVALID_ARG, "internal: more gradients than one pass folds");
     if (h->n_chunks == 0) return 0;
     if (h->mode == BF16OPT_FLAT) {
-        auto k = k_accum<SRC, WRITE, NORM, FlatGrads, U>;
-        FlatGrads gt{gflat};
-        k<<<grid_for(h, k, h->n_chunks), kThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks, gt,
-                                                               h->partials_d, h->gscale);
+        FlatGrads gt;
+        memset(&gt, 0, sizeof gt);
+        gt.k = (uint32_t)K;
+        for (size_t j = 0; j < K; ++j) gt.base[j] = fs.flat[j];
+        launch(gt, 0u, h->n_chunks);
     } else {
-        auto k = k_accum<SRC, WRITE, NORM, ListGrads, U>;
-        for (const Batch &b : h->batches) {
-            if (b.c1 == b.c0) continue;
+        const uint32_t per = (uint32_t)(kListSlots / (K ? K : 1));
+        for (uint32_t s0 = 0; s0 < h->n_tensors; s0 += per) {
+            const uint32_t s1 = std::min<uint32_t>(h->n_tensors, s0 + per);
+            const uint32_t c0 = h->slot_chunk0[s0], c1 = h->slot_chunk0[s1];
+            if (c1 == c0) continue;
             ListGrads gt;
-            gt.slot_base = b.slot0;
+            gt.slot_base = s0;
+            gt.nslots = s1 - s0;
+            gt.k = (uint32_t)K;
             gt.pad = 0;
-            for (uint32_t i = 0; i < (uint32_t)kListSlots; ++i)
-                gt.ptr[i] = (glist && i < b.nslots) ? glist[b.slot0 + i] : nullptr;
-            k<<<grid_for(h, k, b.c1 - b.c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1, gt,
-                                                                   h->partials_d, h->gscale);
+            for (size_t j = 0; j < K; ++j)
+                for (uint32_t i = 0; i < s1 - s0; ++i) gt.ptr[j * (s1 - s0) + i] = (*fs.list[j])[s0 + i];
+            launch(gt, c0, c1);
         }
     }
+    return 0;
+}
+
+template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
+int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
+    constexpr int U = KMAX <= 1 ? BF16K_ACC_U : (KMAX <= 4 ? 2 : 1);
+    int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
+        using GT = std::decay_t<decltype(gt)>;
+        auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
+        k<<<grid_for(h, k, c1 - c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt, h->partials_d, h->gscale);
+    });
+    if (rc) return rc;
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : cuda_fail(h, e, "accumulate kernel launch");
 }
 
-template <int SRC>
-int launch_step(bf16opt_t *h, const GroupTable &gtab, cudaStream_t st) {
-    constexpr int U = BF16K_STEP_U;
-    if (h->n_chunks == 0) return 0;
-    if (h->mode == BF16OPT_FLAT) {
-        auto k = k_step<SRC, FlatGrads, U>;
-        FlatGrads gt{h->defer_flat};
-        k<<<grid_for(h, k, h->n_chunks, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, 0, h->n_chunks,
-                                                                                 gt, gtab, h->norm_d, h->gscale);
-    } else {
-        auto k = k_step<SRC, ListGrads, U>;
-        for (const Batch &b : h->batches) {
-            if (b.c1 == b.c0) continue;
-            ListGrads gt;
-            gt.slot_base = b.slot0;
-            gt.pad = 0;
-            for (uint32_t i = 0; i < (uint32_t)kListSlots; ++i)
-                gt.ptr[i] = (!h->defer_list.empty() && i < b.nslots) ? h->defer_list[b.slot0 + i] : nullptr;
-            k<<<grid_for(h, k, b.c1 - b.c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, b.c0, b.c1,
-                                                                                     gt, gtab, h->norm_d, h->gscale);
-        }
+// fold(acc?, fs) -> (acc if WRITE) and (norm partials if NORM).
+template <bool WRITE, bool NORM>
+int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st) {
+    switch (kmax_for(fs.count())) {
+    case 0: return launch_accum_k<true, 0, false, true>(h, fs, st);   // norm over the stored acc
+    case 1: return has_acc ? launch_accum_k<true, 1, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 1, WRITE, NORM>(h, fs, st);
+    case 4: return has_acc ? launch_accum_k<true, 4, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 4, WRITE, NORM>(h, fs, st);
+    default: return has_acc ? launch_accum_k<true, 8, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 8, WRITE, NORM>(h, fs, st);
     }
+}
+
+template <bool HAS_ACC, int KMAX>
+int launch_step_k(bf16opt_t *h, const FoldSet &fs, const GroupTable &gtab, cudaStream_t st) {
+    constexpr int U = KMAX <= 1 ? BF16K_STEP_U : 1;
+    int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
+        using GT = std::decay_t<decltype(gt)>;
+        auto k = k_step<HAS_ACC, KMAX, GT, U>;
+        k<<<grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt, gtab,
+                                                                          h->norm_d, h->gscale);
+    });
+    if (rc) return rc;
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : cuda_fail(h, e, "step kernel launch");
+}
+
+int launch_step(bf16opt_t *h, bool has_acc, const FoldSet &fs, const GroupTable &gtab, cudaStream_t st) {
+    switch (kmax_for(fs.count())) {
+    case 0: return launch_step_k<true, 0>(h, fs, gtab, st);
+    case 1: return has_acc ? launch_step_k<true, 1>(h, fs, gtab, st) : launch_step_k<false, 1>(h, fs, gtab, st);
+    case 4: return has_acc ? launch_step_k<true, 4>(h, fs, gtab, st) : launch_step_k<false, 4>(h, fs, gtab, st);
+    default: return has_acc ? launch_step_k<true, 8>(h, fs, gtab, st) : launch_step_k<false, 8>(h, fs, gtab, st);
+    }
+}
+
+FoldSet pending_set(const bf16opt_t *h) {
+    FoldSet fs;
+    fs.flat = h->pend_flat;
+    for (const auto &v : h->pend_list) fs.list.push_back(&v);
+    return fs;
 }
 
 void free_scratch(bf16opt_t *h) {
@@ -234,7 +275,6 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
 
     std::vector<Seg> segs;
     std::vector<Interval> iv;
-    uint32_t n_slots = 0;
     if (d->mode == BF16OPT_FLAT) {
         const uint64_t n = d->n;
         if (n > 0) {
@@ -278,7 +318,6 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
             }
         }
         if (expect != n) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "FLAT: ranges do not cover [0, n)");
-        n_slots = 1;
     } else {
         if (d->n_tensors > 0 && !d->tensors) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "LIST: tensors is NULL");
         for (uint32_t i = 0; i < d->n_tensors; ++i) {
@@ -308,32 +347,25 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
             s.group = t.group;
             segs.push_back(s);
         }
-        n_slots = d->n_tensors;
     }
     if (overlaps(iv)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "state buffers overlap");
 
-    // Chunk table and launch batches (LIST: at most kListSlots tensors per launch).
+    // Chunk table: every segment cut into kChunk-element chunks, in segment order.
     std::vector<Chunk> chunks;
-    std::vector<Batch> batches;
-    {
-        Batch cur{0, 0, 0, 0};
-        for (uint32_t si = 0; si < segs.size(); ++si) {
-            const Seg &s = segs[si];
-            if (d->mode == BF16OPT_LIST && s.grad_slot - cur.slot0 >= (uint32_t)kListSlots) {
-                cur.c1 = (uint32_t)chunks.size();
-                cur.nslots = s.grad_slot - cur.slot0;
-                batches.push_back(cur);
-                cur = Batch{(uint32_t)chunks.size(), 0, s.grad_slot, 0};
-            }
-            for (uint64_t off = 0; off < s.numel; off += kChunk) {
-                if (chunks.size() >= 0xffffffffull)
-                    return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
-                chunks.push_back({off, si, (uint32_t)std::min<uint64_t>(kChunk, s.numel - off)});
-            }
+    for (uint32_t si = 0; si < segs.size(); ++si) {
+        const Seg &s = segs[si];
+        for (uint64_t off = 0; off < s.numel; off += kChunk) {
+            if (chunks.size() >= 0xffffffffull) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
+            chunks.push_back({off, si, (uint32_t)std::min<uint64_t>(kChunk, s.numel - off)});
         }
-        cur.c1 = (uint32_t)chunks.size();
-        cur.nslots = n_slots - cur.slot0;
-        batches.push_back(cur);
+    }
+    // LIST: first chunk of every tensor (empty tensors point at the next one's).
+    std::vector<uint32_t> slot_chunk0;
+    if (d->mode == BF16OPT_LIST) {
+        slot_chunk0.assign(d->n_tensors + 1, (uint32_t)chunks.size());
+        for (uint32_t c = (uint32_t)chunks.size(); c-- > 0;) slot_chunk0[segs[chunks[c].seg].grad_slot] = c;
+        for (uint32_t s = d->n_tensors; s-- > 0;)
+            if (slot_chunk0[s] > slot_chunk0[s + 1]) slot_chunk0[s] = slot_chunk0[s + 1];
     }
 
     // Device and scratch.
@@ -351,7 +383,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     h->n = d->mode == BF16OPT_FLAT ? d->n : 0;
     h->n_tensors = d->mode == BF16OPT_LIST ? d->n_tensors : 0;
     h->segs = segs;
-    h->batches = batches;
+    h->slot_chunk0 = slot_chunk0;
     h->n_chunks = (uint32_t)chunks.size();
     h->groups.assign(d->groups, d->groups + d->n_groups);
     h->max_norm = d->max_grad_norm;
@@ -410,7 +442,6 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     const bool first = flags & BF16OPT_FIRST, last = flags & BF16OPT_LAST, defer = flags & BF16OPT_DEFER;
     if (flags & ~(BF16OPT_FIRST | BF16OPT_LAST | BF16OPT_DEFER)) return fail(h, BF16OPT_ERR_INVALID_ARG, "unknown flag");
-    if (defer && !last) return fail(h, BF16OPT_ERR_INVALID_ARG, "BF16OPT_DEFER needs BF16OPT_LAST");
     if (!first && h->state != S_ACC) return fail(h, BF16OPT_ERR_SEQUENCE, "accumulate without FIRST outside an accumulation");
     if (h->mode == BF16OPT_FLAT) {
         if (grad_list) return fail(h, BF16OPT_ERR_INVALID_ARG, "FLAT: grad_list must be NULL");
@@ -425,37 +456,52 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
             if (mis2(g)) return fail(h, BF16OPT_ERR_ALIGNMENT, "LIST: gradient pointers must be 2-B aligned");
         }
     }
+    const size_t pending_before = first ? 0 : h->pend_flat.size() + h->pend_list.size();
+    if (defer && pending_before + 1 > (size_t)kMaxFold)
+        return fail(h, BF16OPT_ERR_INVALID_ARG, "at most 8 deferred micro-batches may be pending");
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
-    int rc = 0;
-    if (!last) {
-        rc = first ? launch_accum<SRC_G, true, false>(h, grad_flat, grad_list, st)
-                   : launch_accum<SRC_AG, true, false>(h, grad_flat, grad_list, st);
-    } else if (!defer) {
-        rc = first ? launch_accum<SRC_G, true, true>(h, grad_flat, grad_list, st)
-                   : launch_accum<SRC_AG, true, true>(h, grad_flat, grad_list, st);
-    } else {
-        rc = first ? launch_accum<SRC_G, false, true>(h, grad_flat, grad_list, st)
-                   : launch_accum<SRC_AG, false, true>(h, grad_flat, grad_list, st);
+
+    // A stored call with a full pending set: fold the pending set into acc first
+    // (same adds, same order), so no pass folds more than kMaxFold gradients.
+    if (!first && !defer && pending_before == (size_t)kMaxFold) {
+        int rc0 = launch_accum<true, false>(h, h->acc_valid, pending_set(h), st);
+        if (rc0) return rc0;
+        h->acc_valid = true;
+        h->pend_flat.clear();
+        h->pend_list.clear();
     }
+    // The gradients this call folds (or keeps): the pending ones, then this one.
+    const bool has_acc = first ? false : h->acc_valid;
+    std::vector<const uint16_t *> pf = first ? std::vector<const uint16_t *>() : h->pend_flat;
+    std::vector<std::vector<const uint16_t *>> pl = first ? std::vector<std::vector<const uint16_t *>>() : h->pend_list;
+    if (h->mode == BF16OPT_FLAT) pf.push_back(grad_flat);
+    else pl.emplace_back(grad_list, grad_list + h->n_tensors);
+    FoldSet fs;
+    fs.flat = pf;
+    for (const auto &v : pl) fs.list.push_back(&v);
+
+    int rc = 0;
+    if (!defer) rc = last ? launch_accum<true, true>(h, has_acc, fs, st) : launch_accum<true, false>(h, has_acc, fs, st);
+    else if (last) rc = launch_accum<false, true>(h, has_acc, fs, st);
     if (rc) return rc;
-    h->deferred = false;
-    h->defer_flat = nullptr;
-    h->defer_list.clear();
+
+    h->acc_valid = has_acc;
+    if (!defer) {
+        h->acc_valid = true;
+        h->pend_flat.clear();
+        h->pend_list.clear();
+    } else {
+        h->pend_flat = std::move(pf);
+        h->pend_list = std::move(pl);
+    }
     if (!last) {
         h->state = S_ACC;
         h->partials_ready = false;
-    } else if (!defer) {
-        h->state = S_ACC_DONE;
-        h->partials_ready = true;
     } else {
-        h->state = S_ACC_DEFERRED;
+        h->state = defer ? S_ACC_DEFERRED : S_ACC_DONE;
         h->partials_ready = true;
-        h->deferred = true;
-        h->defer_with_acc = !first;
-        h->defer_flat = grad_flat;
-        if (h->mode == BF16OPT_LIST) h->defer_list.assign(grad_list, grad_list + h->n_tensors);
     }
     return BF16OPT_OK;
 }
@@ -468,7 +514,8 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
     if (!h->partials_ready) {
-        int rc = launch_accum<SRC_A, false, true>(h, nullptr, nullptr, st);
+        // norm of fold(acc, pending) without storing it; the step folds the same set
+        int rc = launch_accum<false, true>(h, h->acc_valid, pending_set(h), st);
         if (rc) return rc;
     }
     k_norm_final<<<1, kFinalThreads, 0, st>>>(h->partials_d, h->n_chunks, h->max_norm, h->norm_d);
@@ -586,17 +633,13 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
     int rc;
-    if (h->deferred) {
-        rc = h->defer_with_acc ? launch_step<SRC_AG>(h, gtab, st) : launch_step<SRC_G>(h, gtab, st);
-    } else {
-        rc = launch_step<SRC_A>(h, gtab, st);
-    }
+    rc = launch_step(h, h->acc_valid, pending_set(h), gtab, st);
     if (rc) return rc;
     h->t = t;
     h->state = S_IDLE;
-    h->deferred = false;
-    h->defer_flat = nullptr;
-    h->defer_list.clear();
+    h->acc_valid = false;
+    h->pend_flat.clear();
+    h->pend_list.clear();
     h->partials_ready = false;
     return BF16OPT_OK;
 }

@@ -90,19 +90,23 @@ struct GroupTable {
     GroupK g[kMaxGroups];
 };
 
-// Gradient sources passed by value as kernel parameters.
+// Gradient sources passed by value as kernel parameters.  A pass folds k
+// micro-batch gradients (k <= kMaxFold) into the value in micro-batch order.
+constexpr int kMaxFold = 8;
 struct FlatGrads {
-    const uint16_t *base;
-    __device__ __forceinline__ const uint16_t *get(uint32_t) const { return base; }
+    const uint16_t *base[kMaxFold];   // micro-batch j's flat gradient buffer
+    uint32_t k;
+    uint32_t pad;
+    __device__ __forceinline__ const uint16_t *get(uint32_t, int j) const { return base[j]; }
 };
 struct ListGrads {
-    uint32_t slot_base;
+    uint32_t slot_base;               // first tensor of this launch
+    uint32_t nslots;                  // tensors in this launch (k * nslots <= kListSlots)
+    uint32_t k;
     uint32_t pad;
-    const uint16_t *ptr[kListSlots];
-    __device__ __forceinline__ const uint16_t *get(uint32_t s) const { return ptr[s - slot_base]; }
+    const uint16_t *ptr[kListSlots];  // ptr[j * nslots + (tensor - slot_base)]
+    __device__ __forceinline__ const uint16_t *get(uint32_t s, int j) const { return ptr[j * nslots + (s - slot_base)]; }
 };
-
-enum Src { SRC_G = 0, SRC_AG = 1, SRC_A = 2 };  // value = g | acc + g | acc
 
 // ------------------------------------------------------------------ helpers
 
@@ -149,76 +153,118 @@ __device__ __forceinline__ uint32_t phase4_b16(const void *p) { return (uint32_t
 
 // ---------------------------------------------------------------- accumulate
 
-// One pass over chunks [c0, c1): value = g | acc + g | acc (SRC), stored back
-// to acc if WRITE, and its per-chunk sum of squares (times gscale, rounded to
-// FP32 first) written to partials[c] if NORM.
-template <int SRC, bool WRITE, bool NORM, class GT, int U>
+// Folds the pass's gradients into one FP32 value per element, in micro-batch
+// order: v = acc (HAS_ACC) or the first gradient, then v = RN32(v + g_j) for
+// each further gradient -- the same FP32 adds, in the same order, as one
+// accumulate per micro-batch.
+template <bool HAS_ACC, int KMAX>
+__device__ __forceinline__ float fold_scalar(const float *a, const uint16_t *const *g, int K, uint32_t i) {
+    float v = HAS_ACC ? a[i] : __uint_as_float((uint32_t)g[0][i] << 16);
+#pragma unroll
+    for (int j = HAS_ACC ? 0 : 1; j < KMAX; ++j)
+        if (j < K) v = __fadd_rn(v, __uint_as_float((uint32_t)g[j][i] << 16));
+    return v;
+}
+
+template <bool HAS_ACC, int KMAX>
+__device__ __forceinline__ float4 fold_quad(const float4 &av, const uint2 *gv, int K) {
+    float4 r;
+    if (HAS_ACC) {
+        r = av;
+    } else {
+        r = make_float4(bf_lo(gv[0].x), bf_hi(gv[0].x), bf_lo(gv[0].y), bf_hi(gv[0].y));
+    }
+#pragma unroll
+    for (int j = HAS_ACC ? 0 : 1; j < KMAX; ++j) {
+        if (j < K) {
+            r.x = __fadd_rn(r.x, bf_lo(gv[j].x));
+            r.y = __fadd_rn(r.y, bf_hi(gv[j].x));
+            r.z = __fadd_rn(r.z, bf_lo(gv[j].y));
+            r.w = __fadd_rn(r.w, bf_hi(gv[j].y));
+        }
+    }
+    return r;
+}
+
+// Leading scalar elements before every FP32/bf16 pointer of the chunk is at a
+// 16-byte FP32 / 8-byte bf16 boundary, or `len` when they disagree (the chunk
+// then runs element-wise).
+template <int KMAX>
+__device__ __forceinline__ uint32_t chunk_head(const void *fp32_ptr, bool use_fp32, const uint16_t *const *g, int K,
+                                               uint32_t len) {
+    uint32_t ph = 0;
+    bool have = false, vec = true;
+    if (use_fp32) {
+        ph = phase4_f32(fp32_ptr);
+        have = true;
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < K) {
+            const uint32_t pg = phase4_b16(g[j]);
+            if (have && pg != ph) vec = false;
+            ph = pg;
+            have = true;
+        }
+    }
+    uint32_t head = vec ? ((4u - ph) & 3u) : len;
+    return head > len ? len : head;
+}
+
+// One pass over chunks [c0, c1): v = fold(acc?, g_0..g_{K-1}), stored back to
+// acc if WRITE, and its per-chunk sum of squares (times gscale, rounded to
+// FP32 first) written to partials[c] if NORM.  KMAX = 0 reads acc alone.
+template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM, class GT, int U>
 __global__ void __launch_bounds__(kThreads)
 k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
         double *__restrict__ partials, float gscale) {
     __shared__ double sh[kThreads / 32];
-    constexpr bool kReadG = SRC != SRC_A;
-    constexpr bool kReadA = SRC != SRC_G;
-    constexpr bool kUseA = kReadA || WRITE;
+    constexpr int KA = KMAX > 0 ? KMAX : 1;
+    const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         float *a = s.acc + ch.start;
-        const uint16_t *g = kReadG ? gt.get(s.grad_slot) + s.grad_off + ch.start : nullptr;
+        const uint16_t *g[KA];
+#pragma unroll
+        for (int j = 0; j < KA; ++j) g[j] = (j < K) ? gt.get(s.grad_slot, j) + s.grad_off + ch.start : nullptr;
         const uint32_t len = ch.len;
-
-        uint32_t ph = 0;
-        bool vec = true;
-        if (kReadG) ph = phase4_b16(g);
-        if (kUseA) {
-            const uint32_t pa = phase4_f32(a);
-            if (kReadG && pa != ph) vec = false;
-            ph = pa;
-        }
-        uint32_t head = vec ? ((4u - ph) & 3u) : len;
-        if (head > len) head = len;
+        const uint32_t head = chunk_head<KMAX>(a, HAS_ACC || WRITE, g, K, len);
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
 
         Comp cs = {0.f, 0.f};
         auto scalar = [&](uint32_t i) {
-            float val;
-            if (SRC == SRC_G) val = __uint_as_float((uint32_t)g[i] << 16);
-            else if (SRC == SRC_AG) val = __fadd_rn(a[i], __uint_as_float((uint32_t)g[i] << 16));
-            else val = a[i];
-            if (WRITE) a[i] = val;
-            if (NORM) comp_add_sq(cs, __fmul_rn(val, gscale));
+            const float v = fold_scalar<HAS_ACC, KMAX>(a, g, K, i);
+            if (WRITE) a[i] = v;
+            if (NORM) comp_add_sq(cs, __fmul_rn(v, gscale));
         };
         for (uint32_t i = threadIdx.x; i < head; i += kThreads) scalar(i);
         for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) scalar(i);
 
-        const uint2 *g4 = reinterpret_cast<const uint2 *>(g + head);
+        const uint2 *g4[KA];
+#pragma unroll
+        for (int j = 0; j < KA; ++j) g4[j] = reinterpret_cast<const uint2 *>(g[j] + head);
         float4 *a4 = reinterpret_cast<float4 *>(a + head);
         for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
-            uint2 gv[U];
+            uint2 gv[U][KA];
             float4 av[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kThreads;
-                if (j < nq) {
-                    if (kReadG) gv[u] = __ldcs(g4 + j);
-                    if (kReadA) av[u] = __ldcs(a4 + j);
+                const uint32_t q = base + u * kThreads;
+                if (q < nq) {
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j)
+                        if (j < K) gv[u][j] = __ldcs(g4[j] + q);
+                    if (HAS_ACC) av[u] = __ldcs(a4 + q);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kThreads;
-                if (j < nq) {
-                    float4 r;
-                    if (SRC == SRC_G) {
-                        r = make_float4(bf_lo(gv[u].x), bf_hi(gv[u].x), bf_lo(gv[u].y), bf_hi(gv[u].y));
-                    } else if (SRC == SRC_AG) {
-                        r = make_float4(__fadd_rn(av[u].x, bf_lo(gv[u].x)), __fadd_rn(av[u].y, bf_hi(gv[u].x)),
-                                        __fadd_rn(av[u].z, bf_lo(gv[u].y)), __fadd_rn(av[u].w, bf_hi(gv[u].y)));
-                    } else {
-                        r = av[u];
-                    }
-                    if (WRITE) __stcs(a4 + j, r);
+                const uint32_t q = base + u * kThreads;
+                if (q < nq) {
+                    const float4 r = fold_quad<HAS_ACC, KMAX>(av[u], gv[u], K);
+                    if (WRITE) __stcs(a4 + q, r);
                     if (NORM) {
                         comp_add_sq(cs, __fmul_rn(r.x, gscale));
                         comp_add_sq(cs, __fmul_rn(r.y, gscale));
@@ -307,43 +353,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Fused clip + AdamW + master update + bf16 cast over chunks [c0, c1).
-// SRC_A: the gradient is the stored accumulator; SRC_AG: accumulator plus a
-// deferred last micro-batch g; SRC_G: a single deferred micro-batch.
-template <int SRC, class GT, int U>
+// Fused clip + AdamW + master update + bf16 cast over chunks [c0, c1).  The
+// gradient is fold(acc?, g_0..g_{K-1}): the stored accumulator (KMAX = 0), or
+// the accumulator plus deferred micro-batches, or deferred micro-batches alone.
+template <bool HAS_ACC, int KMAX, class GT, int U>
 __global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
        GroupTable gtab, const NormState *__restrict__ ns, float gscale) {
-    constexpr bool kReadG = SRC != SRC_A;
-    constexpr bool kReadA = SRC != SRC_G;
+    constexpr int KA = KMAX > 0 ? KMAX : 1;
+    const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         const GroupK G = gtab.g[s.group];
         const float *a = s.acc + ch.start;
-        const uint16_t *g = kReadG ? gt.get(s.grad_slot) + s.grad_off + ch.start : nullptr;
+        const uint16_t *g[KA];
+#pragma unroll
+        for (int j = 0; j < KA; ++j) g[j] = (j < K) ? gt.get(s.grad_slot, j) + s.grad_off + ch.start : nullptr;
         float *p = s.p + ch.start;
         float *m = s.m + ch.start;
         float *v = s.v + ch.start;
         uint16_t *bf = s.bf + ch.start;
         const uint32_t len = ch.len;
 
+        uint32_t head = chunk_head<KMAX>(p, true, g, K, len);
         const uint32_t ph = phase4_f32(p);
-        bool vec = phase4_f32(m) == ph && phase4_f32(v) == ph && phase4_b16(bf) == ph;
-        if (kReadA) vec = vec && phase4_f32(a) == ph;
-        if (kReadG) vec = vec && phase4_b16(g) == ph;
-        uint32_t head = vec ? ((4u - ph) & 3u) : len;
-        if (head > len) head = len;
+        if (!(phase4_f32(m) == ph && phase4_f32(v) == ph && phase4_b16(bf) == ph && (!HAS_ACC || phase4_f32(a) == ph)))
+            head = len;
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
 
         auto scalar = [&](uint32_t i) {
-            float e;
-            if (SRC == SRC_G) e = __uint_as_float((uint32_t)g[i] << 16);
-            else if (SRC == SRC_AG) e = __fadd_rn(a[i], __uint_as_float((uint32_t)g[i] << 16));
-            else e = a[i];
-            e = __fmul_rn(e, gscale);
+            const float e = __fmul_rn(fold_scalar<HAS_ACC, KMAX>(a, g, K, i), gscale);
             const AdamOut o = adam_elem(e, p[i], m[i], v[i], c_hi, c_lo, G);
             p[i] = o.p;
             m[i] = o.m;
@@ -354,46 +396,42 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
         for (uint32_t i = tail0 + threadIdx.x; i < len; i += kStepThreads) scalar(i);
 
         const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
-        const uint2 *g4 = reinterpret_cast<const uint2 *>(g + head);
+        const uint2 *g4[KA];
+#pragma unroll
+        for (int j = 0; j < KA; ++j) g4[j] = reinterpret_cast<const uint2 *>(g[j] + head);
         float4 *p4 = reinterpret_cast<float4 *>(p + head);
         float4 *m4 = reinterpret_cast<float4 *>(m + head);
         float4 *v4 = reinterpret_cast<float4 *>(v + head);
         uint2 *b4 = reinterpret_cast<uint2 *>(bf + head);
         for (uint32_t base = threadIdx.x; base < nq; base += kStepThreads * U) {
             float4 av[U], pv[U], mv[U], vv[U];
-            uint2 gv[U];
+            uint2 gv[U][KA];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kStepThreads;
-                if (j < nq) {
-                    if (kReadA) av[u] = __ldcs(a4 + j);
-                    if (kReadG) gv[u] = __ldcs(g4 + j);
-                    pv[u] = __ldcs(p4 + j);
-                    mv[u] = __ldcs(m4 + j);
-                    vv[u] = __ldcs(v4 + j);
+                const uint32_t q = base + u * kStepThreads;
+                if (q < nq) {
+                    if (HAS_ACC) av[u] = __ldcs(a4 + q);
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j)
+                        if (j < K) gv[u][j] = __ldcs(g4[j] + q);
+                    pv[u] = __ldcs(p4 + q);
+                    mv[u] = __ldcs(m4 + q);
+                    vv[u] = __ldcs(v4 + q);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint32_t j = base + u * kStepThreads;
-                if (j < nq) {
-                    float e[4];
-                    if (SRC == SRC_G) {
-                        e[0] = bf_lo(gv[u].x); e[1] = bf_hi(gv[u].x); e[2] = bf_lo(gv[u].y); e[3] = bf_hi(gv[u].y);
-                    } else if (SRC == SRC_AG) {
-                        e[0] = __fadd_rn(av[u].x, bf_lo(gv[u].x)); e[1] = __fadd_rn(av[u].y, bf_hi(gv[u].x));
-                        e[2] = __fadd_rn(av[u].z, bf_lo(gv[u].y)); e[3] = __fadd_rn(av[u].w, bf_hi(gv[u].y));
-                    } else {
-                        e[0] = av[u].x; e[1] = av[u].y; e[2] = av[u].z; e[3] = av[u].w;
-                    }
-                    const AdamOut o0 = adam_elem(__fmul_rn(e[0], gscale), pv[u].x, mv[u].x, vv[u].x, c_hi, c_lo, G);
-                    const AdamOut o1 = adam_elem(__fmul_rn(e[1], gscale), pv[u].y, mv[u].y, vv[u].y, c_hi, c_lo, G);
-                    const AdamOut o2 = adam_elem(__fmul_rn(e[2], gscale), pv[u].z, mv[u].z, vv[u].z, c_hi, c_lo, G);
-                    const AdamOut o3 = adam_elem(__fmul_rn(e[3], gscale), pv[u].w, mv[u].w, vv[u].w, c_hi, c_lo, G);
-                    __stcs(p4 + j, make_float4(o0.p, o1.p, o2.p, o3.p));
-                    __stcs(m4 + j, make_float4(o0.m, o1.m, o2.m, o3.m));
-                    __stcs(v4 + j, make_float4(o0.v, o1.v, o2.v, o3.v));
-                    __stcs(b4 + j, make_uint2(pack_bf16x2(o0.p, o1.p), pack_bf16x2(o2.p, o3.p)));
+                const uint32_t q = base + u * kStepThreads;
+                if (q < nq) {
+                    const float4 e = fold_quad<HAS_ACC, KMAX>(av[u], gv[u], K);
+                    const AdamOut o0 = adam_elem(__fmul_rn(e.x, gscale), pv[u].x, mv[u].x, vv[u].x, c_hi, c_lo, G);
+                    const AdamOut o1 = adam_elem(__fmul_rn(e.y, gscale), pv[u].y, mv[u].y, vv[u].y, c_hi, c_lo, G);
+                    const AdamOut o2 = adam_elem(__fmul_rn(e.z, gscale), pv[u].z, mv[u].z, vv[u].z, c_hi, c_lo, G);
+                    const AdamOut o3 = adam_elem(__fmul_rn(e.w, gscale), pv[u].w, mv[u].w, vv[u].w, c_hi, c_lo, G);
+                    __stcs(p4 + q, make_float4(o0.p, o1.p, o2.p, o3.p));
+                    __stcs(m4 + q, make_float4(o0.m, o1.m, o2.m, o3.m));
+                    __stcs(v4 + q, make_float4(o0.v, o1.v, o2.v, o3.v));
+                    __stcs(b4 + q, make_uint2(pack_bf16x2(o0.p, o1.p), pack_bf16x2(o2.p, o3.p)));
                 }
             }
         }

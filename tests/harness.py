@@ -57,7 +57,18 @@ class GpuShard:
     """Device state of a workload + its bf16opt handle."""
 
     def __init__(self, wl, grad_scale=1.0, defer=False):
-        self.wl, self.defer = wl, defer
+        """defer: False, True (defer the last micro-batch only) or a per-micro-batch
+        list of flags (deferred gradients then get buffers of their own)."""
+        self.wl = wl
+        G = wl.gas
+        if defer is True:
+            self.pattern = [False] * (G - 1) + [True]
+        elif not defer:
+            self.pattern = [False] * G
+        else:
+            self.pattern = [bool(x) for x in defer]
+            assert len(self.pattern) == G
+        self.defer = self.pattern[-1]
         self.norms = []
         if wl.mode == "flat":
             self.flat = alloc_flat(wl.n, "cuda", wl.misalign)
@@ -83,19 +94,22 @@ class GpuShard:
             del master
             self.opt = BF16Optimizer(wl.groups, tensors=self.tensors, max_grad_norm=wl.max_norm,
                                      grad_scale=grad_scale)
-        self.gbuf = _alloc(wl.n, torch.int16, wl.misalign)
+        nbuf = wl.gas if any(self.pattern[:-1]) else 1
+        self.gbufs = [_alloc(wl.n, torch.int16, wl.misalign) for _ in range(nbuf)]
+        self.gbuf = self.gbufs[0]
 
-    def grads_arg(self):
+    def grads_arg(self, buf=None):
+        buf = self.gbuf if buf is None else buf
         if self.wl.mode == "flat":
-            return self.gbuf
-        return [self.gbuf[off:off + t.numel] for t, off in zip(self.wl.tensors, self.wl.offsets)]
+            return buf
+        return [buf[off:off + t.numel] for t, off in zip(self.wl.tensors, self.wl.offsets)]
 
     def run_step(self, step):
         wl = self.wl
         for k in range(wl.gas):
-            sgpu.fill_grad(wl, step, k, self.gbuf)
-            self.opt.accumulate(self.grads_arg(), first=(k == 0), last=(k == wl.gas - 1),
-                                defer=self.defer and k == wl.gas - 1)
+            buf = self.gbufs[k % len(self.gbufs)]
+            sgpu.fill_grad(wl, step, k, buf)
+            self.opt.accumulate(self.grads_arg(buf), first=(k == 0), last=(k == wl.gas - 1), defer=self.pattern[k])
         norm = self.opt.grad_norm(sync=True)
         self.opt.step()
         self.norms.append(norm)

@@ -36,10 +36,11 @@ def dense_parity(wl, defer=False, grad_scale=1.0):
     sh.run(wl.steps)
     got = sh.states()
     norms = list(sh.norms)
+    last_deferred = sh.defer
     sh.close()
     ref, scales = oracle_dense(wl, wl.steps, grad_scale)
     check_norms(norms, ref["sumsq"])
-    return compare(got, ref, scales, wl, grad_scale, check_acc=not defer)
+    return compare(got, ref, scales, wl, grad_scale, check_acc=not last_deferred)
 
 
 def sampled_parity(wl, defer=False, k=1 << 15):
@@ -200,7 +201,8 @@ def test_sequence_errors():
     assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
     assert C.bf16opt_grad_norm(h)[0] == C.BF16OPT_ERR_SEQUENCE
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, 0) == C.BF16OPT_ERR_SEQUENCE
-    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, 8) == C.BF16OPT_ERR_INVALID_ARG   # unknown flag
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST) == 0
     assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == 0
@@ -434,3 +436,45 @@ def test_two_partitions_share_the_global_norm():
     ref, scales = oracle_dense(wl, wl.steps)
     check_norms(norms, ref["sumsq"])
     compare(got, ref, scales, wl)
+
+
+# ------------------------------------------------- deferred micro-batches
+
+DEFER_PATTERNS = [
+    [True, True, True, True],                  # nothing stored: norm and step fold all four
+    [True, False, True, True],                 # pairs: one stored pass, then the last two deferred
+    [True, False, False, False],
+    [False, True, True, False],
+    [True, True, False],
+    [True] * 5,                                # five pending (8-wide kernels, runtime count 5)
+    [True] * 8,                                # the maximum
+    [False, True, False, True, False, True, True],
+]
+
+
+@needs_cuda
+@pytest.mark.parametrize("pat", range(len(DEFER_PATTERNS)))
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_deferred_patterns(pat, mode):
+    """Deferring any micro-batches folds the same FP32 adds in the same order."""
+    pattern = DEFER_PATTERNS[pat]
+    sizes = [50_001, 3, 16_384, 777] if mode == "flat" else [20_000, 5, 16_385, 1200]
+    wl = workloads.custom(240 + pat, sizes, decay=[True, False, True, False], gas=len(pattern), steps=2,
+                          grad_sigma=0.05, misalign=pat % 4, mode=mode)
+    st = dense_parity(wl, defer=pattern)
+    print(mode, pattern, st)
+
+
+@needs_cuda
+def test_too_many_deferred():
+    flat, h = _raw_flat(4096)
+    g = torch.zeros(4096, dtype=torch.int16, device="cuda")
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST | C.BF16OPT_DEFER) == 0
+    for _ in range(C.BF16OPT_MAX_DEFERRED - 1):
+        assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == 0
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, 0) == 0      # a stored pass folds all nine
+    assert C.bf16opt_grad_norm(h, 0, True) == (0, 0.0)
+    assert C.bf16opt_step(h) == 0
+    torch.cuda.synchronize()
+    C.bf16opt_destroy(h)
