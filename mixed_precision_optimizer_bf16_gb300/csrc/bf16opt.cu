@@ -115,6 +115,18 @@ bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 #ifndef BF16K_STEP_U
 #define BF16K_STEP_U 2      // quads in flight per thread, fused step
 #endif
+#ifndef BF16K_FOLD4_ACC_U
+#define BF16K_FOLD4_ACC_U 4  // quads in flight, passes folding 2-4 gradients
+#endif
+#ifndef BF16K_FOLD8_ACC_U
+#define BF16K_FOLD8_ACC_U 1  // quads in flight, passes folding 5-8 gradients
+#endif
+#ifndef BF16K_FOLD4_STEP_U
+#define BF16K_FOLD4_STEP_U 2  // quads in flight, fused step folding 2-4 gradients
+#endif
+#ifndef BF16K_FOLD8_STEP_U
+#define BF16K_FOLD8_STEP_U 1  // quads in flight, fused step folding 5-8 gradients
+#endif
 #ifndef BF16K_MAX_CTAS_PER_SM
 #define BF16K_MAX_CTAS_PER_SM 64
 #endif
@@ -174,7 +186,7 @@ int for_each_launch(bf16opt_t *h, const FoldSet &fs, F &&launch) {
 
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
 int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
-    constexpr int U = KMAX <= 1 ? BF16K_ACC_U : (KMAX <= 4 ? 2 : 1);
+    constexpr int U = KMAX <= 1 ? BF16K_ACC_U : (KMAX <= 4 ? BF16K_FOLD4_ACC_U : BF16K_FOLD8_ACC_U);
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
@@ -198,7 +210,7 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
 
 template <bool HAS_ACC, int KMAX>
 int launch_step_k(bf16opt_t *h, const FoldSet &fs, const GroupTable &gtab, cudaStream_t st) {
-    constexpr int U = KMAX <= 1 ? BF16K_STEP_U : 1;
+    constexpr int U = KMAX <= 1 ? BF16K_STEP_U : (KMAX <= 4 ? BF16K_FOLD4_STEP_U : BF16K_FOLD8_STEP_U);
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
