@@ -36,6 +36,9 @@
  *     bf16opt_last_error() gives a one-line message.
  *   - A handle is bound to the device that was current at bf16opt_create and
  *     is not thread-safe: use one handle from one host thread at a time.
+ *   - Results are deterministic and do not depend on the launch grid (the
+ *     environment variable BF16OPT_MAX_GRID, read at create, caps the CTAs
+ *     per launch; it exists to test exactly that).
  *
  * Sequence per optimizer step (checked on the host; BF16OPT_ERR_SEQUENCE):
  *   accumulate(FIRST) ... accumulate(LAST) -> grad_norm -> step

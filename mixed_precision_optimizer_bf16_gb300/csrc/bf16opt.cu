@@ -7,6 +7,7 @@
 // path is computed by those kernels.
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <algorithm>
@@ -50,6 +51,7 @@ struct bf16opt {
     std::vector<std::vector<const uint16_t *>> pend_list;
     std::vector<uint32_t> slot_chunk0;   // LIST: first chunk of tensor s (n_tensors + 1 entries)
     int sm_count = 0;
+    int max_grid = 0;                    // optional cap on CTAs per launch (BF16OPT_MAX_GRID), 0 = none
     bool has_sched = false;
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
@@ -137,7 +139,8 @@ int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThre
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
         per_sm = 1;
     if (per_sm > BF16K_MAX_CTAS_PER_SM) per_sm = BF16K_MAX_CTAS_PER_SM;
-    const uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
+    uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
+    if (h->max_grid > 0 && g > (uint64_t)h->max_grid) g = (uint64_t)h->max_grid;
     return (int)std::max<uint64_t>(1, std::min<uint64_t>(g, nchunks));
 }
 
@@ -402,6 +405,9 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     h->gscale = d->grad_scale;
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || h->sm_count < 1)
         h->sm_count = 1;
+    // Optional cap on the CTAs of every launch (testing that results do not
+    // depend on the grid: the norm's partials are per chunk, not per CTA).
+    if (const char *mg = std::getenv("BF16OPT_MAX_GRID")) h->max_grid = std::max(0, std::atoi(mg));
 
     cudaError_t e = cudaSuccess;
     const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());

@@ -478,3 +478,25 @@ def test_too_many_deferred():
     assert C.bf16opt_step(h) == 0
     torch.cuda.synchronize()
     C.bf16opt_destroy(h)
+
+
+@needs_cuda
+def test_results_do_not_depend_on_the_grid(monkeypatch):
+    """The norm's partials belong to chunks, not CTAs, and the step is
+    element-wise: one CTA per launch gives the same bits as the full grid."""
+    wl = workloads.custom(250, [300_001, 4097, 77], decay=[True, False, True], gas=3, steps=2, grad_sigma=0.1,
+                          misalign=1)
+    outs = []
+    for cap in (None, "1", "7"):
+        if cap is None:
+            monkeypatch.delenv("BF16OPT_MAX_GRID", raising=False)
+        else:
+            monkeypatch.setenv("BF16OPT_MAX_GRID", cap)
+        sh = GpuShard(wl, defer=[True, False, True])
+        sh.run(wl.steps)
+        outs.append((sh.states(), list(sh.norms)))
+        sh.close()
+    for st, nr in outs[1:]:
+        assert nr == outs[0][1]
+        for k in ("p", "m", "v", "p_bf16"):
+            assert np.array_equal(st[k].view(np.uint8), outs[0][0][k].view(np.uint8))
