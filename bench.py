@@ -356,7 +356,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": K * (G + 2),
+        "gpu_launches": K * (sum(1 for c in calls if c) + 3),
     }
     print(json.dumps(line))
     sys.stdout.flush()

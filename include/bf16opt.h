@@ -187,6 +187,14 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
 int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq);
 int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream);
 
+/* CUDA graphs.  The step counter, the hyper-parameters and the LR schedule
+ * live on the device and bf16opt_step computes its scalars there, so the
+ * sequence accumulate ... -> grad_norm (host_norm = NULL) -> step, captured
+ * once on a stream, replays as later steps (same gradient buffers; lr_override
+ * values are frozen into the capture).  Calls that synchronise (grad_norm with
+ * host_norm, grad_norm_local, get/set_step, set_lr_schedule, create, destroy)
+ * must stay outside a capture. */
+
 /* One fused pass: clip, AdamW (t = t + 1, bias-corrected, decoupled
  * weight decay), FP32 master/moment update and bf16 parameter write
  * ("企业官网建设流程全解析", sections 1 and 3.3).
@@ -225,8 +233,9 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
  * are untouched.  NULL is accepted. */
 int bf16opt_destroy(bf16opt_t *h);
 
-/* Step counter t (number of completed bf16opt_step calls), for checkpoint
- * and resume: restore the caller's buffers and set_step(t) to continue. */
+/* Step counter t (number of completed steps, kept on the device; both calls
+ * synchronise), for checkpoint and resume: restore the caller's buffers and
+ * set_step(t) to continue. */
 int bf16opt_get_step(const bf16opt_t *h, int64_t *t);
 int bf16opt_set_step(bf16opt_t *h, int64_t t);
 

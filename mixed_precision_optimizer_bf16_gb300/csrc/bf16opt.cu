@@ -12,6 +12,7 @@
 #include <string>
 #include <algorithm>
 #include <type_traits>
+#include <utility>
 #include <vector>
 
 #include "../../include/bf16opt.h"
@@ -38,6 +39,8 @@ struct bf16opt {
     Chunk *chunks_d = nullptr;
     double *partials_d = nullptr;
     NormState *norm_d = nullptr;
+    StepParams *params_d = nullptr;      // hyper-parameters + schedule (device)
+    StepState *step_d = nullptr;         // device step counter + this step's scalars
     std::vector<bf16opt_group_t> groups;
     float max_norm = 1.0f;
     float gscale = 1.0f;
@@ -52,6 +55,7 @@ struct bf16opt {
     std::vector<uint32_t> slot_chunk0;   // LIST: first chunk of tensor s (n_tensors + 1 entries)
     int sm_count = 0;
     int max_grid = 0;                    // optional cap on CTAs per launch (BF16OPT_MAX_GRID), 0 = none
+    std::vector<std::pair<const void *, int>> occ;  // resident CTAs per SM, per kernel (queried once)
     bool has_sched = false;
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
@@ -134,10 +138,18 @@ bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 #endif
 
 template <class K>
-int grid_for(const bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
+int grid_for(bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
+    const void *key = reinterpret_cast<const void *>(kernel);
+    for (const auto &e : h->occ)
+        if (e.first == key) per_sm = e.second;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        h->occ.emplace_back(key, per_sm);
+    }
     if (per_sm > BF16K_MAX_CTAS_PER_SM) per_sm = BF16K_MAX_CTAS_PER_SM;
     uint64_t g = (uint64_t)h->sm_count * (uint64_t)per_sm;
     if (h->max_grid > 0 && g > (uint64_t)h->max_grid) g = (uint64_t)h->max_grid;
@@ -212,25 +224,25 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
 }
 
 template <bool HAS_ACC, int KMAX>
-int launch_step_k(bf16opt_t *h, const FoldSet &fs, const GroupTable &gtab, cudaStream_t st) {
+int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
     constexpr int U = KMAX <= 1 ? BF16K_STEP_U : (KMAX <= 4 ? BF16K_FOLD4_STEP_U : BF16K_FOLD8_STEP_U);
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
-        k<<<grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt, gtab,
-                                                                          h->norm_d, h->gscale);
+        k<<<grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt,
+                                                                          &h->step_d->gtab, h->norm_d, h->gscale);
     });
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : cuda_fail(h, e, "step kernel launch");
 }
 
-int launch_step(bf16opt_t *h, bool has_acc, const FoldSet &fs, const GroupTable &gtab, cudaStream_t st) {
+int launch_step(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st) {
     switch (kmax_for(fs.count())) {
-    case 0: return launch_step_k<true, 0>(h, fs, gtab, st);
-    case 1: return has_acc ? launch_step_k<true, 1>(h, fs, gtab, st) : launch_step_k<false, 1>(h, fs, gtab, st);
-    case 4: return has_acc ? launch_step_k<true, 4>(h, fs, gtab, st) : launch_step_k<false, 4>(h, fs, gtab, st);
-    default: return has_acc ? launch_step_k<true, 8>(h, fs, gtab, st) : launch_step_k<false, 8>(h, fs, gtab, st);
+    case 0: return launch_step_k<true, 0>(h, fs, st);
+    case 1: return has_acc ? launch_step_k<true, 1>(h, fs, st) : launch_step_k<false, 1>(h, fs, st);
+    case 4: return has_acc ? launch_step_k<true, 4>(h, fs, st) : launch_step_k<false, 4>(h, fs, st);
+    default: return has_acc ? launch_step_k<true, 8>(h, fs, st) : launch_step_k<false, 8>(h, fs, st);
     }
 }
 
@@ -246,10 +258,33 @@ void free_scratch(bf16opt_t *h) {
     if (h->chunks_d) cudaFree(h->chunks_d);
     if (h->partials_d) cudaFree(h->partials_d);
     if (h->norm_d) cudaFree(h->norm_d);
+    if (h->params_d) cudaFree(h->params_d);
+    if (h->step_d) cudaFree(h->step_d);
+    h->params_d = nullptr;
+    h->step_d = nullptr;
     h->segs_d = nullptr;
     h->chunks_d = nullptr;
     h->partials_d = nullptr;
     h->norm_d = nullptr;
+}
+
+// Hyper-parameters and schedule -> device (synchronous; not during a capture).
+cudaError_t upload_params(bf16opt_t *h) {
+    StepParams p;
+    memset(&p, 0, sizeof p);
+    p.n_groups = (int32_t)h->groups.size();
+    for (size_t i = 0; i < h->groups.size(); ++i) {
+        p.lr[i] = h->groups[i].lr;
+        p.beta1[i] = h->groups[i].beta1;
+        p.beta2[i] = h->groups[i].beta2;
+        p.eps[i] = h->groups[i].eps;
+        p.wd[i] = h->groups[i].weight_decay;
+    }
+    p.has_sched = h->has_sched ? 1 : 0;
+    p.warmup = h->sched.warmup_steps;
+    p.decay = h->sched.decay_steps;
+    p.min_ratio = h->sched.min_lr_ratio;
+    return cudaMemcpy(h->params_d, &p, sizeof p, cudaMemcpyHostToDevice);
 }
 
 }  // namespace
@@ -414,7 +449,9 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     if ((e = cudaMalloc(&h->segs_d, nseg * sizeof(Seg))) != cudaSuccess ||
         (e = cudaMalloc(&h->chunks_d, nch * sizeof(Chunk))) != cudaSuccess ||
         (e = cudaMalloc(&h->partials_d, nch * sizeof(double))) != cudaSuccess ||
-        (e = cudaMalloc(&h->norm_d, sizeof(NormState))) != cudaSuccess) {
+        (e = cudaMalloc(&h->norm_d, sizeof(NormState))) != cudaSuccess ||
+        (e = cudaMalloc(&h->params_d, sizeof(StepParams))) != cudaSuccess ||
+        (e = cudaMalloc(&h->step_d, sizeof(StepState))) != cudaSuccess) {
         free_scratch(h);
         delete h;
         cudaGetLastError();
@@ -423,7 +460,9 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     }
     if ((!segs.empty() && (e = cudaMemcpy(h->segs_d, segs.data(), segs.size() * sizeof(Seg), cudaMemcpyHostToDevice)) != cudaSuccess) ||
         (!chunks.empty() && (e = cudaMemcpy(h->chunks_d, chunks.data(), chunks.size() * sizeof(Chunk), cudaMemcpyHostToDevice)) != cudaSuccess) ||
-        (e = cudaMemset(h->norm_d, 0, sizeof(NormState))) != cudaSuccess) {
+        (e = cudaMemset(h->norm_d, 0, sizeof(NormState))) != cudaSuccess ||
+        (e = cudaMemset(h->step_d, 0, sizeof(StepState))) != cudaSuccess ||
+        (e = upload_params(h)) != cudaSuccess) {
         free_scratch(h);
         delete h;
         return fail(nullptr, BF16OPT_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
@@ -444,13 +483,22 @@ int bf16opt_destroy(bf16opt_t *h) {
 
 int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
     if (!h || !t) return BF16OPT_ERR_INVALID_ARG;
-    *t = h->t;
+    DeviceGuard dg(h->device);
+    int64_t v = 0;
+    if (cudaMemcpy(&v, &h->step_d->t, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return BF16OPT_ERR_CUDA;
+    }
+    *t = v;
     return BF16OPT_OK;
 }
 
 int bf16opt_set_step(bf16opt_t *h, int64_t t) {
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (t < 0) return fail(h, BF16OPT_ERR_INVALID_ARG, "step must be >= 0");
+    DeviceGuard dg(h->device);
+    cudaError_t e = cudaMemcpy(&h->step_d->t, &t, sizeof t, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(h, e, "writing the step counter");
     h->t = t;
     return BF16OPT_OK;
 }
@@ -611,6 +659,9 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (!s) {
         h->has_sched = false;
+        DeviceGuard dg(h->device);
+        cudaError_t e = upload_params(h);
+        if (e != cudaSuccess) return cuda_fail(h, e, "uploading the schedule");
         return BF16OPT_OK;
     }
     double f = 0.0;
@@ -618,42 +669,35 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
         return fail(h, BF16OPT_ERR_INVALID_ARG, "lr schedule: need 0 <= warmup_steps <= decay_steps, min_lr_ratio in [0, 1]");
     h->sched = *s;
     h->has_sched = true;
+    DeviceGuard dg(h->device);
+    cudaError_t e = upload_params(h);
+    if (e != cudaSuccess) return cuda_fail(h, e, "uploading the schedule");
     return BF16OPT_OK;
 }
 
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "step needs grad_norm first");
-    const int64_t t = h->t + 1;
-    double sched_f = 1.0;
-    if (h->has_sched) bf16opt_lr_factor(&h->sched, t, &sched_f);
-    GroupTable gtab;
-    memset(&gtab, 0, sizeof gtab);
-    for (size_t i = 0; i < h->groups.size(); ++i) {
-        const bf16opt_group_t &g = h->groups[i];
-        const double lr0 = lr_override ? (double)lr_override[i] : (double)g.lr;
-        if (!std::isfinite(lr0) || lr0 < 0.0) return fail(h, BF16OPT_ERR_INVALID_ARG, "lr_override must be finite and >= 0");
-        const double lr = lr0 * sched_f;
-        const double b1 = g.beta1, b2 = g.beta2;
-        const double bc1 = 1.0 - std::pow(b1, (double)t);
-        const double bc2 = 1.0 - std::pow(b2, (double)t);
-        GroupK &k = gtab.g[i];
-        k.b1 = (float)b1;
-        k.omb1 = (float)(1.0 - b1);
-        k.b2 = (float)b2;
-        k.omb2 = (float)(1.0 - b2);
-        k.eps = g.eps;
-        k.decay = (float)(lr * (double)g.weight_decay);
-        k.step_size = (float)(lr / bc1);
-        k.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    LrOverride ov;
+    memset(&ov, 0, sizeof ov);
+    if (lr_override) {
+        ov.use = 1;
+        for (size_t i = 0; i < h->groups.size(); ++i) {
+            if (!std::isfinite(lr_override[i]) || lr_override[i] < 0.f)
+                return fail(h, BF16OPT_ERR_INVALID_ARG, "lr_override must be finite and >= 0");
+            ov.lr[i] = lr_override[i];
+        }
     }
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
-    int rc;
-    rc = launch_step(h, h->acc_valid, pending_set(h), gtab, st);
+    // t <- t + 1 and this step's scalars, on the device (a captured step replays correctly)
+    k_step_scalars<<<1, 32, 0, st>>>(h->params_d, h->step_d, ov);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "step scalars launch");
+    int rc = launch_step(h, h->acc_valid, pending_set(h), st);
     if (rc) return rc;
-    h->t = t;
+    h->t += 1;
     h->state = S_IDLE;
     h->acc_valid = false;
     h->pend_flat.clear();

@@ -90,6 +90,30 @@ struct GroupTable {
     GroupK g[kMaxGroups];
 };
 
+// Hyper-parameters of the handle, kept on the device so that a captured
+// step (CUDA graph) computes the scalars of whatever step it replays.
+struct StepParams {
+    float lr[kMaxGroups], beta1[kMaxGroups], beta2[kMaxGroups], eps[kMaxGroups], wd[kMaxGroups];
+    int32_t n_groups;
+    int32_t has_sched;             // warmup + cosine factor on every lr
+    int64_t warmup, decay;
+    float min_ratio;
+    int32_t pad;
+};
+
+// Device step counter and the scalars of the current step.
+struct StepState {
+    int64_t t;                     // completed steps
+    int64_t pad;
+    GroupTable gtab;
+};
+
+// Per-call learning rates (optional), by value.
+struct LrOverride {
+    float lr[kMaxGroups];
+    int32_t use;
+};
+
 // Gradient sources passed by value as kernel parameters.  A pass folds k
 // micro-batch gradients (k <= kMaxFold) into the value in micro-batch order.
 constexpr int kMaxFold = 8;
@@ -328,6 +352,44 @@ __global__ void k_norm_from_sumsq(double S, float max_norm, NormState *__restric
     }
 }
 
+// t <- t + 1 and the per-group FP32 scalars of step t, computed in FP64 from
+// the FP32 hyper-parameters: bias corrections 1 - b^t (Kingma & Ba, Algorithm
+// 1), step_size = lr / bc1, 1 / sqrt(bc2), decay = lr * wd; lr times the
+// warmup + cosine factor when a schedule is attached.  One CTA of 32 threads.
+__global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *__restrict__ S, LrOverride ov) {
+    const int64_t t = S->t + 1;
+    const int g = threadIdx.x;
+    if (g < P->n_groups && g < kMaxGroups) {
+        double f = 1.0;
+        if (P->has_sched) {
+            const double r = (double)P->min_ratio;
+            if (t <= P->warmup) {
+                f = (double)t / (double)P->warmup;
+            } else if (t <= P->decay) {
+                const double x = (double)(t - P->warmup) / (double)(P->decay - P->warmup);
+                f = r + (1.0 - r) * 0.5 * (1.0 + cos(3.141592653589793 * x));
+            } else {
+                f = r;
+            }
+        }
+        const double lr = (double)(ov.use ? ov.lr[g] : P->lr[g]) * f;
+        const double b1 = (double)P->beta1[g], b2 = (double)P->beta2[g];
+        const double bc1 = 1.0 - pow(b1, (double)t);
+        const double bc2 = 1.0 - pow(b2, (double)t);
+        GroupK &o = S->gtab.g[g];
+        o.b1 = (float)b1;
+        o.omb1 = (float)(1.0 - b1);
+        o.b2 = (float)b2;
+        o.omb2 = (float)(1.0 - b2);
+        o.eps = P->eps[g];
+        o.decay = (float)(lr * (double)P->wd[g]);
+        o.step_size = (float)(lr / bc1);
+        o.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+    }
+    __syncwarp();
+    if (g == 0) S->t = t;
+}
+
 // ---------------------------------------------------------------------- step
 
 struct AdamOut {
@@ -359,14 +421,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool HAS_ACC, int KMAX, class GT, int U>
 __global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
-       GroupTable gtab, const NormState *__restrict__ ns, float gscale) {
+       const GroupTable *__restrict__ gtab, const NormState *__restrict__ ns, float gscale) {
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
-        const GroupK G = gtab.g[s.group];
+        const GroupK G = gtab->g[s.group];
         const float *a = s.acc + ch.start;
         const uint16_t *g[KA];
 #pragma unroll

@@ -500,3 +500,43 @@ def test_results_do_not_depend_on_the_grid(monkeypatch):
         assert nr == outs[0][1]
         for k in ("p", "m", "v", "p_bf16"):
             assert np.array_equal(st[k].view(np.uint8), outs[0][0][k].view(np.uint8))
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_cuda_graph_replay_matches_eager(mode):
+    """One step captured into a CUDA graph and replayed for the later steps
+    (fresh gradients written into the same buffers before each replay) gives
+    the same bits as calling the API eagerly: the step counter and the
+    per-step scalars live on the device."""
+    wl = workloads.custom(260, [40_000, 3, 16_385, 999], decay=[True, False, True, False], gas=3, steps=4,
+                          grad_sigma=0.1, misalign=2, mode=mode)
+    eager = GpuShard(wl, defer=[False, True, True])
+    eager.opt.set_lr_schedule(2, 4, 0.5)
+    eager.run(wl.steps)
+    want = eager.states()
+    eager.close()
+
+    sh = GpuShard(wl, defer=[False, True, True])
+    sh.opt.set_lr_schedule(2, 4, 0.5)
+    sh.run_step(0)                                # eager warm-up: loads every kernel
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for k in range(wl.gas):
+            sh.opt.accumulate(sh.grads_arg(sh.gbufs[k % len(sh.gbufs)]), first=k == 0, last=k == wl.gas - 1,
+                              defer=sh.pattern[k])
+        sh.opt.grad_norm()
+        sh.opt.step()
+    for s in range(1, wl.steps):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, sh.gbufs[k % len(sh.gbufs)])
+        graph.replay()
+    torch.cuda.synchronize()
+    got = sh.states()
+    assert sh.opt.t == wl.steps
+    sh.close()
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
