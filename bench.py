@@ -368,11 +368,14 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     """Same step through the C ABI with every gradient copied from pinned host
     memory inside the timed region -- whole-buffer copies on one copy stream
     (copies of pinned slices, or one copy split over several streams, measured
-    slower), the copy of micro-batch k+1 overlapping accumulate k -- and the
-    global norm read back to the host every step."""
+    slower) from huge-page-backed registered buffers, the copy of micro-batch
+    k+1 overlapping accumulate k -- and the global norm read back to the host
+    every step."""
     import torch
 
-    host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(G)]
+    from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
+    bufs = [PinnedHostBuffer(n, torch.int16) for _ in range(G)]
+    host = [hb.tensor for hb in bufs]
     for k in range(G):
         host[k].copy_(grads[k])
     torch.cuda.synchronize(dev)
@@ -411,11 +414,15 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
         one()
     torch.cuda.synchronize(dev)
     dt = max_over_ranks(time.perf_counter() - t, dev)
+    huge = all(hb.huge_pages for hb in bufs)
     del host
+    for hb in bufs:
+        hb.close()
     return {"value": round(n * args.e2e_steps * world / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
             "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps,
-            "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1)}
+            "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1),
+            "host_buffers": "huge-page, cudaHostRegister" if huge else "torch pinned"}
 
 
 # ------------------------------------------------------------ CPU oracle arm

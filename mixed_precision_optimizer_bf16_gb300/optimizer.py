@@ -7,6 +7,10 @@ arithmetic is in libbf16opt.so.  State layout for one rank's shard:
         as five contiguous buffers of n elements, plus group ranges;
   LIST: the same five buffers per tensor (separate allocations).
 """
+import ctypes
+import mmap
+
+import numpy as np
 import torch
 
 from . import bf16opt as C
@@ -31,6 +35,82 @@ def alloc_flat(n, device="cuda", misalign=0):
         return base[misalign:misalign + n]
     return dict(master=one(torch.float32), exp_avg=one(torch.float32), exp_avg_sq=one(torch.float32),
                 grad_accum=one(torch.float32), param_bf16=one(torch.int16))
+
+
+def _thp_size():
+    """Size of a transparent huge page (512 MiB on 64 KiB-page Arm kernels, 2 MiB on 4 KiB ones)."""
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+            return int(f.read().strip())
+    except (OSError, ValueError):
+        return 2 << 20
+
+
+def _huge_fraction(start, nbytes):
+    """Fraction of [start, start + nbytes) backed by transparent huge pages (from /proc/self/smaps)."""
+    try:
+        huge, lo, hi = 0, None, None
+        with open("/proc/self/smaps") as f:
+            for line in f:
+                head = line.split()[0]
+                if "-" in head and ":" not in head:
+                    lo, hi = (int(x, 16) for x in head.split("-"))
+                elif head == "AnonHugePages:" and lo is not None and lo <= start < hi:
+                    huge = int(line.split()[1]) * 1024
+        return huge / nbytes if nbytes else 1.0
+    except (OSError, ValueError):
+        return 0.0
+
+
+class PinnedHostBuffer:
+    """Page-locked host memory for gradients that stream to the GPU.
+
+    The region is aligned to the transparent-huge-page size, advised as huge
+    (MADV_HUGEPAGE), faulted in and registered with cudaHostRegister.  Large
+    pages keep the address translations of the host-to-device copies few: on a
+    host whose memory is fragmented by earlier large jobs, small-page pinned
+    buffers slowed copies that overlap HBM-bound kernels by almost 2x, huge-page
+    ones far less.  `tensor` is a CPU tensor over the region (is_pinned()).
+    Falls back to the driver's pinned allocator (torch pin_memory) when the
+    kernel cannot back at least 90 % of the region with huge pages (small-page
+    registered memory was measured slower still) or registration is refused.
+    """
+
+    MADV_HUGEPAGE = 14
+
+    def __init__(self, numel, dtype=torch.int16):
+        itemsize = torch.empty(0, dtype=dtype).element_size()
+        nbytes = int(numel) * itemsize
+        self._registered = None
+        try:
+            align = _thp_size()
+            self._map = mmap.mmap(-1, nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+            addr = ctypes.addressof(ctypes.c_char.from_buffer(self._map))
+            start = (addr + align - 1) & ~(align - 1)
+            libc = ctypes.CDLL(None, use_errno=True)
+            libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+            libc.madvise(ctypes.c_void_p(start), nbytes, self.MADV_HUGEPAGE)   # advisory
+            arr = np.frombuffer(self._map, dtype=np.uint8, count=nbytes, offset=start - addr)
+            arr[:] = 0                                                          # fault the pages in now
+            if _huge_fraction(start, nbytes) < 0.9:
+                raise RuntimeError("not backed by huge pages")
+            if int(torch.cuda.cudart().cudaHostRegister(start, nbytes, 0)) != 0:
+                raise RuntimeError("cudaHostRegister refused")
+            self._registered = start
+            self.tensor = torch.from_numpy(arr).view(dtype)
+            self.huge_pages = True
+        except Exception:
+            self._map = None
+            self.tensor = torch.empty(int(numel), dtype=dtype, pin_memory=True)
+            self.huge_pages = False
+
+    def close(self):
+        """Unregister the region (the tensor must not be used afterwards)."""
+        if self._registered is not None:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaHostUnregister(self._registered)
+            self._registered = None
+        self.tensor = None
 
 
 def global_sumsq(local, group=None):

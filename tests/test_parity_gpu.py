@@ -540,3 +540,17 @@ def test_cuda_graph_replay_matches_eager(mode):
     sh.close()
     for k in ("p", "m", "v", "p_bf16"):
         assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+
+
+@needs_cuda
+def test_pinned_host_buffer_round_trip():
+    from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
+    hb = PinnedHostBuffer(5_000_003, torch.int16)
+    assert hb.tensor.is_pinned() and hb.tensor.numel() == 5_000_003
+    d = torch.randint(-30000, 30000, (5_000_003,), dtype=torch.int16, device="cuda")
+    hb.tensor.copy_(d)
+    e = torch.empty_like(d)
+    e.copy_(hb.tensor, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(d, e)
+    hb.close()
