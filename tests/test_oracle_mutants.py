@@ -37,9 +37,15 @@ MUTANTS = {
     "grad_scale_ignored_in_norm": ("double x = (double)orc_effective(k->acc[i], k->gs);",
                                    "double x = (double)k->acc[i];"),
     "clip_not_applied": ("double gc = (double)e * c;", "double gc = (double)e;"),
+    "lr_warmup_off_by_one": ("return lr * (double)t / (double)warmup;", "return lr * (double)(t - 1) / (double)warmup;"),
+    "lr_cosine_sign": ("(1.0 + cos(3.14159265358979323846 * s))", "(1.0 - cos(3.14159265358979323846 * s))"),
+    "lr_no_min_floor": ("return min_lr + (lr - min_lr) * (1.0 + cos", "return lr * (1.0 + cos"),
 }
 
-BATTERY = [name for name in dir(pins) if name.startswith("test_") and "exhaustive" not in name]
+import test_lr_schedule as lr_pins  # noqa: E402
+
+BATTERY = [getattr(pins, name) for name in dir(pins) if name.startswith("test_") and "exhaustive" not in name]
+BATTERY.append(lr_pins.test_oracle_schedule_closed_forms)
 
 
 def _build(tmp_path, name, src):
@@ -62,11 +68,11 @@ def _run_battery(so_path):
     failed = []
     try:
         oracle.lib()
-        for name in BATTERY:
+        for fn in BATTERY:
             try:
-                getattr(pins, name)()
+                fn()
             except Exception:  # a pin failing is what we look for
-                failed.append(name)
+                failed.append(fn.__name__)
     finally:
         oracle._lib = saved
         oracle._build.build = real_build

@@ -43,10 +43,12 @@ def dense_parity(wl, defer=False, grad_scale=1.0):
     return compare(got, ref, scales, wl, grad_scale, check_acc=not last_deferred)
 
 
-def sampled_parity(wl, defer=False, k=1 << 15):
+def sampled_parity(wl, defer=False, k=1 << 15, extra=()):
     sh = GpuShard(wl, defer=defer)
     sh.run(wl.steps)
     idx = sample_indices(wl, k)
+    if len(extra):
+        idx = np.unique(np.concatenate([idx, np.asarray(extra, dtype=np.int64)]))
     got = sh.states(idx)
     norms = list(sh.norms)
     sh.close()
@@ -161,6 +163,18 @@ def test_tp4_slice_full_size_sampled():
     """72 separate tensors, 3,700,064,256 elements, GAS 8, 2 steps."""
     st = sampled_parity(workloads.workload(4), defer=True)
     print("TP4 slice", st)
+
+
+@needs_cuda
+def test_flat_range_beyond_2_32_elements():
+    """One flat range of 2^32 + 4099 elements (~86 GB on the device): 64-bit
+    element offsets in the chunk table and the kernels, sampled on both sides
+    of 2^31 and 2^32 and at the ragged end."""
+    n = (1 << 32) + 4099
+    wl = workloads.custom(270, [n], gas=2, steps=1, grad_sigma=1e-4)
+    edges = [(1 << 31) + d for d in range(-3, 4)] + [(1 << 32) + d for d in range(-5, 6)] + [n - 1, n - 2, n - 4099]
+    st = sampled_parity(wl, defer=True, k=1 << 14, extra=edges)
+    print("beyond 2^32", st)
 
 
 # ------------------------------------------------------------ behaviour
