@@ -1,10 +1,10 @@
 // bf16opt.cu -- host side of the C ABI declared in include/bf16opt.h.
 //
 // Validates descriptors, builds the segment and chunk tables once on the
-// device, keeps the accumulate -> grad_norm -> step sequence, computes the
-// per-step AdamW scalars in FP64 on the host and launches the kernels of
-// kernels.cuh on the caller's stream.  No CPU fallback: every element of the
-// path is computed by those kernels.
+// device, keeps the accumulate -> grad_norm -> step sequence on the host and
+// launches the kernels of kernels.cuh on the caller's stream (the per-step
+// AdamW scalars are computed on the device, from a device step counter).  No
+// CPU fallback: every element of the path is computed by those kernels.
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -44,7 +44,6 @@ struct bf16opt {
     std::vector<bf16opt_group_t> groups;
     float max_norm = 1.0f;
     float gscale = 1.0f;
-    int64_t t = 0;
     State state = S_IDLE;
     bool acc_valid = false;              // acc holds the fold of the micro-batches folded so far
     bool partials_ready = false;
@@ -499,7 +498,6 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t) {
     DeviceGuard dg(h->device);
     cudaError_t e = cudaMemcpy(&h->step_d->t, &t, sizeof t, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(h, e, "writing the step counter");
-    h->t = t;
     return BF16OPT_OK;
 }
 
@@ -697,7 +695,6 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     if (e != cudaSuccess) return cuda_fail(h, e, "step scalars launch");
     int rc = launch_step(h, h->acc_valid, pending_set(h), st);
     if (rc) return rc;
-    h->t += 1;
     h->state = S_IDLE;
     h->acc_valid = false;
     h->pend_flat.clear();
