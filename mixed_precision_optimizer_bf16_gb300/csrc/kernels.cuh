@@ -1,16 +1,19 @@
 // kernels.cuh -- sm_103a kernels of the BF16 mixed-precision optimizer step.
 //
 // Three bandwidth-bound kernels (no tensor cores: nothing here is a
-// contraction) over a table of chunks:
-//   k_accum        bf16 micro-batch gradient -> FP32 accumulator, optionally with
-//                  the per-chunk partial sums of squares of the global norm fused in
-//                  ("BLOOM 176B 训练技术概览", section "BF16 优化器": FP32 accumulation of
-//                  gradients across pipeline micro-batches);
-//   k_norm_final   fixed-order FP64 sum of the chunk partials, norm and clip
-//                  coefficient ("企业官网建设流程全解析" (cf-1.com), section 4.3: global
-//                  norm clipped at 1.0);
-//   k_step         clip x AdamW x FP32 master/moment update x bf16 cast in one pass
-//                  ("企业官网建设流程全解析", sections 1 and 3.3).
+// contraction) over a table of chunks, and three single-CTA kernels:
+//   k_accum          folds bf16 micro-batch gradients into the FP32 accumulator,
+//                    optionally with the per-chunk partial sums of squares of the
+//                    global norm fused in ("BLOOM 176B 训练技术概览", section
+//                    "BF16 优化器": FP32 accumulation of gradients across pipeline
+//                    micro-batches);
+//   k_norm_final     fixed-order FP64 sum of the chunk partials, norm and clip
+//                    coefficient ("企业官网建设流程全解析" (cf-1.com), section 4.3: global
+//                    norm clipped at 1.0);
+//   k_norm_from_sumsq the same from an all-rank sum handed in by the host (ZeRO);
+//   k_step_scalars   t <- t + 1 and the per-group AdamW scalars of step t;
+//   k_step           clip x AdamW x FP32 master/moment update x bf16 cast in one pass
+//                    ("企业官网建设流程全解析", sections 1 and 3.3).
 //
 // Work decomposition.  A segment is one run of elements with one parameter
 // group and one set of base pointers (a flat range or a list tensor).  Each

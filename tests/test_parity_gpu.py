@@ -131,6 +131,7 @@ def test_list_more_tensors_than_one_launch():
                           grad_sigma=0.05, misalign=3, mode="list")
     dense_parity(wl)
     dense_parity(wl, defer=True)
+    dense_parity(wl, defer=[True, True])      # two pointers per tensor: 512 tensors per launch
 
 
 @needs_cuda
@@ -143,11 +144,13 @@ def test_grad_scale():
 # ----------------------------------------------------------- full-size sampled
 
 @needs_cuda
-@pytest.mark.parametrize("defer", [True, False])
+@pytest.mark.parametrize("defer", [True, False, "all"])
 def test_scaled_bloom_full_size_sampled(defer):
     """1,722,408,960 elements, 293 tensors in one flat buffer, decay/no-decay
-    ranges, GAS 4, 2 steps; the benchmark's launch configuration is defer=True."""
-    st = sampled_parity(workloads.workload(2), defer=defer)
+    ranges, GAS 4, 2 steps; the benchmark's launch configuration is defer=True,
+    its all-deferred variant defer="all"."""
+    wl = workloads.workload(2)
+    st = sampled_parity(wl, defer=[True] * wl.gas if defer == "all" else defer)
     print("scaled BLOOM", defer, st)
 
 
