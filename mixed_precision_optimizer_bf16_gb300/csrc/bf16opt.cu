@@ -15,6 +15,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/bf16opt.h"
 #include "kernels.cuh"
 
@@ -71,6 +73,13 @@ int fail(bf16opt_t *h, int code, const std::string &msg) {
 int cuda_fail(bf16opt_t *h, cudaError_t e, const char *what) {
     return fail(h, BF16OPT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
+
+// Named host range around each API call, seen by profilers that attach through
+// NVTX (no-op otherwise).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct DeviceGuard {
     int prev = -1;
@@ -309,6 +318,7 @@ const char *bf16opt_last_error(const bf16opt_t *h) {
 }
 
 int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
+    NvtxRange nvtx("bf16opt_create");
     if (out) *out = nullptr;
     if (!d || !out) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "desc and out must be non-NULL");
     if (d->mode != BF16OPT_FLAT && d->mode != BF16OPT_LIST)
@@ -472,6 +482,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
 }
 
 int bf16opt_destroy(bf16opt_t *h) {
+    NvtxRange nvtx("bf16opt_destroy");
     if (!h) return BF16OPT_OK;
     DeviceGuard dg(h->device);
     cudaDeviceSynchronize();
@@ -493,6 +504,7 @@ int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
 }
 
 int bf16opt_set_step(bf16opt_t *h, int64_t t) {
+    NvtxRange nvtx("bf16opt_set_step");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (t < 0) return fail(h, BF16OPT_ERR_INVALID_ARG, "step must be >= 0");
     DeviceGuard dg(h->device);
@@ -503,6 +515,7 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t) {
 
 int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list, unsigned flags,
                        void *stream) {
+    NvtxRange nvtx("bf16opt_accumulate");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     const bool first = flags & BF16OPT_FIRST, last = flags & BF16OPT_LAST, defer = flags & BF16OPT_DEFER;
     if (flags & ~(BF16OPT_FIRST | BF16OPT_LAST | BF16OPT_DEFER)) return fail(h, BF16OPT_ERR_INVALID_ARG, "unknown flag");
@@ -571,6 +584,7 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
 }
 
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
+    NvtxRange nvtx("bf16opt_grad_norm");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
         return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm needs a completed accumulation");
@@ -602,6 +616,7 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
 }
 
 int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
+    NvtxRange nvtx("bf16opt_grad_norm_local");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (!local_sumsq) return fail(h, BF16OPT_ERR_INVALID_ARG, "grad_norm_local: local_sumsq is NULL");
     if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
@@ -620,6 +635,7 @@ int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
 }
 
 int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
+    NvtxRange nvtx("bf16opt_set_global_sumsq");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_global_sumsq needs grad_norm_local first");
     DeviceGuard dg(h->device);
@@ -654,6 +670,7 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
 }
 
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
+    NvtxRange nvtx("bf16opt_set_lr_schedule");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (!s) {
         h->has_sched = false;
@@ -674,6 +691,7 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
 }
 
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
+    NvtxRange nvtx("bf16opt_step");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "step needs grad_norm first");
     LrOverride ov;

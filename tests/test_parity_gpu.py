@@ -571,3 +571,51 @@ def test_pinned_host_buffer_round_trip():
     torch.cuda.synchronize()
     assert torch.equal(d, e)
     hb.close()
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_checkpoint_dump_free_restore(mode):
+    """Checkpoint/resume: the state is the caller's buffers plus the step
+    counter.  Two steps, dump master/m/v/bf16 to host memory, free the handle
+    and every buffer, restore into freshly allocated buffers, set the step
+    counter, one more step == three uninterrupted steps, bit for bit."""
+    wl = workloads.custom(280, [30_001, 7, 16_385], decay=[True, False, True], gas=3, steps=3, grad_sigma=0.2,
+                          misalign=1, mode=mode)
+    ref = GpuShard(wl, defer=True)
+    ref.run(3)
+    want = ref.states()
+    ref.close()
+    del ref
+
+    sh = GpuShard(wl, defer=True)
+    sh.run_step(0)
+    sh.run_step(1)
+    torch.cuda.synchronize()
+    saved = {k: v.copy() for k, v in sh.states().items()}
+    t_saved = sh.opt.t
+    sh.close()
+    del sh
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    # fresh buffers with the same offset modulo 16 bytes: the norm's per-chunk
+    # partials follow the thread->element map, which that offset fixes
+    wl2 = workloads.custom(280, [30_001, 7, 16_385], decay=[True, False, True], gas=3, steps=3, grad_sigma=0.2,
+                           misalign=1, mode=mode)
+    sh2 = GpuShard(wl2, defer=True)
+    names = dict(p="master", m="exp_avg", v="exp_avg_sq", p_bf16="param_bf16")
+    for key, name in names.items():
+        host = torch.from_numpy(saved[key].view(np.int16) if key == "p_bf16" else saved[key])
+        if wl2.mode == "flat":
+            sh2.flat[name].copy_(host)
+        else:
+            for d, t, off in zip(sh2.tensors, wl2.tensors, wl2.offsets):
+                d[name].copy_(host[off:off + t.numel])
+    sh2.opt.t = t_saved
+    sh2.run_step(2)
+    got = sh2.states()
+    assert sh2.opt.t == 3
+    sh2.close()
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
