@@ -229,6 +229,17 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
  * that restored its counter with bf16opt_set_step continues the schedule). */
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
 
+/* Opt-in guard for steps whose global norm is Inf or NaN (enable != 0): the
+ * decision is taken on the device by bf16opt_step's first kernel, which then
+ * leaves the step counter unchanged, and the fused kernel returns without
+ * touching master, moments or bf16 parameters -- so it also holds inside a
+ * captured CUDA graph, where the host cannot read the norm before the step.
+ * Off by default: the method has no skip logic (bf16 does not overflow the
+ * way fp16 does; "企业官网建设流程全解析", section 4.1) and grad_norm reports
+ * BF16OPT_WARN_NONFINITE for the caller to act on.  Synchronous (not during a
+ * capture).  Errors: INVALID_ARG (NULL handle), CUDA. */
+int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable);
+
 /* Frees the library's scratch (waits for the device); the caller's buffers
  * are untouched.  NULL is accepted. */
 int bf16opt_destroy(bf16opt_t *h);

@@ -65,7 +65,7 @@ class bf16opt_norm_result_t(ctypes.Structure):
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
-           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq")
+           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_skip_nonfinite")
 
 _lib = None
 
@@ -107,6 +107,8 @@ def load(path=None):
     L.bf16opt_grad_norm_local.argtypes = [hp, c_vp, ctypes.POINTER(ctypes.c_double)]
     L.bf16opt_set_global_sumsq.restype = ctypes.c_int
     L.bf16opt_set_global_sumsq.argtypes = [hp, ctypes.c_double, c_vp]
+    L.bf16opt_set_skip_nonfinite.restype = ctypes.c_int
+    L.bf16opt_set_skip_nonfinite.argtypes = [hp, ctypes.c_int]
     L.bf16opt_lr_factor.restype = ctypes.c_int
     L.bf16opt_lr_factor.argtypes = [ctypes.POINTER(bf16opt_lr_schedule_t), ctypes.c_int64,
                                     ctypes.POINTER(ctypes.c_double)]
@@ -171,6 +173,10 @@ def bf16opt_grad_norm_local(h, stream=0):
 
 def bf16opt_set_global_sumsq(h, global_sumsq, stream=0):
     return load().bf16opt_set_global_sumsq(h, float(global_sumsq), c_vp(int(stream)) if stream else None)
+
+
+def bf16opt_set_skip_nonfinite(h, enable):
+    return load().bf16opt_set_skip_nonfinite(h, 1 if enable else 0)
 
 
 def bf16opt_lr_factor(sched, t):

@@ -58,6 +58,7 @@ struct bf16opt {
     int max_grid = 0;                    // optional cap on CTAs per launch (BF16OPT_MAX_GRID), 0 = none
     std::vector<std::pair<const void *, int>> occ;  // resident CTAs per SM, per kernel (queried once)
     bool has_sched = false;
+    bool skip_nonfinite = false;
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
 };
@@ -238,7 +239,7 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
         k<<<grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt,
-                                                                          &h->step_d->gtab, h->norm_d, h->gscale);
+                                                                          h->step_d, h->norm_d, h->gscale);
     });
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();
@@ -292,6 +293,7 @@ cudaError_t upload_params(bf16opt_t *h) {
     p.warmup = h->sched.warmup_steps;
     p.decay = h->sched.decay_steps;
     p.min_ratio = h->sched.min_lr_ratio;
+    p.skip_nonfinite = h->skip_nonfinite ? 1 : 0;
     return cudaMemcpy(h->params_d, &p, sizeof p, cudaMemcpyHostToDevice);
 }
 
@@ -669,6 +671,16 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
     return BF16OPT_OK;
 }
 
+int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
+    NvtxRange nvtx("bf16opt_set_skip_nonfinite");
+    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    h->skip_nonfinite = enable != 0;
+    DeviceGuard dg(h->device);
+    cudaError_t e = upload_params(h);
+    if (e != cudaSuccess) return cuda_fail(h, e, "uploading the skip setting");
+    return BF16OPT_OK;
+}
+
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
     NvtxRange nvtx("bf16opt_set_lr_schedule");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
@@ -708,7 +720,7 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
     // t <- t + 1 and this step's scalars, on the device (a captured step replays correctly)
-    k_step_scalars<<<1, 32, 0, st>>>(h->params_d, h->step_d, ov);
+    k_step_scalars<<<1, 32, 0, st>>>(h->params_d, h->step_d, ov, h->norm_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "step scalars launch");
     int rc = launch_step(h, h->acc_valid, pending_set(h), st);

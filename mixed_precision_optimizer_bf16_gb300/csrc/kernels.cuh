@@ -101,13 +101,14 @@ struct StepParams {
     int32_t has_sched;             // warmup + cosine factor on every lr
     int64_t warmup, decay;
     float min_ratio;
-    int32_t pad;
+    int32_t skip_nonfinite;        // leave the state alone when the norm is not finite
 };
 
 // Device step counter and the scalars of the current step.
 struct StepState {
     int64_t t;                     // completed steps
-    int64_t pad;
+    int32_t skip;                  // this step is skipped (non-finite norm, skipping enabled)
+    int32_t pad;
     GroupTable gtab;
 };
 
@@ -359,7 +360,9 @@ __global__ void k_norm_from_sumsq(double S, float max_norm, NormState *__restric
 // the FP32 hyper-parameters: bias corrections 1 - b^t (Kingma & Ba, Algorithm
 // 1), step_size = lr / bc1, 1 / sqrt(bc2), decay = lr * wd; lr times the
 // warmup + cosine factor when a schedule is attached.  One CTA of 32 threads.
-__global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *__restrict__ S, LrOverride ov) {
+__global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *__restrict__ S, LrOverride ov,
+                               const NormState *__restrict__ ns) {
+    const int skip = (P->skip_nonfinite && !ns->finite) ? 1 : 0;
     const int64_t t = S->t + 1;
     const int g = threadIdx.x;
     if (g < P->n_groups && g < kMaxGroups) {
@@ -390,7 +393,10 @@ __global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *__re
         o.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
     }
     __syncwarp();
-    if (g == 0) S->t = t;
+    if (g == 0) {
+        S->skip = skip;
+        if (!skip) S->t = t;
+    }
 }
 
 // ---------------------------------------------------------------------- step
@@ -424,9 +430,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool HAS_ACC, int KMAX, class GT, int U>
 __global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
-       const GroupTable *__restrict__ gtab, const NormState *__restrict__ ns, float gscale) {
+       const StepState *__restrict__ st, const NormState *__restrict__ ns, float gscale) {
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
+    if (st->skip) return;                                      // non-finite norm, skipping enabled
+    const GroupTable *__restrict__ gtab = &st->gtab;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const Chunk ch = chunks[c];

@@ -177,6 +177,10 @@ class BF16Optimizer:
         C.check(C.bf16opt_set_global_sumsq(self.h, total, _stream_handle(stream)), self.h)
         return total ** 0.5
 
+    def set_skip_nonfinite(self, enable=True):
+        """Skip (on the device) any step whose global norm is Inf or NaN."""
+        return C.check(C.bf16opt_set_skip_nonfinite(self.h, enable), self.h)
+
     def set_lr_schedule(self, warmup_steps, decay_steps, min_lr_ratio):
         """Attach the warmup + cosine schedule (None detaches); see bf16opt_set_lr_schedule."""
         self._sched = None if warmup_steps is None else C.lr_schedule(warmup_steps, decay_steps, min_lr_ratio)

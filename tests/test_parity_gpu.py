@@ -619,3 +619,60 @@ def test_checkpoint_dump_free_restore(mode):
     sh2.close()
     for k in ("p", "m", "v", "p_bf16"):
         assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+
+
+@needs_cuda
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_skip_nonfinite_step(use_graph):
+    """With skipping enabled a step whose norm is Inf leaves every state buffer
+    and the step counter untouched (decided on the device, so it also works in
+    a replayed graph); the next clean step continues exactly like a run that
+    never saw the bad step."""
+    import harness
+    wl = workloads.custom(290, [20_000, 333], decay=[True, False], gas=2, steps=2, grad_sigma=0.1, misalign=1)
+    ref = GpuShard(wl)
+    ref.run(2)                                   # steps 0 and 1, no bad step
+    want = ref.states()
+    ref.close()
+
+    sh = GpuShard(wl)
+    sh.opt.set_skip_nonfinite(True)
+    sh.run_step(0)
+    torch.cuda.synchronize()
+    before = sh.states()
+    bufs = [harness._alloc(wl.n, torch.int16, wl.misalign) for _ in range(wl.gas)]   # one per micro-batch
+
+    def enqueue():
+        for k in range(wl.gas):
+            sh.opt.accumulate(bufs[k], first=k == 0, last=k == wl.gas - 1)
+        sh.opt.grad_norm()
+        sh.opt.step()
+
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            enqueue()
+
+    def step_with(step_index, poison):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, step_index, k, bufs[k])
+        if poison:
+            bufs[1][123] = 0x7F80                    # bf16 +Inf in micro-batch 1
+        if graph is None:
+            enqueue()
+        else:
+            graph.replay()
+        torch.cuda.synchronize()
+
+    step_with(1, poison=True)
+    skipped = sh.states()
+    assert sh.opt.t == 1
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(skipped[k].view(np.uint8), before[k].view(np.uint8)), k
+    step_with(1, poison=False)
+    assert sh.opt.t == 2
+    got = sh.states()
+    sh.close()
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
