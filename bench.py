@@ -399,7 +399,10 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     (copies of pinned slices, or one copy split over several streams, measured
     slower) from huge-page-backed registered buffers, the copy of micro-batch
     k+1 overlapping accumulate k -- and the global norm read back to the host
-    every step."""
+    every step.  Beside it: the bare link (one micro-batch copied alone, the
+    best of three) and each step's wall time, because the step is bound by that
+    link, whose speed on a virtualised host varied several-fold between
+    processes on one machine."""
     import torch
 
     from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
@@ -432,6 +435,16 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
             free[G - 1].record(comp)
         return norm
 
+    # the bare link: one micro-batch copied alone, nothing else on the GPU
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    link = []
+    for _ in range(3):
+        with torch.cuda.stream(copy):
+            c0.record(copy)
+            grads[0].copy_(host[0], non_blocking=True)
+            c1.record(copy)
+        c1.synchronize()
+        link.append(2 * n / (c0.elapsed_time(c1) * 1e-3) / 1e9)
     for _ in range(2):
         one()
     torch.cuda.synchronize(dev)
@@ -439,11 +452,14 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
         import torch.distributed as dist
         dist.barrier()
     t = time.perf_counter()
+    marks = [t]
     for _ in range(args.e2e_steps):
         one()
+        marks.append(time.perf_counter())
     torch.cuda.synchronize(dev)
     dt = max_over_ranks(time.perf_counter() - t, dev)
     huge = all(hb.huge_pages for hb in bufs)
+    huge_frac = min(hb.huge_fraction for hb in bufs)
     del host
     for hb in bufs:
         hb.close()
@@ -451,7 +467,10 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
             "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps,
             "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1),
-            "host_buffers": "huge-page, cudaHostRegister" if huge else "torch pinned"}
+            "host_buffers": "huge-page, cudaHostRegister" if huge else "torch pinned",
+            "host_huge_fraction": round(huge_frac, 3),
+            "h2d_link_gbs_alone": round(max(link), 1),
+            "step_wall_ms": [round((b - a) * 1e3, 1) for a, b in zip(marks, marks[1:])]}
 
 
 # ------------------------------------------------------------ CPU oracle arm

@@ -82,6 +82,7 @@ class PinnedHostBuffer:
         itemsize = torch.empty(0, dtype=dtype).element_size()
         nbytes = int(numel) * itemsize
         self._registered = None
+        self.huge_fraction = 0.0
         try:
             align = _thp_size()
             self._map = mmap.mmap(-1, nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
@@ -92,7 +93,8 @@ class PinnedHostBuffer:
             libc.madvise(ctypes.c_void_p(start), nbytes, self.MADV_HUGEPAGE)   # advisory
             arr = np.frombuffer(self._map, dtype=np.uint8, count=nbytes, offset=start - addr)
             arr[:] = 0                                                          # fault the pages in now
-            if _huge_fraction(start, nbytes) < 0.9:
+            self.huge_fraction = _huge_fraction(start, nbytes)
+            if self.huge_fraction < 0.9:
                 raise RuntimeError("not backed by huge pages")
             if int(torch.cuda.cudart().cudaHostRegister(start, nbytes, 0)) != 0:
                 raise RuntimeError("cudaHostRegister refused")
