@@ -198,6 +198,36 @@ def test_hand_worked_single_element():
     assert pb[0] == 0x3F80
 
 
+def test_hand_worked_two_steps():
+    """The single-element case continued: g = -0.25 at t = 2 from the stored
+    FP32 state of step 1.  Expected values from exact rationals (the square
+    root in 50-digit decimal), each rounded once to FP32:
+    m2 = 0.9 m1 - 0.025 -> 0x3CA3D70B, v2 = 0.95 v1 + 0.003125 -> 0x3C75C290,
+    p2 = p1 (1 - lr wd) - lr m2/(1 - 0.9^2) / (sqrt(v2/(1 - 0.95^2)) + eps)
+    -> 0x3F7FFAEF; bias correction at t = 2 is what moves it."""
+    from decimal import Decimal
+    p = np.array([1.0], np.float32)
+    m = np.zeros(1, np.float32)
+    v = np.zeros(1, np.float32)
+    pb = np.zeros(1, np.uint16)
+    oracle.adamw(p, m, v, pb, np.array([0.5], np.float32), 1.0, grp(), 1, threads=1)
+    p1, m1, v1 = F(p[0]), F(m[0]), F(v[0])
+    g = F(-0.25)
+    oracle.adamw(p, m, v, pb, np.array([-0.25], np.float32), 1.0, grp(), 2, threads=1)
+
+    m2 = F(B1) * m1 + (1 - F(B1)) * g
+    v2 = F(B2) * v1 + (1 - F(B2)) * g * g
+    vhat = v2 / (1 - F(B2) ** 2)
+    root = Fraction((Decimal(vhat.numerator) / Decimal(vhat.denominator)).sqrt())
+    p2 = p1 - F(LR) * F(WD) * p1 - F(LR) * (m2 / (1 - F(B1) ** 2)) / (root + F(EPS))
+    for got, want in ((m[0], m2), (v[0], v2), (p[0], p2)):
+        bits, mid = rn32_bits(want)
+        assert mid > 1e-12
+        assert f32_bits(got) == bits
+    assert (f32_bits(m[0]), f32_bits(v[0]), f32_bits(p[0])) == (0x3CA3D70B, 0x3C75C290, 0x3F7FFAEF)
+    assert pb[0] == rne_bf16_bits_from_f32(p[0]) == 0x3F80
+
+
 def test_hand_worked_rounding_point_no_decay():
     """Accumulated grad exactly 1.0 (see the tie test), norm = 1 = max_norm so
     c = 1, wd = 0: p1 = 1 - 6e-5 / (1 + 1e-8) = 0.99994000000060, nearest FP32
