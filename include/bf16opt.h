@@ -226,7 +226,9 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
 /* Attaches a copy of schedule `s` to the handle (NULL detaches it).  Every later
  * bf16opt_step then uses lr = (lr_override[g] or the group's lr) * f(t) with t
  * the step number of that step (the step counter plus one, so a resumed run
- * that restored its counter with bf16opt_set_step continues the schedule). */
+ * that restored its counter with bf16opt_set_step continues the schedule).
+ * Waits for all work on the handle's device first, so steps already enqueued
+ * keep the old schedule; not during a stream capture. */
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
 
 /* Opt-in guard for steps whose global norm is Inf or NaN (enable != 0): the
@@ -236,17 +238,21 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
  * captured CUDA graph, where the host cannot read the norm before the step.
  * Off by default: the method has no skip logic (bf16 does not overflow the
  * way fp16 does; "企业官网建设流程全解析", section 4.1) and grad_norm reports
- * BF16OPT_WARN_NONFINITE for the caller to act on.  Synchronous (not during a
- * capture).  Errors: INVALID_ARG (NULL handle), CUDA. */
+ * BF16OPT_WARN_NONFINITE for the caller to act on.  Waits for all work on the
+ * handle's device first, so steps already enqueued keep the old setting; not
+ * during a stream capture.  Errors: INVALID_ARG (NULL handle), CUDA. */
 int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable);
 
 /* Frees the library's scratch (waits for the device); the caller's buffers
  * are untouched.  NULL is accepted. */
 int bf16opt_destroy(bf16opt_t *h);
 
-/* Step counter t (number of completed steps, kept on the device; both calls
- * synchronise), for checkpoint and resume: restore the caller's buffers and
- * set_step(t) to continue. */
+/* Step counter t (number of completed steps, kept on the device), for
+ * checkpoint and resume: restore the caller's buffers and set_step(t) to
+ * continue.  Both calls first wait for all work on the handle's device
+ * (cudaDeviceSynchronize), so they are ordered after every step already
+ * enqueued, on any stream (non-blocking ones included); not during a stream
+ * capture.  Errors: INVALID_ARG (NULL, t < 0), CUDA. */
 int bf16opt_get_step(const bf16opt_t *h, int64_t *t);
 int bf16opt_set_step(bf16opt_t *h, int64_t t);
 
@@ -266,7 +272,7 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t);
  * else 1.  `out` is device-accessible memory owned by the caller; the result
  * is written there on `stream` (nothing is synchronised).
  *
- * Scratch: one FP64 partial per 16,384-element chunk, kept in a file-scope
+ * Scratch: one FP64 partial per 32,768-element chunk, kept in a file-scope
  * device array of 65,536 entries (512 KiB) that every GPU loading this
  * library holds until the process exits; hence n is limited to
  * BF16OPT_STATIC_NORM_MAX_ELEMS (2^30) elements and larger n is rejected with

@@ -277,6 +277,12 @@ void free_scratch(bf16opt_t *h) {
     h->norm_d = nullptr;
 }
 
+// The calls that read or write the device step state or hyper-parameters with
+// a plain copy first wait for all work on the handle's device: a step still in
+// flight on a non-blocking stream (which the legacy stream of cudaMemcpy does
+// not wait for) is then ordered before them.  Not allowed during a capture.
+cudaError_t quiesce() { return cudaDeviceSynchronize(); }
+
 // Hyper-parameters and schedule -> device (synchronous; not during a capture).
 cudaError_t upload_params(bf16opt_t *h) {
     StepParams p;
@@ -497,7 +503,7 @@ int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
     if (!h || !t) return BF16OPT_ERR_INVALID_ARG;
     DeviceGuard dg(h->device);
     int64_t v = 0;
-    if (cudaMemcpy(&v, &h->step_d->t, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    if (quiesce() != cudaSuccess || cudaMemcpy(&v, &h->step_d->t, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
         cudaGetLastError();
         return BF16OPT_ERR_CUDA;
     }
@@ -510,7 +516,9 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t) {
     if (!h) return BF16OPT_ERR_INVALID_ARG;
     if (t < 0) return fail(h, BF16OPT_ERR_INVALID_ARG, "step must be >= 0");
     DeviceGuard dg(h->device);
-    cudaError_t e = cudaMemcpy(&h->step_d->t, &t, sizeof t, cudaMemcpyHostToDevice);
+    cudaError_t e = quiesce();
+    if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
+    e = cudaMemcpy(&h->step_d->t, &t, sizeof t, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(h, e, "writing the step counter");
     return BF16OPT_OK;
 }
@@ -674,9 +682,11 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
 int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
     NvtxRange nvtx("bf16opt_set_skip_nonfinite");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
-    h->skip_nonfinite = enable != 0;
     DeviceGuard dg(h->device);
-    cudaError_t e = upload_params(h);
+    cudaError_t e = quiesce();
+    if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
+    h->skip_nonfinite = enable != 0;
+    e = upload_params(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "uploading the skip setting");
     return BF16OPT_OK;
 }
@@ -684,20 +694,15 @@ int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
     NvtxRange nvtx("bf16opt_set_lr_schedule");
     if (!h) return BF16OPT_ERR_INVALID_ARG;
-    if (!s) {
-        h->has_sched = false;
-        DeviceGuard dg(h->device);
-        cudaError_t e = upload_params(h);
-        if (e != cudaSuccess) return cuda_fail(h, e, "uploading the schedule");
-        return BF16OPT_OK;
-    }
     double f = 0.0;
-    if (bf16opt_lr_factor(s, 1, &f) != BF16OPT_OK)
+    if (s && bf16opt_lr_factor(s, 1, &f) != BF16OPT_OK)
         return fail(h, BF16OPT_ERR_INVALID_ARG, "lr schedule: need 0 <= warmup_steps <= decay_steps, min_lr_ratio in [0, 1]");
-    h->sched = *s;
-    h->has_sched = true;
     DeviceGuard dg(h->device);
-    cudaError_t e = upload_params(h);
+    cudaError_t e = quiesce();
+    if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
+    h->has_sched = s != nullptr;
+    if (s) h->sched = *s;
+    e = upload_params(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "uploading the schedule");
     return BF16OPT_OK;
 }
@@ -744,7 +749,7 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
 // already held by a caching allocator (a raw cudaMalloc can then fail), and
 // latency-sensitive loops that cannot take the device synchronisation that
 // cudaMalloc/cudaFree imply.  For them this entry point keeps its scratch --
-// one FP64 partial per 16,384-element chunk -- in a file-scope device array
+// one FP64 partial per 32,768-element chunk -- in a file-scope device array
 // of fixed size, so it never allocates.  The array exists once per GPU that
 // loads this library and stays allocated until the process exits.
 // ---------------------------------------------------------------------------
@@ -755,6 +760,8 @@ namespace {
 
 constexpr uint32_t kStaticMaxChunks = 65536;  // 512 KiB of FP64 partials
 constexpr int kStaticMaxDevices = 64;
+static_assert((BF16OPT_STATIC_NORM_MAX_ELEMS + kChunk - 1) / kChunk <= kStaticMaxChunks,
+              "the static norm scratch must hold one partial per chunk of the largest accepted n");
 
 static __device__ __align__(256) double g_static_partials[kStaticMaxChunks];
 

@@ -676,3 +676,34 @@ def test_skip_nonfinite_step(use_graph):
     sh.close()
     for k in ("p", "m", "v", "p_bf16"):
         assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+
+
+@needs_cuda
+def test_step_counter_calls_wait_for_steps_on_side_streams():
+    """get_step, set_step and the set_* calls are ordered after a step still in
+    flight on a non-blocking stream: a sleep kernel (about 20 ms) holds the
+    stream, so a plain copy on the legacy stream would read or write the
+    counter before the step's own increment."""
+    wl = workloads.custom(291, [50_000, 77], decay=[True, False], gas=1, steps=3, grad_sigma=0.1)
+    sh = GpuShard(wl)
+    side = torch.cuda.Stream()
+
+    def step_on_side(step_index):
+        sgpu.fill_grad(wl, step_index, 0, sh.gbuf)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(40_000_000)
+            sh.opt.accumulate(sh.grads_arg(), first=True, last=True, stream=side)
+            sh.opt.grad_norm(stream=side)
+            sh.opt.step(stream=side)
+
+    step_on_side(0)
+    assert sh.opt.t == 1                 # read waits for the step behind the sleep
+    step_on_side(1)
+    sh.opt.t = 10                        # write is ordered after that step (t = 2 there)
+    torch.cuda.synchronize()
+    assert sh.opt.t == 10
+    step_on_side(2)
+    sh.opt.set_skip_nonfinite(False)     # waits too; the step completes first
+    assert sh.opt.t == 11
+    sh.close()
