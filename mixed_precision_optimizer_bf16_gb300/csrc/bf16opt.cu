@@ -824,7 +824,13 @@ k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, f
                 }
             }
         }
-        const double tot = cta_sum((double)cs.s + (double)cs.c, sh);
+        double mine = (double)cs.s + (double)cs.c;
+        if (!isfinite(mine)) {                          // rare: a square overflowed FP32
+            GradPtrs<1> gp;
+            gp.p[0] = nullptr;
+            mine = sumsq_rescaled<false, true, 0, 1, kThreads>(a, gp, 0, head, nq, len, gscale);
+        }
+        const double tot = cta_sum(mine, sh);
         if (threadIdx.x == 0) partials[c] = tot;
     }
 }

@@ -81,7 +81,7 @@ struct NormState {
     int32_t pad;
 };
 
-// Per-group scalars of one step, FP32, precomputed on the host in FP64.
+// Per-group scalars of one step, FP32, computed in FP64 by k_step_scalars.
 struct GroupK {
     float b1, omb1, b2, omb2;
     float eps;
@@ -158,6 +158,12 @@ __device__ __forceinline__ void comp_add_sq(Comp &a, float x) {
     a.c = __fadd_rn(a.c, __fadd_rn(err, e));
 }
 
+// Gradient pointers of one pass, by value (for the out-of-line rescaled sum).
+template <int KA>
+struct GradPtrs {
+    const uint16_t *p[KA];
+};
+
 // Deterministic CTA sum of one double per thread (kThreads threads); result valid in thread 0.
 __device__ __forceinline__ double cta_sum(double x, double *sh) {
 #pragma unroll
@@ -212,6 +218,34 @@ __device__ __forceinline__ float4 fold_quad(const float4 &av, const uint2 *gv, i
         }
     }
     return r;
+}
+
+// A thread's sum of squares over its elements of a chunk, for a thread whose
+// plain FP32 sum came out non-finite.  bf16 has FP32's exponent range, so a
+// gradient above ~1.8e19 is an ordinary value whose square overflows FP32 but
+// not the FP64 sum of squares of the definition.  Each value is multiplied by
+// 2^-96 first (exact for every value above 2^-30), squared and summed the
+// same compensated way, and the sum is scaled back by 2^192 in FP64.  Scaled
+// squares that underflow stand for less than 2^43 each, against a thread sum
+// above FP32's maximum (~2^128): relative 2^-78 even for 128 of them.  A
+// genuinely infinite or NaN element stays non-finite.  Visits the same
+// elements as the vector pass: head, tail, then quads threadIdx.x + k * NT.
+// FOLD: the value is fold(acc?, g...) (not stored by the pass); otherwise
+// acc[i] (stored by the pass, or read alone).
+template <bool FOLD, bool HAS_ACC, int KMAX, int KA, int NT>
+__device__ __noinline__ double sumsq_rescaled(const float *a, GradPtrs<KA> gp, int K, uint32_t head, uint32_t nq,
+                                              uint32_t len, float gscale) {
+    Comp cs = {0.f, 0.f};
+    auto add = [&](uint32_t i) {
+        const float v = FOLD ? fold_scalar<HAS_ACC, KMAX>(a, gp.p, K, i) : a[i];
+        comp_add_sq(cs, __fmul_rn(__fmul_rn(v, gscale), 0x1p-96f));
+    };
+    const uint32_t tail0 = head + (nq << 2);
+    for (uint32_t i = threadIdx.x; i < head; i += NT) add(i);
+    for (uint32_t i = tail0 + threadIdx.x; i < len; i += NT) add(i);
+    for (uint32_t q = threadIdx.x; q < nq; q += NT)
+        for (uint32_t r = 0; r < 4; ++r) add(head + 4 * q + r);
+    return ((double)cs.s + (double)cs.c) * 0x1p192;
 }
 
 // Leading scalar elements before every FP32/bf16 pointer of the chunk is at a
@@ -303,7 +337,14 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
             }
         }
         if (NORM) {
-            const double tot = cta_sum((double)cs.s + (double)cs.c, sh);
+            double mine = (double)cs.s + (double)cs.c;
+            if (!isfinite(mine)) {                      // rare: a square overflowed FP32
+                GradPtrs<KA> gp;
+#pragma unroll
+                for (int j = 0; j < KA; ++j) gp.p[j] = g[j];
+                mine = sumsq_rescaled<!WRITE, HAS_ACC, KMAX, KA, kThreads>(a, gp, K, head, nq, len, gscale);
+            }
+            const double tot = cta_sum(mine, sh);
             if (threadIdx.x == 0) partials[c] = tot;
         }
     }

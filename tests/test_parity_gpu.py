@@ -3,6 +3,7 @@
 Every test here needs a CUDA GPU and the built library; all are marked gpu.
 """
 import ctypes
+import math
 import gc
 
 import numpy as np
@@ -707,3 +708,54 @@ def test_step_counter_calls_wait_for_steps_on_side_streams():
     sh.opt.set_skip_nonfinite(False)     # waits too; the step completes first
     assert sh.opt.t == 11
     sh.close()
+
+
+# Gradient elements whose squares exceed FP32's range (bf16 has FP32's exponent
+# range, so these are ordinary bf16 values), placed in the head, vector body and
+# ragged tail of several chunks and in both tensors.  The largest dominates the
+# norm (about 2.5e30), so the clip coefficient and every stored moment stay
+# normal FP32 numbers.
+BIG_GRADS = {1: 1.5e19, 40_000: -3e25, 40_001: 2.5e30, 65_537: 1e20, 70_000: -7e19, 70_100: 4e22}
+
+
+def _big_gradient_workload():
+    wl = workloads.custom(292, [70_001, 333], decay=[True, False], gas=2, steps=1, grad_sigma=0.1, misalign=1)
+    grads = [synth.fill_grad(wl, 0, k, np.empty(wl.n, np.uint16)) for k in range(wl.gas)]
+    for i, x in BIG_GRADS.items():
+        grads[i % 2][i] = int(np.float32(x).view(np.uint32)) >> 16     # bf16 by truncation
+    return wl, grads
+
+
+@needs_cuda
+@pytest.mark.parametrize("variant", ["stored_last", "defer_last", "all_deferred", "no_last_flag"])
+def test_gradients_whose_squares_overflow_fp32(variant):
+    """The definition's sum of squares is FP64, where 2.5e30 squared is an
+    ordinary number: the norm must be finite and equal the oracle's, the clip
+    must bring the gradient to norm 1, and the step must match element by
+    element -- on every pass that computes the norm's partials (stored LAST,
+    deferred LAST, all deferred, and the norm pass over the stored acc)."""
+    import harness
+    wl, grads = _big_gradient_workload()
+    pattern = {"stored_last": [False, False], "defer_last": [False, True], "all_deferred": [True, True],
+               "no_last_flag": [False, False]}[variant]
+    sh = GpuShard(wl, defer=pattern)
+    for k in range(wl.gas):
+        buf = sh.gbufs[k % len(sh.gbufs)]
+        buf.copy_(torch.from_numpy(grads[k].view(np.int16)))
+        sh.opt.accumulate(sh.grads_arg(buf), first=k == 0,
+                          last=k == wl.gas - 1 and variant != "no_last_flag", defer=pattern[k])
+    norm = sh.opt.grad_norm(sync=True)
+    sh.opt.step()
+    torch.cuda.synchronize()
+    got = sh.states()
+    sh.close()
+
+    p0 = synth.fill_master(wl, np.empty(wl.n, np.float32))
+    ref = oracle.run_dense(p0.copy(), lambda s, k: grads[k], wl.ranges(), ogroups(wl), 1, wl.gas, wl.max_norm)
+    S = ref["sumsq"][0]
+    assert math.isfinite(S) and S > 6e60
+    assert math.isfinite(norm) and abs(norm - math.sqrt(S)) <= harness.REL * math.sqrt(S)
+    sc = {"M": np.zeros(wl.n), "A": np.abs(p0.astype(np.float64))}
+    harness._update_scales(sc, wl, wl.group_of(np.arange(wl.n)), ref["acc"], ref["clip"][0], ref["m"], ref["v"],
+                           1, 1.0)
+    compare(got, ref, sc, wl, check_acc=variant in ("stored_last", "no_last_flag"))

@@ -9,6 +9,7 @@ failure has already run every other test; it must pass alone in a fresh
 process as well as after the other tests.
 """
 import ctypes
+import math
 
 import numpy as np
 import pytest
@@ -79,3 +80,34 @@ def test_static_norm_matches_handle_norm_twice():
         C.BF16OPT_ERR_INVALID_ARG
     assert "exceeds" in C.bf16opt_last_error(None)
     opt.close()
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+def test_static_norm_of_values_whose_squares_overflow_fp32():
+    """FP32 accumulator values of 1.5e19 ... 3e30 are finite but their squares
+    are not in FP32; the norm is the FP64 sum of squares (each square of an
+    FP32 value is exact in FP64; math.fsum rounds the sum once).  Values sit in
+    the head, the vector body and the tail of the chunks.  An infinite element
+    still gives an infinite norm."""
+    C.load()
+    rng = np.random.default_rng(5)
+    n = 200_003
+    host = rng.normal(0.0, 0.1, n).astype(np.float32)
+    for i, x in {0: 1.5e19, 3: -2e20, 70_000: 3e30, 70_001: -1e25, n - 1: 7e21}.items():
+        host[i] = x
+    acc = torch.empty(n + 64, dtype=torch.float32, device="cuda")[3:3 + n]
+    acc.copy_(torch.from_numpy(host))
+    res = torch.zeros(3, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), n, 1.0, 1.0, res.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    sumsq, norm, clip = _read(res)
+    ref = math.fsum(float(x) * float(x) for x in host.tolist())
+    assert abs(sumsq - ref) <= REL * ref
+    assert abs(norm - math.sqrt(ref)) <= REL * math.sqrt(ref)
+    assert abs(clip - 1.0 / math.sqrt(ref)) <= REL / math.sqrt(ref)
+
+    acc[5] = float("inf")
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), n, 1.0, 1.0, res.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    assert math.isinf(_read(res)[1])
