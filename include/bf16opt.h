@@ -267,12 +267,13 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t);
  * Computes, without a handle and without allocating anything, the global L2
  * norm of a flat FP32 gradient accumulator `grad_accum` of n elements (each
  * element times grad_scale, rounded to FP32), with the same deterministic
- * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard, and the
+ * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard (whose
+ * master buffer has the accumulator's offset modulo 128 bytes), and the
  * clip coefficient c = max_grad_norm / norm if norm > max_grad_norm (> 0),
  * else 1.  `out` is device-accessible memory owned by the caller; the result
  * is written there on `stream` (nothing is synchronised).
  *
- * Scratch: one FP64 partial per 32,768-element chunk, kept in a file-scope
+ * Scratch: one FP64 partial per chunk of up to 32,768 elements, kept in a file-scope
  * device array of 65,536 entries (512 KiB) that every GPU loading this
  * library holds until the process exits; hence n is limited to
  * BF16OPT_STATIC_NORM_MAX_ELEMS (2^30) elements and larger n is rejected with

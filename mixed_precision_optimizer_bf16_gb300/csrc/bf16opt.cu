@@ -121,6 +121,10 @@ bool overlaps(std::vector<Interval> &iv) {
     return false;
 }
 
+// Elements by which the first chunk over an FP32 buffer starting at `p` is
+// shorter than kChunk: p's element index modulo kHeadAlign.
+uint32_t first_chunk_cut(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) & (kHeadAlign - 1)); }
+
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 
@@ -417,13 +421,20 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     }
     if (overlaps(iv)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "state buffers overlap");
 
-    // Chunk table: every segment cut into kChunk-element chunks, in segment order.
+    // Chunk table: every segment cut into chunks of at most kChunk elements, in
+    // segment order.  The first chunk of a segment is shortened by the master
+    // buffer's element offset from a kHeadAlign boundary, so that every later
+    // chunk starts on such a boundary: those chunks need no scalar head, and no
+    // 128-byte line of the (equally offset) buffers is split between two chunks.
     std::vector<Chunk> chunks;
     for (uint32_t si = 0; si < segs.size(); ++si) {
         const Seg &s = segs[si];
-        for (uint64_t off = 0; off < s.numel; off += kChunk) {
+        const uint64_t first = kChunk - first_chunk_cut(s.p);
+        for (uint64_t off = 0; off < s.numel;) {
             if (chunks.size() >= 0xffffffffull) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
-            chunks.push_back({off, si, (uint32_t)std::min<uint64_t>(kChunk, s.numel - off)});
+            const uint64_t len = std::min<uint64_t>(off == 0 ? first : kChunk, s.numel - off);
+            chunks.push_back({off, si, (uint32_t)len});
+            off += len;
         }
     }
     // LIST: first chunk of every tensor (empty tensors point at the next one's).
@@ -760,7 +771,7 @@ namespace {
 
 constexpr uint32_t kStaticMaxChunks = 65536;  // 512 KiB of FP64 partials
 constexpr int kStaticMaxDevices = 64;
-static_assert((BF16OPT_STATIC_NORM_MAX_ELEMS + kChunk - 1) / kChunk <= kStaticMaxChunks,
+static_assert((BF16OPT_STATIC_NORM_MAX_ELEMS + kHeadAlign - 1 + kChunk - 1) / kChunk <= kStaticMaxChunks,
               "the static norm scratch must hold one partial per chunk of the largest accepted n");
 
 static __device__ __align__(256) double g_static_partials[kStaticMaxChunks];
@@ -791,20 +802,25 @@ int static_scratch(int dev, double **out, std::string &msg) {
 // as the handle's norm pass over a one-range FLAT shard.
 template <int U>
 __global__ void __launch_bounds__(kThreads)
-k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, float gscale,
+k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, uint32_t cut, float gscale,
                   double *__restrict__ partials) {
     __shared__ double sh[kThreads / 32];
     for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const uint64_t start = (uint64_t)c * kChunk;
-        const uint32_t len = (uint32_t)((n - start) < kChunk ? (n - start) : kChunk);
+        // chunk c = [c kChunk - cut, (c + 1) kChunk - cut) clipped to [0, n): the
+        // handle's chunking of a one-range FLAT shard over the same buffer
+        const uint64_t start = c == 0 ? 0 : (uint64_t)c * kChunk - cut;
+        const uint64_t lim = (uint64_t)(c + 1) * kChunk - cut;
+        const uint64_t end = lim < n ? lim : n;
+        const uint32_t len = (uint32_t)(end - start);
         const float *a = acc + start;
-        uint32_t head = (4u - phase4_f32(a)) & 3u;
+        uint32_t head = (kHeadAlign - phaseA_f32(a)) & (kHeadAlign - 1);
         if (head > len) head = len;
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
         Comp cs = {0.f, 0.f};
-        for (uint32_t i = threadIdx.x; i < head; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
-        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
+        const uint32_t rh = scalar_lane<kThreads>(c, 0), rt = scalar_lane<kThreads>(c, 1);
+        for (uint32_t i = rh; i < head; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
+        for (uint32_t i = tail0 + rt; i < len; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
         const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
         for (uint32_t base = threadIdx.x; base < nq; base += kThreads * U) {
             float4 av[U];
@@ -828,7 +844,7 @@ k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, f
         if (!isfinite(mine)) {                          // rare: a square overflowed FP32
             GradPtrs<1> gp;
             gp.p[0] = nullptr;
-            mine = sumsq_rescaled<false, true, 0, 1, kThreads>(a, gp, 0, head, nq, len, gscale);
+            mine = sumsq_rescaled<false, true, 0, 1, kThreads>(a, gp, 0, head, nq, len, gscale, rh, rt);
         }
         const double tot = cta_sum(mine, sh);
         if (threadIdx.x == 0) partials[c] = tot;
@@ -885,11 +901,12 @@ extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, flo
     if (rc) return fail(nullptr, rc, msg);
     int sms = 1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-    const uint32_t nchunks = (uint32_t)((n + kChunk - 1) / kChunk);
+    const uint32_t cut = first_chunk_cut(grad_accum);
+    const uint32_t nchunks = n == 0 ? 0u : (uint32_t)((n + cut + kChunk - 1) / kChunk);
     cudaStream_t st = (cudaStream_t)stream;
     if (nchunks > 0) {
         const uint32_t grid = std::min<uint32_t>(nchunks, (uint32_t)sms * 8u);
-        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, grad_scale, partials);
+        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, cut, grad_scale, partials);
     }
     k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out);
     cudaError_t e = cudaGetLastError();

@@ -50,10 +50,19 @@ namespace bf16k {
 #ifndef BF16K_CHUNK
 #define BF16K_CHUNK 32768
 #endif
+#ifndef BF16K_HEAD_ALIGN
+#define BF16K_HEAD_ALIGN 32
+#endif
 constexpr int kAccThreads = BF16K_ACC_THREADS;    // threads per CTA, accumulate / norm passes
 constexpr int kStepThreads = BF16K_STEP_THREADS;  // threads per CTA, fused step
 constexpr int kThreads = kAccThreads;
 constexpr uint32_t kChunk = BF16K_CHUNK;          // elements per chunk (multiple of 4)
+// The vector body of a chunk starts where the lead pointer's element index is
+// a multiple of kHeadAlign (power of two, >= 4): 128-byte FP32 / 64-byte bf16
+// boundaries at 32, so that no warp's 512-byte access starts or ends inside a
+// 32-byte sector when the buffers are offset from those boundaries.
+constexpr uint32_t kHeadAlign = BF16K_HEAD_ALIGN;
+static_assert(kHeadAlign >= 4 && (kHeadAlign & (kHeadAlign - 1)) == 0, "kHeadAlign: a power of two >= 4");
 constexpr int kMaxGroups = 16;
 constexpr int kListSlots = 1024;     // gradient pointers per LIST-mode launch
 constexpr int kFinalThreads = 1024;
@@ -180,10 +189,12 @@ __device__ __forceinline__ double cta_sum(double x, double *sh) {
     return r;
 }
 
-// Leading element count until a pointer's FP32/bf16 element index is a
-// multiple of 4 (16-byte FP32 / 8-byte bf16 boundary).
+// A pointer's FP32/bf16 element index modulo 4 (16-byte FP32 / 8-byte bf16
+// boundary) and modulo kHeadAlign.
 __device__ __forceinline__ uint32_t phase4_f32(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) & 3u); }
 __device__ __forceinline__ uint32_t phase4_b16(const void *p) { return (uint32_t)(((uintptr_t)p >> 1) & 3u); }
+__device__ __forceinline__ uint32_t phaseA_f32(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) & (kHeadAlign - 1)); }
+__device__ __forceinline__ uint32_t phaseA_b16(const void *p) { return (uint32_t)(((uintptr_t)p >> 1) & (kHeadAlign - 1)); }
 
 // ---------------------------------------------------------------- accumulate
 
@@ -227,37 +238,65 @@ __device__ __forceinline__ float4 fold_quad(const float4 &av, const uint2 *gv, i
 // 2^-96 first (exact for every value above 2^-30), squared and summed the
 // same compensated way, and the sum is scaled back by 2^192 in FP64.  Scaled
 // squares that underflow stand for less than 2^43 each, against a thread sum
-// above FP32's maximum (~2^128): relative 2^-78 even for 128 of them.  A
-// genuinely infinite or NaN element stays non-finite.  Visits the same
-// elements as the vector pass: head, tail, then quads threadIdx.x + k * NT.
+// above FP32's maximum (~2^128): relative 2^-78 even for 128 of them.  The
+// scaled sum of finite values cannot overflow, so an infinite sum here means
+// an infinite element and is returned as +Inf (the compensation term is NaN
+// then, Inf - Inf); a NaN element gives NaN -- as the definition's FP64 sum
+// would.  Visits the same
+// elements as the vector pass: head (from rh), tail (from rt), then quads
+// threadIdx.x + k * NT.
 // FOLD: the value is fold(acc?, g...) (not stored by the pass); otherwise
 // acc[i] (stored by the pass, or read alone).
 template <bool FOLD, bool HAS_ACC, int KMAX, int KA, int NT>
 __device__ __noinline__ double sumsq_rescaled(const float *a, GradPtrs<KA> gp, int K, uint32_t head, uint32_t nq,
-                                              uint32_t len, float gscale) {
+                                              uint32_t len, float gscale, uint32_t rh, uint32_t rt) {
     Comp cs = {0.f, 0.f};
     auto add = [&](uint32_t i) {
         const float v = FOLD ? fold_scalar<HAS_ACC, KMAX>(a, gp.p, K, i) : a[i];
         comp_add_sq(cs, __fmul_rn(__fmul_rn(v, gscale), 0x1p-96f));
     };
     const uint32_t tail0 = head + (nq << 2);
-    for (uint32_t i = threadIdx.x; i < head; i += NT) add(i);
-    for (uint32_t i = tail0 + threadIdx.x; i < len; i += NT) add(i);
+    for (uint32_t i = rh; i < head; i += NT) add(i);
+    for (uint32_t i = tail0 + rt; i < len; i += NT) add(i);
     for (uint32_t q = threadIdx.x; q < nq; q += NT)
         for (uint32_t r = 0; r < 4; ++r) add(head + 4 * q + r);
-    return ((double)cs.s + (double)cs.c) * 0x1p192;
+    const double s = isinf(cs.s) ? (double)cs.s : (double)cs.s + (double)cs.c;
+    return s * 0x1p192;
 }
 
-// Leading scalar elements before every FP32/bf16 pointer of the chunk is at a
-// 16-byte FP32 / 8-byte bf16 boundary, or `len` when they disagree (the chunk
-// then runs element-wise).
+__host__ __device__ constexpr int ilog2(uint32_t x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+
+// Thread index, rotated by whole warps, that takes a chunk's scalar head
+// (half = 0) or tail (half = 1) elements.  The scalar elements cost a dependent
+// load -> store round trip; always giving them to warp 0 made that warp lag
+// further behind with every chunk (nothing re-synchronises the warps between
+// chunks) and left the SM nearly idle while it caught up at the end.  The warp
+// is the top bits of a Fibonacci hash of the chunk index (Knuth, TAOCP vol. 3,
+// section 6.4), which spreads the chunks b, b + G, b + 2G, ... of one CTA over
+// all warps for any grid size G; the tail goes to the warp half-way round.
+// The map depends only on the chunk index, so results stay grid-independent.
+template <int NT>
+__device__ __forceinline__ uint32_t scalar_lane(uint32_t c, uint32_t half) {
+    constexpr uint32_t W = NT / 32;
+    static_assert(W >= 2 && (W & (W - 1)) == 0, "scalar_lane: a power-of-two number of warps");
+    constexpr int kShift = 32 - ilog2(W);
+    const uint32_t w = (c * 2654435761u + (half ? 0x80000000u : 0u)) >> kShift;
+    return (threadIdx.x + NT - w * 32) % NT;
+}
+
+// Leading scalar elements of the chunk: up to the first element at which the
+// lead pointer (the FP32 one if used, else the first gradient) sits on a
+// kHeadAlign-element boundary; every other pointer is then at least on a
+// 16-byte FP32 / 8-byte bf16 boundary, because all must share their element
+// index modulo 4 -- or `len` when they do not (the chunk runs element-wise).
 template <int KMAX>
 __device__ __forceinline__ uint32_t chunk_head(const void *fp32_ptr, bool use_fp32, const uint16_t *const *g, int K,
                                                uint32_t len) {
-    uint32_t ph = 0;
+    uint32_t ph = 0, lead = 0;
     bool have = false, vec = true;
     if (use_fp32) {
         ph = phase4_f32(fp32_ptr);
+        lead = phaseA_f32(fp32_ptr);
         have = true;
     }
 #pragma unroll
@@ -265,11 +304,12 @@ __device__ __forceinline__ uint32_t chunk_head(const void *fp32_ptr, bool use_fp
         if (j < K) {
             const uint32_t pg = phase4_b16(g[j]);
             if (have && pg != ph) vec = false;
+            if (!have) lead = phaseA_b16(g[j]);
             ph = pg;
             have = true;
         }
     }
-    uint32_t head = vec ? ((4u - ph) & 3u) : len;
+    uint32_t head = vec ? ((kHeadAlign - lead) & (kHeadAlign - 1)) : len;
     return head > len ? len : head;
 }
 
@@ -301,8 +341,9 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
             if (WRITE) a[i] = v;
             if (NORM) comp_add_sq(cs, __fmul_rn(v, gscale));
         };
-        for (uint32_t i = threadIdx.x; i < head; i += kThreads) scalar(i);
-        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kThreads) scalar(i);
+        const uint32_t rh = scalar_lane<kThreads>(c, 0), rt = scalar_lane<kThreads>(c, 1);
+        for (uint32_t i = rh; i < head; i += kThreads) scalar(i);
+        for (uint32_t i = tail0 + rt; i < len; i += kThreads) scalar(i);
 
         const uint2 *g4[KA];
 #pragma unroll
@@ -342,7 +383,7 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
                 GradPtrs<KA> gp;
 #pragma unroll
                 for (int j = 0; j < KA; ++j) gp.p[j] = g[j];
-                mine = sumsq_rescaled<!WRITE, HAS_ACC, KMAX, KA, kThreads>(a, gp, K, head, nq, len, gscale);
+                mine = sumsq_rescaled<!WRITE, HAS_ACC, KMAX, KA, kThreads>(a, gp, K, head, nq, len, gscale, rh, rt);
             }
             const double tot = cta_sum(mine, sh);
             if (threadIdx.x == 0) partials[c] = tot;
@@ -506,8 +547,9 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             v[i] = o.v;
             bf[i] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
         };
-        for (uint32_t i = threadIdx.x; i < head; i += kStepThreads) scalar(i);
-        for (uint32_t i = tail0 + threadIdx.x; i < len; i += kStepThreads) scalar(i);
+        const uint32_t rh = scalar_lane<kStepThreads>(c, 0), rt = scalar_lane<kStepThreads>(c, 1);
+        for (uint32_t i = rh; i < head; i += kStepThreads) scalar(i);
+        for (uint32_t i = tail0 + rt; i < len; i += kStepThreads) scalar(i);
 
         const float4 *a4 = reinterpret_cast<const float4 *>(a + head);
         const uint2 *g4[KA];

@@ -88,7 +88,7 @@ def test_static_norm_of_values_whose_squares_overflow_fp32():
     are not in FP32; the norm is the FP64 sum of squares (each square of an
     FP32 value is exact in FP64; math.fsum rounds the sum once).  Values sit in
     the head, the vector body and the tail of the chunks.  An infinite element
-    still gives an infinite norm."""
+    gives an infinite norm and a zero clip coefficient, a NaN one a NaN norm."""
     C.load()
     rng = np.random.default_rng(5)
     n = 200_003
@@ -110,4 +110,9 @@ def test_static_norm_of_values_whose_squares_overflow_fp32():
     acc[5] = float("inf")
     assert C.bf16opt_grad_norm_static(acc.data_ptr(), n, 1.0, 1.0, res.data_ptr(), stream) == 0
     torch.cuda.synchronize()
-    assert math.isinf(_read(res)[1])
+    sumsq, norm, clip = _read(res)
+    assert math.isinf(norm) and norm > 0 and clip == 0.0
+    acc[7] = float("nan")
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), n, 1.0, 1.0, res.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    assert math.isnan(_read(res)[1])
