@@ -121,8 +121,21 @@ bool overlaps(std::vector<Interval> &iv) {
     return false;
 }
 
+// Elements per chunk of a shard of `total` elements: kChunk from 2^25
+// elements up; smaller shards get proportionally smaller chunks (a power of
+// two, at least kMinChunk), so that they still spread over every SM -- a
+// 1M-element shard in 32,768-element chunks kept 32 of 152 SMs busy.  Depends
+// only on the shard's size, never on the GPU.
+constexpr uint32_t kMinChunk = 2048;
+static_assert(kMinChunk % kHeadAlign == 0 && kMinChunk <= kChunk, "chunk sizes are multiples of kHeadAlign");
+uint32_t chunk_elems(uint64_t total) {
+    uint64_t c = kMinChunk;
+    while (c < kChunk && c * 1024 < total) c <<= 1;
+    return (uint32_t)c;
+}
+
 // Elements by which the first chunk over an FP32 buffer starting at `p` is
-// shorter than kChunk: p's element index modulo kHeadAlign.
+// shorter than the others: p's element index modulo kHeadAlign.
 uint32_t first_chunk_cut(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) & (kHeadAlign - 1)); }
 
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
@@ -421,18 +434,21 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     }
     if (overlaps(iv)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "state buffers overlap");
 
-    // Chunk table: every segment cut into chunks of at most kChunk elements, in
+    // Chunk table: every segment cut into chunks of at most `chunk` elements, in
     // segment order.  The first chunk of a segment is shortened by the master
     // buffer's element offset from a kHeadAlign boundary, so that every later
     // chunk starts on such a boundary: those chunks need no scalar head, and no
     // 128-byte line of the (equally offset) buffers is split between two chunks.
+    uint64_t total = 0;
+    for (const Seg &s : segs) total += s.numel;
+    const uint32_t chunk = chunk_elems(total);
     std::vector<Chunk> chunks;
     for (uint32_t si = 0; si < segs.size(); ++si) {
         const Seg &s = segs[si];
-        const uint64_t first = kChunk - first_chunk_cut(s.p);
+        const uint64_t first = chunk - first_chunk_cut(s.p);
         for (uint64_t off = 0; off < s.numel;) {
             if (chunks.size() >= 0xffffffffull) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
-            const uint64_t len = std::min<uint64_t>(off == 0 ? first : kChunk, s.numel - off);
+            const uint64_t len = std::min<uint64_t>(off == 0 ? first : chunk, s.numel - off);
             chunks.push_back({off, si, (uint32_t)len});
             off += len;
         }
@@ -797,19 +813,19 @@ int static_scratch(int dev, double **out, std::string &msg) {
     return BF16OPT_OK;
 }
 
-// Partial sums of squares of implicit chunks [c*kChunk, min(n, (c+1)*kChunk)) of
+// Partial sums of squares of implicit chunks (sized and cut as in the handle's chunk table) of
 // a flat FP32 buffer: the same thread->element map, compensated sum and CTA tree
 // as the handle's norm pass over a one-range FLAT shard.
 template <int U>
 __global__ void __launch_bounds__(kThreads)
-k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, uint32_t cut, float gscale,
-                  double *__restrict__ partials) {
+k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, uint32_t chunk, uint32_t cut,
+                  float gscale, double *__restrict__ partials) {
     __shared__ double sh[kThreads / 32];
     for (uint32_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        // chunk c = [c kChunk - cut, (c + 1) kChunk - cut) clipped to [0, n): the
+        // chunk c = [c chunk - cut, (c + 1) chunk - cut) clipped to [0, n): the
         // handle's chunking of a one-range FLAT shard over the same buffer
-        const uint64_t start = c == 0 ? 0 : (uint64_t)c * kChunk - cut;
-        const uint64_t lim = (uint64_t)(c + 1) * kChunk - cut;
+        const uint64_t start = c == 0 ? 0 : (uint64_t)c * chunk - cut;
+        const uint64_t lim = (uint64_t)(c + 1) * chunk - cut;
         const uint64_t end = lim < n ? lim : n;
         const uint32_t len = (uint32_t)(end - start);
         const float *a = acc + start;
@@ -901,12 +917,13 @@ extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, flo
     if (rc) return fail(nullptr, rc, msg);
     int sms = 1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-    const uint32_t cut = first_chunk_cut(grad_accum);
-    const uint32_t nchunks = n == 0 ? 0u : (uint32_t)((n + cut + kChunk - 1) / kChunk);
+    const uint32_t chunk = chunk_elems(n), cut = first_chunk_cut(grad_accum);
+    const uint32_t nchunks = n == 0 ? 0u : (uint32_t)((n + cut + chunk - 1) / chunk);
     cudaStream_t st = (cudaStream_t)stream;
     if (nchunks > 0) {
         const uint32_t grid = std::min<uint32_t>(nchunks, (uint32_t)sms * 8u);
-        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, cut, grad_scale, partials);
+        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, chunk, cut, grad_scale,
+                                                                   partials);
     }
     k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out);
     cudaError_t e = cudaGetLastError();
