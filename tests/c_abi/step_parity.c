@@ -1,0 +1,185 @@
+/*
+ * step_parity.c -- the C ABI driven from plain C, checked against the oracle.
+ *
+ * Test program, not part of the library.  Two optimizer steps over a
+ * 100,003-element FLAT shard in two parameter groups (weight decay 0.01 and
+ * 0), every buffer one element past a 256-byte boundary, GAS 3 with the last
+ * micro-batch deferred, run through include/bf16opt.h with device memory from
+ * the CUDA runtime -- no Python, no PyTorch.  The same two steps run through
+ * the FP64 CPU oracle (oracle/oracle.h) on the same seeded inputs
+ * (synth/synth.h).
+ *
+ * Tolerances are those of the parity tests: the norm within 1e-6 relative;
+ * m within 1e-6 of max(|m_ref|, M_t) and the master within 1e-6 of
+ * max(|p_ref|, A_t), where M_t = b1 M_{t-1} + (1 - b1)|gc_t| and
+ * A_t = A_{t-1}(1 - lr wd) + lr |u_t| (A_0 = |p_0|) are the sums of the
+ * magnitudes of the terms of each recurrence; v within 1e-6 relative; and
+ * every bf16 parameter the round-to-nearest-even bf16 of the GPU's master.
+ *
+ * Exit status: 0 when everything agrees, 1 on a parity failure, 2 on an API
+ * or CUDA error.
+ */
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime_api.h>
+
+#include "bf16opt.h"
+#include "oracle.h"
+#include "synth.h"
+
+#define N 100003u
+#define SPLIT 70001u      /* [0, SPLIT) decays, [SPLIT, N) does not */
+#define GAS 3u
+#define STEPS 2u
+#define WORKLOAD 31u
+#define REL 1e-6
+
+static int api(int rc, const char *what, const bf16opt_t *h) {
+    if (rc < 0) {
+        fprintf(stderr, "%s: %s (%s)\n", what, bf16opt_error_string(rc), bf16opt_last_error(h));
+        exit(2);
+    }
+    return rc;
+}
+
+static void cuda(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) {
+        fprintf(stderr, "%s: %s\n", what, cudaGetErrorString(e));
+        exit(2);
+    }
+}
+
+/* Device buffer of `count` elements of `size` bytes, one element past the
+ * allocation's (256-byte aligned) start; *base receives what to free. */
+static void *dev_offset(size_t count, size_t size, void **base) {
+    cuda(cudaMalloc(base, (count + 64) * size), "cudaMalloc");
+    return (char *)*base + size;
+}
+
+int main(void) {
+    const bf16opt_group_t groups[2] = {{6e-5f, 0.9f, 0.95f, 1e-8f, 0.01f}, {6e-5f, 0.9f, 0.95f, 1e-8f, 0.0f}};
+    orc_group_t ogroups[2];
+    for (int g = 0; g < 2; ++g) {   /* the oracle gets the same FP32-rounded values */
+        ogroups[g].lr = groups[g].lr;
+        ogroups[g].beta1 = groups[g].beta1;
+        ogroups[g].beta2 = groups[g].beta2;
+        ogroups[g].eps = groups[g].eps;
+        ogroups[g].weight_decay = groups[g].weight_decay;
+    }
+    const bf16opt_range_t ranges[2] = {{0, SPLIT, 0, 0}, {SPLIT, N, 1, 0}};
+
+    /* host inputs and oracle state */
+    float *p = malloc(N * sizeof(float)), *m = calloc(N, sizeof(float)), *v = calloc(N, sizeof(float));
+    float *acc = calloc(N, sizeof(float));
+    uint16_t *pb = calloc(N, sizeof(uint16_t));
+    uint16_t *grads[GAS];
+    double *M = calloc(N, sizeof(double)), *A = malloc(N * sizeof(double));
+    const uint64_t kmaster = synth_key(0, WORKLOAD, SYNTH_KIND_MASTER, 0, 0);
+    for (uint32_t i = 0; i < N; ++i) {
+        p[i] = synth_normal_f32(kmaster, i, synth_scale_for_sigma(0.02));
+        A[i] = fabs((double)p[i]);
+    }
+    for (uint32_t k = 0; k < GAS; ++k) grads[k] = malloc(N * sizeof(uint16_t));
+
+    /* device state */
+    void *bases[5 + GAS];
+    float *d_p = dev_offset(N, 4, &bases[0]), *d_m = dev_offset(N, 4, &bases[1]);
+    float *d_v = dev_offset(N, 4, &bases[2]), *d_acc = dev_offset(N, 4, &bases[3]);
+    uint16_t *d_pb = dev_offset(N, 2, &bases[4]);
+    uint16_t *d_g[GAS];
+    for (uint32_t k = 0; k < GAS; ++k) d_g[k] = dev_offset(N, 2, &bases[5 + k]);
+    cuda(cudaMemcpy(d_p, p, N * sizeof(float), cudaMemcpyHostToDevice), "upload masters");
+    cuda(cudaMemset(d_m, 0, N * sizeof(float)), "memset");
+    cuda(cudaMemset(d_v, 0, N * sizeof(float)), "memset");
+
+    bf16opt_desc_t d;
+    memset(&d, 0, sizeof d);
+    d.mode = BF16OPT_FLAT;
+    d.n_groups = 2;
+    d.groups = groups;
+    d.n = N;
+    d.master = d_p;
+    d.exp_avg = d_m;
+    d.exp_avg_sq = d_v;
+    d.grad_accum = d_acc;
+    d.param_bf16 = d_pb;
+    d.ranges = ranges;
+    d.n_ranges = 2;
+    d.max_grad_norm = 1.0f;
+    d.grad_scale = 1.0f;
+    bf16opt_t *h = NULL;
+    api(bf16opt_create(&d, &h), "bf16opt_create", NULL);
+
+    int bad = 0;
+    double worst_norm = 0.0;
+    for (uint32_t s = 0; s < STEPS; ++s) {
+        for (uint32_t k = 0; k < GAS; ++k) {
+            const uint64_t key = synth_key(0, WORKLOAD, SYNTH_KIND_GRAD, s, k);
+            for (uint32_t i = 0; i < N; ++i) grads[k][i] = synth_grad_bf16(key, i, synth_scale_for_sigma(0.05), 0, 0);
+            cuda(cudaMemcpy(d_g[k], grads[k], N * sizeof(uint16_t), cudaMemcpyHostToDevice), "upload gradient");
+            unsigned flags = (k == 0 ? BF16OPT_FIRST : 0u) | (k == GAS - 1 ? BF16OPT_LAST | BF16OPT_DEFER : 0u);
+            api(bf16opt_accumulate(h, d_g[k], NULL, flags, NULL), "bf16opt_accumulate", h);
+            orc_accumulate(acc, grads[k], N, k == 0, 1);
+        }
+        double norm = 0.0;
+        api(bf16opt_grad_norm(h, NULL, &norm), "bf16opt_grad_norm", h);
+        api(bf16opt_step(h, NULL, NULL), "bf16opt_step", h);
+
+        const double S = orc_sumsq(acc, N, 1.0f, 1), c = orc_clip_coef(S, 1.0);
+        const int64_t t = (int64_t)s + 1;
+        orc_adamw(p, m, v, pb, acc, SPLIT, 1.0f, c, &ogroups[0], t, 1);
+        orc_adamw(p + SPLIT, m + SPLIT, v + SPLIT, pb + SPLIT, acc + SPLIT, N - SPLIT, 1.0f, c, &ogroups[1], t, 1);
+        const double rel = fabs(norm - sqrt(S)) / sqrt(S);
+        if (rel > worst_norm) worst_norm = rel;
+        if (!(rel <= REL)) {
+            fprintf(stderr, "step %u: norm %.17g vs %.17g\n", s, norm, sqrt(S));
+            bad = 1;
+        }
+        /* operand scales of the recurrences (from the oracle's stored state) */
+        for (uint32_t i = 0; i < N; ++i) {
+            const orc_group_t *G = &ogroups[i < SPLIT ? 0 : 1];
+            M[i] = G->beta1 * M[i] + (1.0 - G->beta1) * fabs((double)acc[i]) * c;
+            const double u = fabs((double)m[i] / (1.0 - pow(G->beta1, (double)t))) /
+                             (sqrt((double)v[i] / (1.0 - pow(G->beta2, (double)t))) + G->eps);
+            A[i] = A[i] * (1.0 - G->lr * G->weight_decay) + G->lr * u;
+        }
+    }
+    cuda(cudaDeviceSynchronize(), "device sync");
+
+    float *gp = malloc(N * sizeof(float)), *gm = malloc(N * sizeof(float)), *gv = malloc(N * sizeof(float));
+    uint16_t *gpb = malloc(N * sizeof(uint16_t));
+    cuda(cudaMemcpy(gp, d_p, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
+    cuda(cudaMemcpy(gm, d_m, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
+    cuda(cudaMemcpy(gv, d_v, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
+    cuda(cudaMemcpy(gpb, d_pb, N * sizeof(uint16_t), cudaMemcpyDeviceToHost), "download");
+    int64_t steps_done = 0;
+    api(bf16opt_get_step(h, &steps_done), "bf16opt_get_step", h);
+    if (steps_done != STEPS) {
+        fprintf(stderr, "step counter %lld, expected %u\n", (long long)steps_done, STEPS);
+        bad = 1;
+    }
+
+    double worst_m = 0.0, worst_v = 0.0, worst_p = 0.0;
+    for (uint32_t i = 0; i < N; ++i) {
+        const double sm = fmax(fabs((double)m[i]), M[i]), sv = fabs((double)v[i]), sp = fmax(fabs((double)p[i]), A[i]);
+        const double em = fabs((double)gm[i] - m[i]), ev = fabs((double)gv[i] - v[i]), ep = fabs((double)gp[i] - p[i]);
+        if (!(em <= REL * sm) || !(ev <= REL * sv) || !(ep <= REL * sp) || gpb[i] != orc_f32_to_bf16(gp[i])) {
+            if (bad < 10)
+                fprintf(stderr, "element %u: m %.9g/%.9g v %.9g/%.9g p %.9g/%.9g bf16 %04x\n", i, gm[i], m[i], gv[i],
+                        v[i], gp[i], p[i], gpb[i]);
+            bad += 1;
+        }
+        if (sm > 0 && em / sm > worst_m) worst_m = em / sm;
+        if (sv > 0 && ev / sv > worst_v) worst_v = ev / sv;
+        if (sp > 0 && ep / sp > worst_p) worst_p = ep / sp;
+    }
+    printf("c-abi step parity: %u elements, %u steps, GAS %u; norm rel err %.3g; scaled err m %.3g v %.3g p %.3g; %s\n",
+           N, STEPS, GAS, worst_norm, worst_m, worst_v, worst_p, bad ? "FAIL" : "ok");
+
+    api(bf16opt_destroy(h), "bf16opt_destroy", NULL);
+    for (int k = 0; k < (int)(5 + GAS); ++k) cudaFree(bases[k]);
+    return bad ? 1 : 0;
+}
