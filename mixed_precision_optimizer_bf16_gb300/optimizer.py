@@ -20,6 +20,31 @@ def _ptr(t):
     return t.data_ptr() if t is not None else 0
 
 
+_BF16_BITS = tuple(d for d in (torch.bfloat16, torch.int16, getattr(torch, "uint16", None)) if d is not None)
+
+
+def _check_buffer(t, what, dtypes, numel=None):
+    """A device tensor the library may read/write through a raw pointer: CUDA,
+    contiguous, one of `dtypes`, and `numel` elements when given.  The C ABI
+    receives bare pointers and cannot check any of this itself."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{what}: must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{what}: {t.numel()} elements, expected {numel}")
+
+
+def _check_state(d, what):
+    n = d["master"].numel()
+    for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum"):
+        _check_buffer(d[k], f"{what}[{k!r}]", (torch.float32,), n)
+    _check_buffer(d["param_bf16"], f"{what}['param_bf16']", _BF16_BITS, n)
+    return n
+
+
 def _stream_handle(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -142,12 +167,14 @@ class BF16Optimizer:
             raise ValueError("give exactly one of flat= or tensors=")
         self.groups = [dict(g) for g in groups]
         if flat is not None:
-            n = flat["master"].numel()
+            n = _check_state(flat, "flat")
+            self.n, self.numels = n, None
             self.desc = C.flat_desc(n, _ptr(flat["master"]), _ptr(flat["exp_avg"]), _ptr(flat["exp_avg_sq"]),
                                     _ptr(flat["grad_accum"]), _ptr(flat["param_bf16"]), self.groups, ranges,
                                     max_grad_norm, grad_scale)
             self.mode = C.BF16OPT_FLAT
         else:
+            self.n, self.numels = None, [_check_state(t, f"tensors[{i}]") for i, t in enumerate(tensors)]
             tl = [(_ptr(t["master"]), _ptr(t["exp_avg"]), _ptr(t["exp_avg_sq"]), _ptr(t["grad_accum"]),
                    _ptr(t["param_bf16"]), t["master"].numel(), int(t.get("group", 0))) for t in tensors]
             self.desc = C.list_desc(tl, self.groups, max_grad_norm, grad_scale)
@@ -159,9 +186,17 @@ class BF16Optimizer:
         """grad: bf16 (int16-viewed) tensor (FLAT) or list of them (LIST)."""
         flags = (C.BF16OPT_FIRST if first else 0) | (C.BF16OPT_LAST if last else 0) | (C.BF16OPT_DEFER if defer else 0)
         if self.mode == C.BF16OPT_FLAT:
-            rc = C.bf16opt_accumulate(self.h, _ptr(grad), None, flags, _stream_handle(stream))
+            if self.n:
+                _check_buffer(grad, "grad", _BF16_BITS, self.n)
+            rc = C.bf16opt_accumulate(self.h, _ptr(grad) if self.n else 0, None, flags, _stream_handle(stream))
         else:
-            rc = C.bf16opt_accumulate(self.h, 0, [_ptr(g) for g in grad], flags, _stream_handle(stream))
+            if len(grad) != len(self.numels):
+                raise ValueError(f"grad: {len(grad)} tensors, expected {len(self.numels)}")
+            for i, (g, k) in enumerate(zip(grad, self.numels)):
+                if k:
+                    _check_buffer(g, f"grad[{i}]", _BF16_BITS, k)
+            rc = C.bf16opt_accumulate(self.h, 0, [_ptr(g) if k else 0 for g, k in zip(grad, self.numels)], flags,
+                                      _stream_handle(stream))
         return C.check(rc, self.h)
 
     def grad_norm(self, stream=None, sync=False):
@@ -189,7 +224,10 @@ class BF16Optimizer:
         return C.check(C.bf16opt_set_lr_schedule(self.h, self._sched), self.h)
 
     def step(self, lr=None, stream=None):
+        """lr: None (the groups' rates), one rate for every group, or one per group."""
         lrs = None if lr is None else ([float(lr)] * len(self.groups) if not hasattr(lr, "__len__") else list(lr))
+        if lrs is not None and len(lrs) != len(self.groups):
+            raise ValueError(f"lr: {len(lrs)} rates for {len(self.groups)} groups")
         return C.check(C.bf16opt_step(self.h, lrs, _stream_handle(stream)), self.h)
 
     @property

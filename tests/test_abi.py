@@ -145,3 +145,17 @@ def test_valid_descriptor_without_device_is_unsupported(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         C.load(str(tmp_path / "libbf16opt.so"))
+
+
+def test_python_binding_refuses_host_tensors():
+    """The binding checks what the C ABI cannot (bare pointers): state buffers
+    must be contiguous CUDA tensors of the right dtype and size, and it says so
+    before any CUDA call."""
+    torch = pytest.importorskip("torch")
+    from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer
+    n = 16
+    flat = {k: torch.zeros(n, dtype=torch.float32) for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum")}
+    flat["param_bf16"] = torch.zeros(n, dtype=torch.int16)
+    groups = [dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)]
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        BF16Optimizer(groups, flat=flat)

@@ -760,3 +760,39 @@ def test_gradients_whose_squares_overflow_fp32(variant):
     harness._update_scales(sc, wl, wl.group_of(np.arange(wl.n)), ref["acc"], ref["clip"][0], ref["m"], ref["v"],
                            1, 1.0)
     compare(got, ref, sc, wl, check_acc=variant in ("stored_last", "no_last_flag"))
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_python_binding_rejects_mismatched_arguments(mode):
+    """Gradients of the wrong dtype (FP32, FP16), size, layout or device, a
+    gradient list of the wrong length, and a per-group lr list of the wrong
+    length are refused in Python, before the library could read past a buffer;
+    the handle's sequence is untouched and the next correct step matches the
+    oracle."""
+    wl = workloads.custom(293, [5000, 77], decay=[True, False], gas=1, steps=1, grad_sigma=0.1, mode=mode)
+    sh = GpuShard(wl)
+    k0 = wl.n if mode == "flat" else 5000           # the first (or only) gradient tensor
+    bad = [torch.zeros(k0, dtype=torch.float32, device="cuda"),
+           torch.zeros(k0, dtype=torch.float16, device="cuda"),
+           torch.zeros(k0 + 1, dtype=torch.int16, device="cuda"),
+           torch.zeros(2 * k0, dtype=torch.int16, device="cuda")[::2],
+           torch.zeros(k0, dtype=torch.int16)]
+    good_tail = torch.zeros(77, dtype=torch.int16, device="cuda")
+    for b in bad:
+        with pytest.raises(ValueError):
+            sh.opt.accumulate(b if mode == "flat" else [b, good_tail], first=True, last=True)
+    if mode == "list":
+        with pytest.raises(ValueError, match="tensors"):
+            sh.opt.accumulate(sh.grads_arg()[:1], first=True, last=True)
+    sgpu.fill_grad(wl, 0, 0, sh.gbuf)
+    sh.opt.accumulate(sh.grads_arg(), first=True, last=True)
+    sh.opt.grad_norm(sync=True)
+    with pytest.raises(ValueError, match="rates"):
+        sh.opt.step(lr=[1e-4, 1e-4, 1e-4])
+    sh.opt.step()
+    torch.cuda.synchronize()
+    got = sh.states()
+    sh.close()
+    ref, scales = oracle_dense(wl, 1)
+    compare(got, ref, scales, wl)
