@@ -468,6 +468,9 @@ DEFER_PATTERNS = [
     [True] * 5,                                # five pending (8-wide kernels, runtime count 5)
     [True] * 8,                                # the maximum
     [False, True, False, True, False, True, True],
+    [True] * 8 + [False],                      # 8 pending, then a stored pass: pre-fold, then this one
+    [True] * 8 + [False, True],                # ... and a deferred last micro-batch after it
+    [False] + [True] * 8 + [False, False],     # the pre-fold onto a stored accumulator
 ]
 
 
@@ -796,3 +799,33 @@ def test_python_binding_rejects_mismatched_arguments(mode):
     sh.close()
     ref, scales = oracle_dense(wl, 1)
     compare(got, ref, scales, wl)
+
+
+def _random_case(seed):
+    """A seeded random workload and micro-batch deferral pattern: GAS 1..12,
+    1..5 tensors of 1..40,000 elements, FLAT or LIST, misaligned 0..7, and any
+    defer pattern the library accepts (at most 8 deferred micro-batches pending
+    at once; a stored micro-batch after 8 pending makes the library fold them
+    first)."""
+    rng = np.random.default_rng(7_000 + seed)
+    gas = int(rng.integers(1, 13))
+    pattern, pending = [], 0
+    for _ in range(gas):
+        d = bool(rng.integers(0, 2)) and pending < 8
+        pattern.append(d)
+        pending = pending + 1 if d else 0
+    ntens = int(rng.integers(1, 6))
+    sizes = [int(x) for x in rng.integers(1, 40_000, ntens)]
+    wl = workloads.custom(400 + seed, sizes, decay=[bool(x) for x in rng.integers(0, 2, ntens)], gas=gas, steps=2,
+                          grad_sigma=float(rng.choice([1e-3, 0.05, 0.5])), misalign=int(rng.integers(0, 8)),
+                          mode="list" if seed % 2 else "flat")
+    return wl, pattern, float(rng.choice([1.0, 0.5, 3.0]))
+
+
+@needs_cuda
+@pytest.mark.parametrize("seed", range(16))
+def test_random_sequences_match_oracle(seed):
+    """Random shapes, layouts, GAS and deferral patterns: every one equals the
+    oracle (norms, m, v, master, bf16) over two steps."""
+    wl, pattern, gscale = _random_case(seed)
+    dense_parity(wl, defer=pattern, grad_scale=gscale)
