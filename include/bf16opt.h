@@ -21,11 +21,13 @@
  * Conventions.
  *   - Every buffer is caller-owned device memory (e.g. from PyTorch) that must
  *     outlive the handle; buffers must not overlap.  The library owns only
- *     its scratch (segment/chunk tables, norm partials, norm scalars).
+ *     its scratch (segment/chunk tables, norm partials, norm scalars, the
+ *     step counter and the per-step scalars).
  *   - FP32 buffers must be 4-byte aligned and bf16 buffers 2-byte aligned
  *     (BF16OPT_ERR_ALIGNMENT otherwise).  Any offset modulo 16 bytes works;
  *     full speed needs every buffer of a tensor to share the same element
- *     offset modulo 16 bytes.
+ *     offset modulo 16 bytes, and the last few percent the same offset
+ *     modulo 128 bytes (any such offset runs as fast as an aligned one).
  *   - Elements are counted in uint64_t; a tensor or shard may exceed 2^32.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  All device work is enqueued on it; no call synchronises
@@ -36,6 +38,12 @@
  *     bf16opt_last_error() gives a one-line message.
  *   - A handle is bound to the device that was current at bf16opt_create and
  *     is not thread-safe: use one handle from one host thread at a time.
+ *     The library keeps a registry of live handles: a pointer that
+ *     bf16opt_create did not return, or a handle already destroyed, is
+ *     rejected with BF16OPT_ERR_INVALID_ARG by every call (bf16opt_destroy
+ *     included) and never dereferenced.  bf16opt_destroy frees all the
+ *     handle's memory but a small host record, so no later handle ever
+ *     receives a destroyed handle's address.
  *   - Results are deterministic and do not depend on the launch grid (the
  *     environment variable BF16OPT_MAX_GRID, read at create, caps the CTAs
  *     per launch; it exists to test exactly that).
@@ -244,7 +252,8 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
 int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable);
 
 /* Frees the library's scratch (waits for the device); the caller's buffers
- * are untouched.  NULL is accepted. */
+ * are untouched.  NULL is accepted.  A pointer that is not a live handle
+ * (never created, or already destroyed) gives BF16OPT_ERR_INVALID_ARG. */
 int bf16opt_destroy(bf16opt_t *h);
 
 /* Step counter t (number of completed steps, kept on the device), for
@@ -298,6 +307,19 @@ typedef struct {
 
 int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, float grad_scale, float max_grad_norm,
                              bf16opt_norm_result_t *out, void *stream);
+
+/* ---- checked build -------------------------------------------------------
+ * No counterpart in the paper: a debugging aid standing in for a memory
+ * checker.  In a build compiled with -DBF16K_CHECKS the kernels test, before
+ * each chunk's accesses, that the chunk lies inside its segment, that its
+ * scalar head and vector body stay inside the chunk and that every vector
+ * pointer is 16-byte (FP32) / 8-byte (bf16) aligned; a violation sets a bit in
+ * a device word (1 = chunk outside its segment, 2 = body outside the chunk,
+ * 4 = misaligned vector pointer) and the chunk is skipped instead of accessed.
+ * This call waits for the device, stores the word into *bits and clears it.
+ * Release builds: *bits = 0 and BF16OPT_ERR_UNSUPPORTED.
+ * Errors: INVALID_ARG (bits NULL), UNSUPPORTED, CUDA. */
+int bf16opt_debug_faults(uint32_t *bits);
 
 /* Static message of a status code; one-line message of the handle's last error. */
 const char *bf16opt_error_string(int code);

@@ -65,13 +65,16 @@ class bf16opt_norm_result_t(ctypes.Structure):
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
-           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_skip_nonfinite")
+           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_skip_nonfinite",
+           "bf16opt_debug_faults")
 
 _lib = None
 
 
 def lib_path():
-    return _build.LIB_PATH
+    """The library to load: $BF16OPT_LIBRARY if set (e.g. a checked build of the
+    same sources), else the in-tree libbf16opt.so."""
+    return os.environ.get("BF16OPT_LIBRARY") or _build.LIB_PATH
 
 
 def load(path=None):
@@ -79,7 +82,7 @@ def load(path=None):
     global _lib
     if _lib is not None and path is None:
         return _lib
-    path = path or _build.LIB_PATH
+    path = path or lib_path()
     if not os.path.exists(path):
         raise RuntimeError(f"libbf16opt.so is not built ({path}); run __graft_entry__.build() -- "
                            "there is no fallback implementation")
@@ -109,6 +112,8 @@ def load(path=None):
     L.bf16opt_set_global_sumsq.argtypes = [hp, ctypes.c_double, c_vp]
     L.bf16opt_set_skip_nonfinite.restype = ctypes.c_int
     L.bf16opt_set_skip_nonfinite.argtypes = [hp, ctypes.c_int]
+    L.bf16opt_debug_faults.restype = ctypes.c_int
+    L.bf16opt_debug_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.bf16opt_lr_factor.restype = ctypes.c_int
     L.bf16opt_lr_factor.argtypes = [ctypes.POINTER(bf16opt_lr_schedule_t), ctypes.c_int64,
                                     ctypes.POINTER(ctypes.c_double)]
@@ -116,7 +121,7 @@ def load(path=None):
     L.bf16opt_set_lr_schedule.argtypes = [hp, ctypes.POINTER(bf16opt_lr_schedule_t)]
     L.bf16opt_grad_norm_static.restype = ctypes.c_int
     L.bf16opt_grad_norm_static.argtypes = [c_vp, c_u64, c_f32, c_f32, c_vp, c_vp]
-    if path == _build.LIB_PATH:
+    if path == lib_path():
         _lib = L
     return L
 
@@ -203,6 +208,13 @@ def bf16opt_grad_norm_static(grad_accum, n, grad_scale, max_grad_norm, out, stre
 
 def bf16opt_error_string(code):
     return load().bf16opt_error_string(code).decode()
+
+
+def bf16opt_debug_faults():
+    """(status, fault bits) of a checked build; release builds give UNSUPPORTED."""
+    bits = ctypes.c_uint32(0)
+    rc = load().bf16opt_debug_faults(ctypes.byref(bits))
+    return rc, bits.value
 
 
 def bf16opt_last_error(h=None):

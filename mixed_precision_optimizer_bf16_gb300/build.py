@@ -24,8 +24,15 @@ def _stale(out, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_cmd(extra=()):
-    return [nvcc()] + NVCC_FLAGS + list(extra) + ["-I", os.path.join(ROOT, "include"), "-o", LIB_PATH] + SOURCES
+def build_cmd(extra=(), out=None):
+    return [nvcc()] + NVCC_FLAGS + list(extra) + ["-I", os.path.join(ROOT, "include"), "-o", out or LIB_PATH] + SOURCES
+
+
+def build_checked(out):
+    """Compile the checked variant (-DBF16K_CHECKS: kernels test chunk ranges
+    and vector alignment and record violations instead of accessing) to `out`."""
+    subprocess.run(build_cmd(["-DBF16K_CHECKS=1"], out), check=True)
+    return out
 
 
 def build(force=False, extra=()):

@@ -14,6 +14,8 @@
 #include <type_traits>
 #include <utility>
 #include <vector>
+#include <mutex>
+#include <unordered_set>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -27,6 +29,11 @@ namespace {
 enum State { S_IDLE = 0, S_ACC, S_ACC_DONE, S_ACC_DEFERRED, S_LOCAL_NORMED, S_NORMED };
 
 thread_local std::string g_create_error;
+
+// Live handles: every entry point rejects a pointer that bf16opt_create did not
+// return or that bf16opt_destroy already freed, instead of dereferencing it.
+std::mutex g_live_mu;
+std::unordered_set<const void *> g_live;
 
 }  // namespace
 
@@ -64,6 +71,12 @@ struct bf16opt {
 };
 
 namespace {
+
+bool live(const bf16opt_t *h) {
+    if (!h) return false;
+    std::lock_guard<std::mutex> lock(g_live_mu);
+    return g_live.count(h) != 0;
+}
 
 int fail(bf16opt_t *h, int code, const std::string &msg) {
     if (h) h->last_error = msg;
@@ -339,7 +352,8 @@ const char *bf16opt_error_string(int code) {
 }
 
 const char *bf16opt_last_error(const bf16opt_t *h) {
-    return h ? h->last_error.c_str() : g_create_error.c_str();
+    if (!h) return g_create_error.c_str();
+    return live(h) ? h->last_error.c_str() : "not a live bf16opt handle (never created, or destroyed)";
 }
 
 int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
@@ -511,6 +525,10 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
         delete h;
         return fail(nullptr, BF16OPT_ERR_CUDA, std::string("table upload: ") + cudaGetErrorString(e));
     }
+    {
+        std::lock_guard<std::mutex> lock(g_live_mu);
+        g_live.insert(h);
+    }
     g_create_error.clear();
     *out = h;
     return BF16OPT_OK;
@@ -519,15 +537,28 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
 int bf16opt_destroy(bf16opt_t *h) {
     NvtxRange nvtx("bf16opt_destroy");
     if (!h) return BF16OPT_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_live_mu);
+        if (g_live.erase(h) == 0) return BF16OPT_ERR_INVALID_ARG;   // never created, or destroyed twice
+    }
     DeviceGuard dg(h->device);
     cudaDeviceSynchronize();
     free_scratch(h);
-    delete h;
+    // Everything the handle owns is released, but the small struct itself is
+    // kept (a tombstone): were its address handed out again by a later create,
+    // a stale copy of this handle would pass the registry check.
+    std::vector<Seg>().swap(h->segs);
+    std::vector<const uint16_t *>().swap(h->pend_flat);
+    std::vector<std::vector<const uint16_t *>>().swap(h->pend_list);
+    std::vector<uint32_t>().swap(h->slot_chunk0);
+    std::vector<std::pair<const void *, int>>().swap(h->occ);
+    std::vector<bf16opt_group_t>().swap(h->groups);
+    std::string().swap(h->last_error);
     return BF16OPT_OK;
 }
 
 int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
-    if (!h || !t) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h) || !t) return BF16OPT_ERR_INVALID_ARG;
     DeviceGuard dg(h->device);
     int64_t v = 0;
     if (quiesce() != cudaSuccess || cudaMemcpy(&v, &h->step_d->t, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
@@ -540,7 +571,7 @@ int bf16opt_get_step(const bf16opt_t *h, int64_t *t) {
 
 int bf16opt_set_step(bf16opt_t *h, int64_t t) {
     NvtxRange nvtx("bf16opt_set_step");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (t < 0) return fail(h, BF16OPT_ERR_INVALID_ARG, "step must be >= 0");
     DeviceGuard dg(h->device);
     cudaError_t e = quiesce();
@@ -553,7 +584,7 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t) {
 int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list, unsigned flags,
                        void *stream) {
     NvtxRange nvtx("bf16opt_accumulate");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     const bool first = flags & BF16OPT_FIRST, last = flags & BF16OPT_LAST, defer = flags & BF16OPT_DEFER;
     if (flags & ~(BF16OPT_FIRST | BF16OPT_LAST | BF16OPT_DEFER)) return fail(h, BF16OPT_ERR_INVALID_ARG, "unknown flag");
     if (!first && h->state != S_ACC) return fail(h, BF16OPT_ERR_SEQUENCE, "accumulate without FIRST outside an accumulation");
@@ -622,7 +653,7 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
 
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
     NvtxRange nvtx("bf16opt_grad_norm");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
         return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm needs a completed accumulation");
     DeviceGuard dg(h->device);
@@ -654,7 +685,7 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
 
 int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
     NvtxRange nvtx("bf16opt_grad_norm_local");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (!local_sumsq) return fail(h, BF16OPT_ERR_INVALID_ARG, "grad_norm_local: local_sumsq is NULL");
     if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
         return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm_local needs a completed accumulation");
@@ -673,7 +704,7 @@ int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
 
 int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
     NvtxRange nvtx("bf16opt_set_global_sumsq");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_global_sumsq needs grad_norm_local first");
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
@@ -708,7 +739,7 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
 
 int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
     NvtxRange nvtx("bf16opt_set_skip_nonfinite");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     DeviceGuard dg(h->device);
     cudaError_t e = quiesce();
     if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
@@ -720,7 +751,7 @@ int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
 
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
     NvtxRange nvtx("bf16opt_set_lr_schedule");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     double f = 0.0;
     if (s && bf16opt_lr_factor(s, 1, &f) != BF16OPT_OK)
         return fail(h, BF16OPT_ERR_INVALID_ARG, "lr schedule: need 0 <= warmup_steps <= decay_steps, min_lr_ratio in [0, 1]");
@@ -736,7 +767,7 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
 
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     NvtxRange nvtx("bf16opt_step");
-    if (!h) return BF16OPT_ERR_INVALID_ARG;
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (h->state != S_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "step needs grad_norm first");
     LrOverride ov;
     memset(&ov, 0, sizeof ov);
@@ -833,6 +864,9 @@ k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, u
         if (head > len) head = len;
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
+        if (check_fails(end > n, kFaultChunkRange) || check_fails(tail0 > len, kFaultBody) ||
+            check_fails(nq != 0 && mis16(a + head), kFaultAlign))
+            continue;
         Comp cs = {0.f, 0.f};
         const uint32_t rh = scalar_lane<kThreads>(c, 0), rt = scalar_lane<kThreads>(c, 1);
         for (uint32_t i = rh; i < head; i += kThreads) comp_add_sq(cs, __fmul_rn(a[i], gscale));
@@ -929,4 +963,23 @@ extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, flo
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "grad_norm_static kernel launch");
     return BF16OPT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Fault word of the checked build (see kernels.cuh).
+// ---------------------------------------------------------------------------
+extern "C" int bf16opt_debug_faults(uint32_t *bits) {
+    if (!bits) return BF16OPT_ERR_INVALID_ARG;
+    *bits = 0;
+#ifdef BF16K_CHECKS
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_check_faults, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_check_faults, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "reading the fault word");
+    *bits = v;
+    return BF16OPT_OK;
+#else
+    return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "not a checked build (compile with -DBF16K_CHECKS)");
+#endif
 }

@@ -145,6 +145,33 @@ struct ListGrads {
     __device__ __forceinline__ const uint16_t *get(uint32_t s, int j) const { return ptr[j * nslots + (s - slot_base)]; }
 };
 
+// ------------------------------------------------------------ checked build
+// Built with -DBF16K_CHECKS, the kernels also test what the host guarantees by
+// construction -- every chunk lies inside its segment, the scalar head and the
+// vector body stay inside the chunk, every vector pointer is 16-byte (FP32) /
+// 8-byte (bf16) aligned -- and on a violation set a bit in g_check_faults and
+// skip the chunk instead of making the access (no trap, no fault).  The tests
+// are uniform across a CTA, so a skipped chunk never splits a barrier.
+// Release builds compile them away.
+enum : uint32_t { kFaultChunkRange = 1u, kFaultBody = 2u, kFaultAlign = 4u };
+#ifdef BF16K_CHECKS
+__device__ uint32_t g_check_faults;
+#endif
+__device__ __forceinline__ bool check_fails(bool bad, uint32_t bit) {
+#ifdef BF16K_CHECKS
+    if (bad) {
+        atomicOr(&g_check_faults, bit);
+        return true;
+    }
+#else
+    (void)bad;
+    (void)bit;
+#endif
+    return false;
+}
+__device__ __forceinline__ bool mis16(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+__device__ __forceinline__ bool mis8(const void *p) { return ((uintptr_t)p & 7u) != 0; }
+
 // ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -334,6 +361,15 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
         const uint32_t head = chunk_head<KMAX>(a, HAS_ACC || WRITE, g, K, len);
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
+        if (check_fails(ch.start + len > s.numel, kFaultChunkRange) || check_fails(tail0 > len, kFaultBody))
+            continue;
+        if (nq != 0) {
+            bool bad = (HAS_ACC || WRITE) && mis16(a + head);
+#pragma unroll
+            for (int j = 0; j < KA; ++j)
+                if (j < K) bad = bad || mis8(g[j] + head);
+            if (check_fails(bad, kFaultAlign)) continue;
+        }
 
         Comp cs = {0.f, 0.f};
         auto scalar = [&](uint32_t i) {
@@ -538,6 +574,16 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             head = len;
         const uint32_t nq = (len - head) >> 2;
         const uint32_t tail0 = head + (nq << 2);
+        if (check_fails(ch.start + len > s.numel, kFaultChunkRange) || check_fails(tail0 > len, kFaultBody))
+            continue;
+        if (nq != 0) {
+            bool bad = mis16(p + head) || mis16(m + head) || mis16(v + head) || mis8(bf + head) ||
+                       (HAS_ACC && mis16(a + head));
+#pragma unroll
+            for (int j = 0; j < KA; ++j)
+                if (j < K) bad = bad || mis8(g[j] + head);
+            if (check_fails(bad, kFaultAlign)) continue;
+        }
 
         auto scalar = [&](uint32_t i) {
             const float e = __fmul_rn(fold_scalar<HAS_ACC, KMAX>(a, g, K, i), gscale);

@@ -19,3 +19,16 @@ def pytest_configure(config):
 def pytest_collection_modifyitems(config, items):
     # Keep the no-allocation entry-point file last even if names change.
     items.sort(key=lambda it: 1 if os.path.basename(str(it.fspath)).startswith("test_zz_") else 0)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # Under a checked build of the library (BF16OPT_CHECK_FAULTS set, the build
+    # named by BF16OPT_LIBRARY), any bounds or alignment violation the kernels
+    # recorded during the session fails it.
+    if not os.environ.get("BF16OPT_CHECK_FAULTS"):
+        return
+    from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
+    rc, bits = C.bf16opt_debug_faults()
+    print(f"\nchecked build: status {rc}, fault bits {bits:#x}")
+    if rc != 0 or bits != 0:
+        session.exitstatus = 1

@@ -159,3 +159,22 @@ def test_python_binding_refuses_host_tensors():
     groups = [dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)]
     with pytest.raises(ValueError, match="CUDA tensor"):
         BF16Optimizer(groups, flat=flat)
+
+
+def test_unknown_handles_are_rejected_without_dereference(lib):
+    """A pointer bf16opt_create never returned is refused by every handle call
+    (the library checks a registry of live handles before touching it)."""
+    fake = ctypes.c_void_p(0x10)          # never a handle; dereferencing it would crash
+    E = C.BF16OPT_ERR_INVALID_ARG
+    g = ctypes.c_void_p(0x1000)
+    assert C.bf16opt_accumulate(fake, g.value, None, C.BF16OPT_FIRST) == E
+    assert C.bf16opt_grad_norm(fake, 0, True)[0] == E
+    assert C.bf16opt_grad_norm_local(fake)[0] == E
+    assert C.bf16opt_set_global_sumsq(fake, 1.0) == E
+    assert C.bf16opt_step(fake) == E
+    assert C.bf16opt_get_step(fake)[0] == E
+    assert C.bf16opt_set_step(fake, 3) == E
+    assert C.bf16opt_set_skip_nonfinite(fake, True) == E
+    assert C.bf16opt_set_lr_schedule(fake, C.lr_schedule(10, 100, 0.1)) == E
+    assert C.bf16opt_destroy(fake) == E
+    assert "not a live" in C.bf16opt_last_error(fake)

@@ -829,3 +829,23 @@ def test_random_sequences_match_oracle(seed):
     oracle (norms, m, v, master, bf16) over two steps."""
     wl, pattern, gscale = _random_case(seed)
     dense_parity(wl, defer=pattern, grad_scale=gscale)
+
+
+@needs_cuda
+def test_destroyed_handle_is_rejected():
+    """After bf16opt_destroy the handle value is refused by every call, and a
+    second destroy is an error, not a double free."""
+    flat, h = _raw_flat(1000)
+    g = torch.zeros(1000, dtype=torch.int16, device="cuda")
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST | C.BF16OPT_LAST) == 0
+    assert C.bf16opt_destroy(h) == 0
+    E = C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_grad_norm(h, 0, True)[0] == E
+    assert C.bf16opt_step(h) == E
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST) == E
+    assert C.bf16opt_get_step(h)[0] == E
+    assert C.bf16opt_destroy(h) == E
+    assert "not a live" in C.bf16opt_last_error(h)
+    flat2, h2 = _raw_flat(1000)                  # a new handle works normally
+    assert C.bf16opt_accumulate(h2, g.data_ptr(), None, C.BF16OPT_FIRST | C.BF16OPT_LAST) == 0
+    assert C.bf16opt_destroy(h2) == 0
