@@ -179,6 +179,10 @@ class BF16Optimizer:
                    _ptr(t["param_bf16"]), t["master"].numel(), int(t.get("group", 0))) for t in tensors]
             self.desc = C.list_desc(tl, self.groups, max_grad_norm, grad_scale)
             self.mode = C.BF16OPT_LIST
+        # the library holds raw pointers: keep the tensors alive with the handle
+        self._state = [flat] if flat is not None else list(tensors)
+        self._sched_args = None
+        self._skip = False
         rc, self.h = C.bf16opt_create(self.desc)
         C.check(rc, None)
 
@@ -216,12 +220,52 @@ class BF16Optimizer:
 
     def set_skip_nonfinite(self, enable=True):
         """Skip (on the device) any step whose global norm is Inf or NaN."""
-        return C.check(C.bf16opt_set_skip_nonfinite(self.h, enable), self.h)
+        rc = C.check(C.bf16opt_set_skip_nonfinite(self.h, enable), self.h)
+        self._skip = bool(enable)
+        return rc
 
     def set_lr_schedule(self, warmup_steps, decay_steps, min_lr_ratio):
         """Attach the warmup + cosine schedule (None detaches); see bf16opt_set_lr_schedule."""
         self._sched = None if warmup_steps is None else C.lr_schedule(warmup_steps, decay_steps, min_lr_ratio)
-        return C.check(C.bf16opt_set_lr_schedule(self.h, self._sched), self.h)
+        rc = C.check(C.bf16opt_set_lr_schedule(self.h, self._sched), self.h)
+        self._sched_args = None if warmup_steps is None else (int(warmup_steps), int(decay_steps), float(min_lr_ratio))
+        return rc
+
+    _CKPT_KEYS = ("master", "exp_avg", "exp_avg_sq", "param_bf16")
+
+    def state_dict(self):
+        """Checkpoint: the step counter, the settings and host copies of every
+        tensor's FP32 master, moments and bf16 parameters (the accumulator carries
+        nothing between steps).  Waits for the device (the step counter read does)."""
+        t = self.t
+        return {"t": t, "groups": [dict(g) for g in self.groups], "lr_schedule": self._sched_args,
+                "skip_nonfinite": self._skip,
+                "tensors": [{k: d[k].detach().to("cpu", copy=True) for k in self._CKPT_KEYS} for d in self._state]}
+
+    def load_state_dict(self, sd):
+        """Restore a state_dict() into this optimizer's buffers (same layout:
+        tensor count, sizes and dtypes) and continue from its step.  Continuing
+        is bit-identical to an uninterrupted run when every buffer has the same
+        offset modulo 128 bytes as when the checkpoint was taken (that offset
+        fixes the chunking of the norm's partial sums)."""
+        if len(sd["tensors"]) != len(self._state):
+            raise ValueError(f"checkpoint has {len(sd['tensors'])} tensors, this optimizer {len(self._state)}")
+        if [dict(g) for g in sd["groups"]] != self.groups:
+            raise ValueError("checkpoint groups differ from this optimizer's")
+        for i, (src, dst) in enumerate(zip(sd["tensors"], self._state)):
+            for k in self._CKPT_KEYS:
+                if src[k].shape != dst[k].shape or src[k].element_size() != dst[k].element_size():
+                    raise ValueError(f"tensors[{i}][{k!r}]: checkpoint {tuple(src[k].shape)}/{src[k].dtype}, "
+                                     f"buffer {tuple(dst[k].shape)}/{dst[k].dtype}")
+        torch.cuda.synchronize()
+        for src, dst in zip(sd["tensors"], self._state):
+            for k in self._CKPT_KEYS:
+                dst[k].copy_(src[k].view(dst[k].dtype))
+        torch.cuda.synchronize()
+        if sd.get("lr_schedule") is not None:
+            self.set_lr_schedule(*sd["lr_schedule"])
+        self.set_skip_nonfinite(bool(sd.get("skip_nonfinite", False)))
+        self.t = int(sd["t"])
 
     def step(self, lr=None, stream=None):
         """lr: None (the groups' rates), one rate for every group, or one per group."""
@@ -244,6 +288,7 @@ class BF16Optimizer:
         if getattr(self, "h", None) is not None and self.h.value:
             C.bf16opt_destroy(self.h)
             self.h = None
+        self._state = []
 
     def __del__(self):
         try:

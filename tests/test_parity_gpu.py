@@ -849,3 +849,47 @@ def test_destroyed_handle_is_rejected():
     flat2, h2 = _raw_flat(1000)                  # a new handle works normally
     assert C.bf16opt_accumulate(h2, g.data_ptr(), None, C.BF16OPT_FIRST | C.BF16OPT_LAST) == 0
     assert C.bf16opt_destroy(h2) == 0
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_state_dict_file_round_trip(tmp_path, mode):
+    """Checkpoint through the Python API and a file: two steps with an LR
+    schedule and skipping enabled, state_dict() saved with torch.save, every
+    buffer freed, a fresh optimizer over new buffers (same offset modulo 128
+    bytes) loads it and takes the third step -- equal, bit for bit, to three
+    uninterrupted steps."""
+    wl = workloads.custom(294, [30_001, 7, 16_385], decay=[True, False, True], gas=2, steps=3, grad_sigma=0.2,
+                          misalign=3, mode=mode)
+
+    def configure(opt):
+        opt.set_lr_schedule(1, 10, 0.1)
+        opt.set_skip_nonfinite(True)
+
+    ref = GpuShard(wl, defer=True)
+    configure(ref.opt)
+    ref.run(3)
+    want = ref.states()
+    ref.close()
+    del ref
+
+    sh = GpuShard(wl, defer=True)
+    configure(sh.opt)
+    sh.run_step(0)
+    sh.run_step(1)
+    path = tmp_path / "opt.pt"
+    torch.save(sh.opt.state_dict(), path)
+    sh.close()
+    del sh
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    sh2 = GpuShard(wl, defer=True)             # fresh buffers, fresh handle, default settings
+    sd = torch.load(path, weights_only=True)      # plain tensors, numbers and lists
+    sh2.opt.load_state_dict(sd)
+    assert sh2.opt.t == 2
+    sh2.run_step(2)
+    got = sh2.states()
+    sh2.close()
+    for k in ("p", "m", "v", "p_bf16"):
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
