@@ -7,6 +7,7 @@ arithmetic is in libbf16opt.so.  State layout for one rank's shard:
         as five contiguous buffers of n elements, plus group ranges;
   LIST: the same five buffers per tensor (separate allocations).
 """
+import contextlib
 import ctypes
 import mmap
 
@@ -186,8 +187,69 @@ class BF16Optimizer:
         rc, self.h = C.bf16opt_create(self.desc)
         C.check(rc, None)
 
-    def accumulate(self, grad, first=False, last=False, defer=False, stream=None):
-        """grad: bf16 (int16-viewed) tensor (FLAT) or list of them (LIST)."""
+    @classmethod
+    def from_parameters(cls, param_groups, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.0,
+                        max_grad_norm=1.0, grad_scale=1.0):
+        """One FLAT shard over a model's bf16 parameters.
+
+        param_groups: an iterable of parameters, or torch.optim-style dicts
+        {"params": [...], optional "lr", "betas", "eps", "weight_decay"}.  Every
+        parameter must be a bf16 CUDA tensor.  The parameters are laid out one
+        after another, group by group (one range per group); the FP32 masters
+        start as the parameters' values; afterwards each parameter's .data is a
+        view into the flat bf16 parameter buffer (the step writes it in place)
+        and its .grad a view into the flat bf16 gradient buffer `grad_buffer`,
+        which backward adds into: call zero_grad() before each micro-batch's
+        backward and accumulate() (no gradient argument) after it.
+        """
+        groups = list(param_groups)
+        if groups and isinstance(groups[0], torch.Tensor):
+            groups = [{"params": groups}]
+        seen, layout, hyper, ranges, n = set(), [], [], [], 0
+        for gi, g in enumerate(groups):
+            b1, b2 = g.get("betas", betas)
+            hyper.append(dict(lr=float(g.get("lr", lr)), beta1=float(b1), beta2=float(b2), eps=float(g.get("eps", eps)),
+                              weight_decay=float(g.get("weight_decay", weight_decay))))
+            begin = n
+            for p in g["params"]:
+                if id(p) in seen:
+                    raise ValueError("a parameter appears twice")
+                if not (isinstance(p, torch.Tensor) and p.is_cuda and p.dtype == torch.bfloat16):
+                    raise ValueError("every parameter must be a bf16 CUDA tensor")
+                seen.add(id(p))
+                layout.append((p, n))
+                n += p.numel()
+            ranges.append((begin, n, gi))
+        dev = layout[0][0].device if layout else torch.device("cuda")
+        flat = {k: torch.zeros(n, dtype=torch.float32, device=dev)
+                for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum")}
+        flat["param_bf16"] = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        grads = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        with torch.no_grad():
+            for p, off in layout:
+                k = p.numel()
+                flat["param_bf16"][off:off + k].copy_(p.reshape(-1))
+                flat["master"][off:off + k].copy_(p.reshape(-1).float())
+                p.data = flat["param_bf16"][off:off + k].view(p.shape)
+                p.grad = grads[off:off + k].view(p.shape)
+        opt = cls(hyper, flat=flat, ranges=ranges, max_grad_norm=max_grad_norm, grad_scale=grad_scale)
+        opt.grad_buffer = grads
+        opt.flat = flat
+        opt.ranges = ranges
+        return opt
+
+    def zero_grad(self, stream=None):
+        """Zero the flat gradient buffer of a from_parameters() optimizer."""
+        with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+            self.grad_buffer.zero_()
+
+    def accumulate(self, grad=None, first=False, last=False, defer=False, stream=None):
+        """grad: bf16 (or int16-viewed) tensor (FLAT) or list of them (LIST);
+        None = the flat gradient buffer of a from_parameters() optimizer."""
+        if grad is None:
+            grad = getattr(self, "grad_buffer", None)
+            if grad is None:
+                raise ValueError("no gradient given and no gradient buffer (see from_parameters)")
         flags = (C.BF16OPT_FIRST if first else 0) | (C.BF16OPT_LAST if last else 0) | (C.BF16OPT_DEFER if defer else 0)
         if self.mode == C.BF16OPT_FLAT:
             if self.n:
