@@ -107,7 +107,10 @@ static float orc_effective(float acc, float grad_scale) {
 
 /* ------------------------------------------------------------------- norm */
 
-/* Fixed summation order: sequential FP64 sums over chunks of ORC_CHUNK
+/* The squared global L2 norm of the accumulated gradient over every element
+ * of every parameter group ("企业官网建设流程全解析" (cf-1.com), section 4.3:
+ * clipping by the global gradient norm).
+ * Fixed summation order: sequential FP64 sums over chunks of ORC_CHUNK
  * elements, then a sequential FP64 sum of the chunk sums in index order.
  * Squares of FP32 values are exact in FP64.  The result does not depend on
  * the thread count. */
@@ -158,7 +161,9 @@ double orc_clip_coef(double sumsq, double max_norm) {
 
 /* ------------------------------------------------------------------ AdamW */
 
-/* One element of one AdamW step (Kingma & Ba Algorithm 1 with decoupled,
+/* "企业官网建设流程全解析", section 1: FP32 master weights, momentum and variance
+ * next to the 16-bit parameters; section 3.3: AdamW (lr 6e-5, weight decay 0.01).
+ * One element of one AdamW step (Kingma & Ba Algorithm 1 with decoupled,
  * lr-scaled weight decay, Loshchilov & Hutter), FP64 throughout, from the
  * FP32-stored m, v and master; the results are stored as FP32 and the bf16
  * parameter is cast from the stored FP32 master.
@@ -280,7 +285,9 @@ void orc_sample_run(const orc_stream_t *s, const uint64_t *idx, uint64_t k, cons
 
 /* ------------------------------------------------------------- LR schedule */
 
-/* Warmup: lr grows linearly and reaches lr at step `warmup`.  Decay: the
+/* "单机多卡实战：Megatron-DeepSpeed训练类BLOOM模型全流程解析", section 3: lr 6e-5,
+ * min_lr 1e-6, lr_decay_style cosine, warmup_iters 500.
+ * Warmup: lr grows linearly and reaches lr at step `warmup`.  Decay: the
  * cosine half-wave from lr (just after warmup) to min_lr (at step `decay`):
  * lr_t = min_lr + (lr - min_lr) (1 + cos(pi s)) / 2, s = (t - warmup)/(decay - warmup). */
 double orc_lr_at(double lr, double min_lr, int64_t warmup, int64_t decay, int64_t t) {
