@@ -40,6 +40,14 @@ MUTANTS = {
     "lr_warmup_off_by_one": ("return lr * (double)t / (double)warmup;", "return lr * (double)(t - 1) / (double)warmup;"),
     "lr_cosine_sign": ("(1.0 + cos(3.14159265358979323846 * s))", "(1.0 - cos(3.14159265358979323846 * s))"),
     "lr_no_min_floor": ("return min_lr + (lr - min_lr) * (1.0 + cos", "return lr * (1.0 + cos"),
+    "betas_swapped_in_bias_correction": ("*bc1 = 1.0 - pow(G->beta1, (double)t);",
+                                         "*bc1 = 1.0 - pow(G->beta2, (double)t);"),
+    "bias_correction_t_plus_1": ("pow(G->beta1, (double)t)", "pow(G->beta1, (double)(t + 1))"),
+    "first_moment_unclipped": ("(1.0 - G->beta1) * gc;", "(1.0 - G->beta1) * (double)e;"),
+    "second_moment_unclipped": ("(1.0 - G->beta2) * gc * gc", "(1.0 - G->beta2) * (double)e * e"),
+    "grad_scale_ignored_in_update": ("orc_effective(k->acc[i], k->gs), k->c,", "k->acc[i], k->c,"),
+    "later_micro_batches_overwrite": ("return (float)((double)a + gd);", "return (float)gd;"),
+    "eps_scaled_by_bias_correction": ("(sqrt(vhat) + G->eps)", "(sqrt(vhat) + G->eps / sqrt(bc2))"),
 }
 
 import test_lr_schedule as lr_pins  # noqa: E402
