@@ -893,3 +893,27 @@ def test_state_dict_file_round_trip(tmp_path, mode):
     sh2.close()
     for k in ("p", "m", "v", "p_bf16"):
         assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+
+
+SWEEP_SIZES = [1, 2, 3, 4, 5, 7, 8, 31, 32, 33, 63, 64, 65, 2047, 2048, 2049, 4095, 4096, 4097]
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_small_sizes_every_misalignment(mode):
+    """Every buffer offset 0..7 elements for sizes around the quad, warp and
+    128-byte boundaries (1 ... 4097 elements; LIST adds a second, 5-element
+    tensor), GAS cycling 1, 2, 3 and the last micro-batch deferred on every
+    other case: 152 dense runs, each equal to the oracle over two steps."""
+    case = 0
+    for n in SWEEP_SIZES:
+        for mis in range(8):
+            gas = 1 + case % 3
+            sizes = [n] if mode == "flat" else [n, 5]
+            wl = workloads.custom(600 + case, sizes, decay=[True, False][:len(sizes)], gas=gas, steps=2,
+                                  grad_sigma=0.3, misalign=mis, mode=mode)
+            try:
+                dense_parity(wl, defer=bool(case % 2))
+            except AssertionError as e:
+                raise AssertionError(f"n={n} misalign={mis} gas={gas} defer={bool(case % 2)}: {e}") from None
+            case += 1
