@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-variant", action="store_true", help="skip the all-deferred variant timing")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time of the CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time of the CPU baseline")
     return ap.parse_args()
 
 
@@ -380,7 +380,7 @@ def run_ours(args):
         return
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_oracle(wl, args.cpu_seconds, steps=1)
+        cpu = cpu_oracle(wl, args.cpu_seconds, steps=None)
     traffic = profiled_traffic() if (args.workload == 2 and not args.elements) else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -493,7 +493,9 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
 def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
     """The CPU oracle, as it stands, on a bounded contiguous sample of the
     workload: `steps` whole optimizer steps (GAS accumulates, norm, clip,
-    AdamW per group) over S elements, S sized from a pilot to about `seconds`."""
+    AdamW per group) over S elements, S sized from a pilot to about `seconds`
+    (at most 2^28 elements).  steps=None: as many whole steps over the largest
+    sample as fill about `seconds` (1 to 100)."""
     import numpy as np
 
     import oracle
@@ -514,8 +516,9 @@ def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
 
     def make(S):
         p = synth.fill_master(wl, np.empty(S, np.float32), off0)
+        sets = 2 if auto else min(2, max(1, steps + warmup))   # timed steps alternate between them
         gr = [[synth.fill_grad(wl, s, k, np.empty(S, np.uint16), off0) for k in range(wl.gas)]
-              for s in range(min(2, max(1, steps + warmup)))]
+              for s in range(sets)]
         return p, gr
 
     def timed(S, p, gr, nsteps, t0=0):
@@ -537,12 +540,15 @@ def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
         return time.perf_counter() - t
 
     S0 = 1 << 22
+    auto = steps is None
     p, gr = make(S0)
     dt0 = timed(S0, p, gr, 1)
     per_elem = dt0 / S0
-    S = int(min(max(seconds / max(steps, 1) / per_elem, S0), 1 << 28, wl.n - off0))
+    S = int(min(max(seconds / (1 if auto else max(steps, 1)) / per_elem, S0), 1 << 28, wl.n - off0))
     S -= S % 4096
     p, gr = make(S)
+    if auto:   # one untimed step at the full sample size sets the step count
+        steps = int(min(100, max(1, round(seconds / timed(S, p, gr, 1)))))
     if warmup:
         timed(S, p.copy(), gr, warmup)
     dt = timed(S, p, gr, steps)
