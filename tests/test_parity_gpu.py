@@ -917,3 +917,46 @@ def test_small_sizes_every_misalignment(mode):
             except AssertionError as e:
                 raise AssertionError(f"n={n} misalign={mis} gas={gas} defer={bool(case % 2)}: {e}") from None
             case += 1
+
+
+def _tiny_gradient_workload():
+    """Gradients of magnitude 1e-25 ... 1e-18 (random sign, log-uniform), so
+    that (1 - b2) g^2 spans FP32's subnormal range and underflow to zero while
+    m stays normal; the norm is far below 1, so nothing is clipped."""
+    wl = workloads.custom(295, [40_001, 99], decay=[True, False], gas=2, steps=3, grad_sigma=0.1, misalign=1)
+    rng = np.random.default_rng(295)
+    grads = []
+    for _ in range(wl.steps * wl.gas):
+        mag = 10.0 ** rng.uniform(-25, -18, wl.n)
+        x = (mag * rng.choice([-1.0, 1.0], wl.n)).astype(np.float32)
+        grads.append((x.view(np.uint32) >> 16).astype(np.uint16))       # bf16 by truncation
+    return wl, grads
+
+
+@needs_cuda
+def test_gradients_with_subnormal_second_moments():
+    import harness
+    wl, grads = _tiny_gradient_workload()
+    sh = GpuShard(wl, defer=True)
+    for s in range(wl.steps):
+        for k in range(wl.gas):
+            sh.gbuf.copy_(torch.from_numpy(grads[s * wl.gas + k].view(np.int16)))
+            sh.opt.accumulate(sh.grads_arg(), first=k == 0, last=k == wl.gas - 1, defer=k == wl.gas - 1)
+        sh.opt.grad_norm(sync=True)
+        sh.opt.step()
+    torch.cuda.synchronize()
+    got = sh.states()
+    sh.close()
+
+    p0 = synth.fill_master(wl, np.empty(wl.n, np.float32))
+    p, m, v = p0.copy(), np.zeros(wl.n, np.float32), np.zeros(wl.n, np.float32)
+    sc = {"M": np.zeros(wl.n), "A": np.abs(p0.astype(np.float64))}
+    gof = wl.group_of(np.arange(wl.n))
+    for s in range(wl.steps):
+        ref = oracle.run_dense(p, lambda st, k: grads[s * wl.gas + k], wl.ranges(), ogroups(wl), 1, wl.gas,
+                               wl.max_norm, t0=s, m=m, v=v)
+        p, m, v = ref["p"], ref["m"], ref["v"]
+        harness._update_scales(sc, wl, gof, ref["acc"], ref["clip"][0], m, v, s + 1, 1.0)
+    tiny = np.finfo(np.float32).tiny
+    assert np.count_nonzero((ref["v"] > 0) & (ref["v"] < tiny)) > 1000          # the case really is subnormal
+    compare(got, ref, sc, wl, check_acc=False)
