@@ -28,6 +28,7 @@ class Tensor:
     numel: int
     decay: bool
     init: tuple  # ("normal", sigma) | ("const", value) | ("loguniform", e_lo, e_hi)
+    group: int = -1  # parameter group; -1: 0 if it decays, else 1
 
 
 @dataclass
@@ -52,15 +53,16 @@ class Workload:
         self._ends = np.array([o + t.numel for o, t in zip(self.offsets, self.tensors)], dtype=np.int64)
 
     def group_of_tensor(self, i):
-        return 0 if self.tensors[i].decay else 1
+        t = self.tensors[i]
+        return t.group if t.group >= 0 else (0 if t.decay else 1)
 
     def tensor_of(self, idx):
         """Tensor index of each global element index."""
         return np.searchsorted(self._ends, np.asarray(idx, dtype=np.int64), side="right")
 
     def group_of(self, idx):
-        dec = np.array([t.decay for t in self.tensors])
-        return np.where(dec[self.tensor_of(idx)], 0, 1).astype(np.uint32)
+        grp = np.array([self.group_of_tensor(i) for i in range(len(self.tensors))], dtype=np.uint32)
+        return grp[self.tensor_of(idx)]
 
     def ranges(self):
         """Flat-mode group ranges [begin, end, group], neighbours of one group merged."""

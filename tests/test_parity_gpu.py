@@ -960,3 +960,48 @@ def test_gradients_with_subnormal_second_moments():
     tiny = np.finfo(np.float32).tiny
     assert np.count_nonzero((ref["v"] > 0) & (ref["v"] < tiny)) > 1000          # the case really is subnormal
     compare(got, ref, sc, wl, check_acc=False)
+
+
+def _group(lr=6e-5, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.01):
+    return dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
+
+
+HYPER_EDGES = {
+    # name: (groups for [decay, no-decay], max_norm, grad_scale)
+    "clipping_off": ([_group(), _group(weight_decay=0.0)], 0.0, 1.0),
+    "lr_zero": ([_group(lr=0.0), _group(lr=0.0, weight_decay=0.0)], 1.0, 1.0),
+    "betas_zero": ([_group(beta1=0.0, beta2=0.0), _group(beta1=0.0, beta2=0.0, weight_decay=0.0)], 1.0, 1.0),
+    "strong_decay": ([_group(lr=0.5, weight_decay=1.0), _group(lr=0.5, weight_decay=0.0)], 1.0, 1.0),
+    "eps_one": ([_group(eps=1.0), _group(eps=1.0, weight_decay=0.0)], 1.0, 1.0),
+    "negative_grad_scale": ([_group(), _group(weight_decay=0.0)], 1.0, -0.5),
+}
+
+
+@needs_cuda
+@pytest.mark.parametrize("edge", sorted(HYPER_EDGES))
+def test_hyper_parameter_edges(edge):
+    """Clipping disabled (max_norm <= 0), lr = 0, beta1 = beta2 = 0 (no
+    momentum, v = gc^2), weight decay 1 at lr 0.5, eps = 1 and a negative
+    grad_scale: each equals the oracle over two steps (gradients large enough
+    that clipping is active wherever it is on)."""
+    groups, max_norm, gscale = HYPER_EDGES[edge]
+    wl = workloads.custom(300 + sorted(HYPER_EDGES).index(edge), [30_000, 77, 5_000], decay=[True, False, True],
+                          gas=2, steps=2, grad_sigma=0.5, misalign=1, max_norm=max_norm)
+    wl.groups = groups
+    dense_parity(wl, defer=True, grad_scale=gscale)
+
+
+@needs_cuda
+@pytest.mark.parametrize("mode", ["flat", "list"])
+def test_sixteen_groups(mode):
+    """The maximum of 16 parameter groups, each with its own lr, betas, eps and
+    weight decay, over 16 tensors (group g = tensor g)."""
+    rng = np.random.default_rng(16)
+    wl = workloads.custom(320 + (mode == "list"), [int(x) for x in rng.integers(1, 9000, 16)], gas=2, steps=2,
+                          grad_sigma=0.2, misalign=2, mode=mode)
+    for g, t in enumerate(wl.tensors):
+        t.group = g
+    wl.groups = [_group(lr=float(10.0 ** rng.uniform(-5, -2)), beta1=float(rng.uniform(0.5, 0.99)),
+                        beta2=float(rng.uniform(0.9, 0.999)), eps=float(10.0 ** rng.uniform(-9, -6)),
+                        weight_decay=float(rng.choice([0.0, 0.01, 0.1]))) for _ in range(16)]
+    dense_parity(wl, defer=True)
