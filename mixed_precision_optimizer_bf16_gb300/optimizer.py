@@ -189,7 +189,7 @@ class BF16Optimizer:
 
     @classmethod
     def from_parameters(cls, param_groups, lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.0,
-                        max_grad_norm=1.0, grad_scale=1.0):
+                        max_grad_norm=1.0, grad_scale=1.0, grad_buffers=1):
         """One FLAT shard over a model's bf16 parameters.
 
         param_groups: an iterable of parameters, or torch.optim-style dicts
@@ -201,6 +201,12 @@ class BF16Optimizer:
         and its .grad a view into the flat bf16 gradient buffer `grad_buffer`,
         which backward adds into: call zero_grad() before each micro-batch's
         backward and accumulate() (no gradient argument) after it.
+
+        grad_buffers=N allocates N flat gradient buffers (2 bytes per element
+        each); use_grad_buffer(i) points every .grad at buffer i.  With one
+        buffer per micro-batch every micro-batch can be deferred, so the FP32
+        accumulator is never stored: 42 instead of 64 bytes per element per
+        step at GAS 4, the same FP32 adds in the same order.
         """
         groups = list(param_groups)
         if groups and isinstance(groups[0], torch.Tensor):
@@ -224,22 +230,35 @@ class BF16Optimizer:
         flat = {k: torch.zeros(n, dtype=torch.float32, device=dev)
                 for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum")}
         flat["param_bf16"] = torch.empty(n, dtype=torch.bfloat16, device=dev)
-        grads = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        if grad_buffers < 1:
+            raise ValueError("grad_buffers must be >= 1")
+        bufs = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(int(grad_buffers))]
         with torch.no_grad():
             for p, off in layout:
                 k = p.numel()
                 flat["param_bf16"][off:off + k].copy_(p.reshape(-1))
                 flat["master"][off:off + k].copy_(p.reshape(-1).float())
                 p.data = flat["param_bf16"][off:off + k].view(p.shape)
-                p.grad = grads[off:off + k].view(p.shape)
         opt = cls(hyper, flat=flat, ranges=ranges, max_grad_norm=max_grad_norm, grad_scale=grad_scale)
-        opt.grad_buffer = grads
         opt.flat = flat
         opt.ranges = ranges
+        opt.grad_buffers = bufs
+        opt._layout = layout
+        opt.use_grad_buffer(0)
         return opt
 
+    def use_grad_buffer(self, i, stream=None):
+        """Point every parameter's .grad at flat gradient buffer i of a
+        from_parameters() optimizer and zero that buffer; returns it."""
+        buf = self.grad_buffers[i]
+        for p, off in self._layout:
+            p.grad = buf[off:off + p.numel()].view(p.shape)
+        self.grad_buffer = buf
+        self.zero_grad(stream)
+        return buf
+
     def zero_grad(self, stream=None):
-        """Zero the flat gradient buffer of a from_parameters() optimizer."""
+        """Zero the current flat gradient buffer of a from_parameters() optimizer."""
         with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
             self.grad_buffer.zero_()
 

@@ -2,9 +2,10 @@
 
 A small bf16 model is trained with BF16Optimizer.from_parameters: autograd
 writes each micro-batch's bf16 gradients into the optimizer's flat gradient
-buffer, the library accumulates them (the last micro-batch deferred into the
-step), clips and applies AdamW, and the model's parameters -- views into the
-flat bf16 parameter buffer -- change in place.  Every step is checked against
+buffer (one reused buffer, or one per micro-batch), the library accumulates
+them (the last micro-batch, or every one, deferred into the step), clips and
+applies AdamW, and the model's parameters -- views into the flat bf16
+parameter buffer -- change in place.  Every step is checked against
 the oracle fed the very gradients autograd produced, with the parity tests'
 tolerances, and the loss must fall.
 """
@@ -29,14 +30,19 @@ def _host(t, dtype):
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
-def test_training_loop_matches_oracle_every_step():
+@pytest.mark.parametrize("resident", [False, True])
+def test_training_loop_matches_oracle_every_step(resident):
+    """resident=False: one gradient buffer, the last micro-batch deferred;
+    resident=True: one gradient buffer per micro-batch and every micro-batch
+    deferred (the accumulator is never stored)."""
     torch.manual_seed(0)
     model = torch.nn.Sequential(torch.nn.Linear(48, 160), torch.nn.GELU(), torch.nn.Linear(160, 48))
     model = model.cuda().to(torch.bfloat16)
     decay = [p for name, p in model.named_parameters() if name.endswith("weight")]
     no_decay = [p for name, p in model.named_parameters() if name.endswith("bias")]
+    gas = 3
     opt = BF16Optimizer.from_parameters([{"params": decay, "weight_decay": 0.01}, {"params": no_decay}],
-                                        lr=1e-2, max_grad_norm=1.0)
+                                        lr=1e-2, max_grad_norm=1.0, grad_buffers=gas if resident else 1)
     flat = opt.flat
     n = flat["master"].numel()
     base, end = flat["param_bf16"].data_ptr(), flat["param_bf16"].data_ptr() + 2 * n
@@ -52,17 +58,20 @@ def test_training_loop_matches_oracle_every_step():
     sc = {"M": np.zeros(n), "A": np.abs(p.astype(np.float64))}
 
     gen = torch.Generator(device="cuda").manual_seed(1)
-    gas, losses = 3, []
+    losses = []
     for step in range(5):
         grads = []
         for k in range(gas):
-            opt.zero_grad()
+            if resident:
+                opt.use_grad_buffer(k)
+            else:
+                opt.zero_grad()
             x = torch.randn(64, 48, device="cuda", generator=gen).to(torch.bfloat16)
             y = 0.5 * torch.roll(x, 1, dims=1)
             loss = ((model(x).float() - y.float()) ** 2).mean()
             loss.backward()
             grads.append(_host(opt.grad_buffer, torch.int16).view(np.uint16))
-            opt.accumulate(first=k == 0, last=k == gas - 1, defer=k == gas - 1)
+            opt.accumulate(first=k == 0, last=k == gas - 1, defer=resident or k == gas - 1)
             losses.append(loss.item())
         norm = opt.grad_norm(sync=True)
         opt.step()
