@@ -151,9 +151,18 @@ typedef struct bf16opt bf16opt_t;    /* opaque handle */
 
 /* ---- entry points ------------------------------------------------------- */
 
-/* Validates `d`, copies its host arrays, builds the segment and chunk tables
- * on the device and allocates the norm scratch.  *out receives the handle
- * (NULL on error).  The step counter starts at 0. */
+/* One handle per rank's parameter shard ("BLOOM 176B 训练技术概览", section
+ * 并行细节 / ZeRO: each GPU holds only its part of the parameters, gradients
+ * and optimizer states).  Validates `d` before any CUDA call, copies its host
+ * arrays (the caller may free them on return), builds the segment and chunk
+ * tables on the device and allocates the library's scratch; the device
+ * buffers stay the caller's.  *out receives the handle (NULL on error).  The
+ * step counter starts at 0.  Errors: INVALID_ARG (NULL d or out, bad mode,
+ * 0 or more than BF16OPT_MAX_GROUPS groups, a hyper-parameter out of range,
+ * non-finite max_grad_norm, zero or non-finite grad_scale, NULL buffers,
+ * ranges that do not tile [0, n) in order, overlapping buffers, more than
+ * 2^32 - 1 chunks), ALIGNMENT, UNSUPPORTED (no CUDA device), OOM, CUDA;
+ * bf16opt_last_error(NULL) has the message. */
 int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out);
 
 /* Adds one micro-batch of bf16 gradients into the FP32 accumulator
@@ -164,7 +173,10 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out);
  *   flags: BF16OPT_FIRST / BF16OPT_LAST / BF16OPT_DEFER (see above).
  * The gradient buffer is read on `stream`; it may be reused after the work
  * on `stream` is done, except under BF16OPT_DEFER (until the pass that folds
- * it).  A DEFER beyond BF16OPT_MAX_DEFERRED pending is BF16OPT_ERR_INVALID_ARG. */
+ * it).  Errors: SEQUENCE (no FIRST outside an accumulation), INVALID_ARG
+ * (not a live handle, unknown flag, a NULL or wrong-mode gradient pointer, a
+ * DEFER beyond BF16OPT_MAX_DEFERRED pending), ALIGNMENT (a gradient pointer
+ * not 2-byte aligned), CUDA. */
 int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *const *grad_list,
                        unsigned flags, void *stream);
 
@@ -174,7 +186,9 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
  * on the device for bf16opt_step.  host_norm == NULL: fully asynchronous.
  * host_norm != NULL: waits for `stream` and stores the norm (FP64); returns
  * BF16OPT_WARN_NONFINITE if it is Inf or NaN (the caller decides whether to
- * call bf16opt_step; the library does not skip steps). */
+ * call bf16opt_step; the library skips nothing unless bf16opt_set_skip_nonfinite
+ * asked it to).  Errors: SEQUENCE (no completed accumulation), INVALID_ARG
+ * (not a live handle), CUDA. */
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
 
 /* Multi-rank use.  Under ZeRO every rank owns one partition of the parameters
@@ -200,14 +214,18 @@ int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream);
  * sequence accumulate ... -> grad_norm (host_norm = NULL) -> step, captured
  * once on a stream, replays as later steps (same gradient buffers; lr_override
  * values are frozen into the capture).  Calls that synchronise (grad_norm with
- * host_norm, grad_norm_local, get/set_step, set_lr_schedule, create, destroy)
- * must stay outside a capture. */
+ * host_norm, grad_norm_local, get/set_step, set_lr_schedule,
+ * set_skip_nonfinite, debug_faults, create, destroy) must stay outside a
+ * capture. */
 
 /* One fused pass: clip, AdamW (t = t + 1, bias-corrected, decoupled
  * weight decay), FP32 master/moment update and bf16 parameter write
  * ("企业官网建设流程全解析", sections 1 and 3.3).
  * lr_override: NULL, or a HOST array of n_groups learning rates that
- * replaces the groups' lr for this step only (for an LR schedule). */
+ * replaces the groups' lr for this step only (for an LR schedule; read during
+ * the call only).  Errors: SEQUENCE (no grad_norm or set_global_sumsq since
+ * the accumulation), INVALID_ARG (not a live handle, a negative or non-finite
+ * lr_override entry), CUDA. */
 int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream);
 
 /* Learning-rate schedule of the training configuration ("单机多卡实战：
@@ -236,7 +254,8 @@ int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor)
  * the step number of that step (the step counter plus one, so a resumed run
  * that restored its counter with bf16opt_set_step continues the schedule).
  * Waits for all work on the handle's device first, so steps already enqueued
- * keep the old schedule; not during a stream capture. */
+ * keep the old schedule; not during a stream capture.  Errors: INVALID_ARG
+ * (not a live handle, an invalid schedule as for bf16opt_lr_factor), CUDA. */
 int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s);
 
 /* Opt-in guard for steps whose global norm is Inf or NaN (enable != 0): the
