@@ -91,15 +91,18 @@ def _huge_fraction(start, nbytes):
 class PinnedHostBuffer:
     """Page-locked host memory for gradients that stream to the GPU.
 
-    The region is aligned to the transparent-huge-page size, advised as huge
-    (MADV_HUGEPAGE), faulted in and registered with cudaHostRegister.  Large
-    pages keep the address translations of the host-to-device copies few: on a
-    host whose memory is fragmented by earlier large jobs, small-page pinned
-    buffers slowed copies that overlap HBM-bound kernels by almost 2x, huge-page
-    ones far less.  `tensor` is a CPU tensor over the region (is_pinned()).
-    Falls back to the driver's pinned allocator (torch pin_memory) when the
-    kernel cannot back at least 90 % of the region with huge pages (small-page
-    registered memory was measured slower still) or registration is refused.
+    The region is aligned to the transparent-huge-page size and rounded up to
+    whole huge pages, advised as huge (MADV_HUGEPAGE), faulted in and registered
+    with cudaHostRegister.  Large pages keep the address translations of the
+    host-to-device copies few: on a host whose memory is fragmented by earlier
+    large jobs, small-page pinned buffers slowed copies that overlap HBM-bound
+    kernels by almost 2x, huge-page ones far less.  Whole huge pages leave no
+    small-page tail, which the kernel's background collapse (khugepaged) would
+    keep trying, and failing, to merge while it is pinned.  `tensor` is a CPU
+    tensor over the first numel elements (is_pinned()).  Falls back to the
+    driver's pinned allocator (torch pin_memory) when the kernel cannot back at
+    least 90 % of the region with huge pages (small-page registered memory was
+    measured slower still) or registration is refused.
     """
 
     MADV_HUGEPAGE = 14
@@ -111,21 +114,22 @@ class PinnedHostBuffer:
         self.huge_fraction = 0.0
         try:
             align = _thp_size()
-            self._map = mmap.mmap(-1, nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+            span = max(align, (nbytes + align - 1) // align * align)          # whole huge pages
+            self._map = mmap.mmap(-1, span + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
             addr = ctypes.addressof(ctypes.c_char.from_buffer(self._map))
             start = (addr + align - 1) & ~(align - 1)
             libc = ctypes.CDLL(None, use_errno=True)
             libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
-            libc.madvise(ctypes.c_void_p(start), nbytes, self.MADV_HUGEPAGE)   # advisory
-            arr = np.frombuffer(self._map, dtype=np.uint8, count=nbytes, offset=start - addr)
-            arr[:] = 0                                                          # fault the pages in now
-            self.huge_fraction = _huge_fraction(start, nbytes)
+            libc.madvise(ctypes.c_void_p(start), span, self.MADV_HUGEPAGE)     # advisory
+            whole = np.frombuffer(self._map, dtype=np.uint8, count=span, offset=start - addr)
+            whole[:] = 0                                                        # fault every page in now
+            self.huge_fraction = _huge_fraction(start, span)
             if self.huge_fraction < 0.9:
                 raise RuntimeError("not backed by huge pages")
-            if int(torch.cuda.cudart().cudaHostRegister(start, nbytes, 0)) != 0:
+            if int(torch.cuda.cudart().cudaHostRegister(start, span, 0)) != 0:
                 raise RuntimeError("cudaHostRegister refused")
             self._registered = start
-            self.tensor = torch.from_numpy(arr).view(dtype)
+            self.tensor = torch.from_numpy(whole[:nbytes]).view(dtype)
             self.huge_pages = True
         except Exception:
             self._map = None
