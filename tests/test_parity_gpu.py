@@ -471,6 +471,7 @@ DEFER_PATTERNS = [
     [True] * 8 + [False],                      # 8 pending, then a stored pass: pre-fold, then this one
     [True] * 8 + [False, True],                # ... and a deferred last micro-batch after it
     [False] + [True] * 8 + [False, False],     # the pre-fold onto a stored accumulator
+    [True] * 7 + [False] + [True] * 7 + [False] + [True],   # runs of 8 folded by their 8th (GAS 17)
 ]
 
 
