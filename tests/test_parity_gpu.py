@@ -156,10 +156,16 @@ def test_scaled_bloom_full_size_sampled(defer):
 
 
 @needs_cuda
-def test_large_partition_full_size_sampled():
-    """1.83e9 flat elements, GAS 32, 1 step."""
-    st = sampled_parity(workloads.workload(3), defer=True)
-    print("large partition", st)
+@pytest.mark.parametrize("pattern", ["last", "eights"])
+def test_large_partition_full_size_sampled(pattern):
+    """1.83e9 flat elements, GAS 32, 1 step: the last micro-batch deferred, or
+    every gradient resident with each run of 8 folded by its 8th and the last
+    8 deferred into the norm pass and the step (32 gradient buffers, ~150 GB
+    on the device; the 8-gradient fold kernels at full size)."""
+    import bench
+    wl = workloads.workload(3)
+    st = sampled_parity(wl, defer=True if pattern == "last" else bench.resident_pattern(wl.gas))
+    print("large partition", pattern, st)
 
 
 @needs_cuda
