@@ -83,18 +83,6 @@ def pass_bytes(pattern):
     return calls, step
 
 
-def resident_pattern(G, fold=8):
-    """Deferral pattern that keeps every micro-batch's gradient resident: all
-    G deferred when G <= fold; otherwise runs of `fold`, each folded into the
-    accumulator by its last micro-batch, and the final run deferred into the
-    norm pass and the step (never more than `fold` pending)."""
-    if G <= fold:
-        return [True] * G
-    tail = G % fold or fold
-    head = G - tail
-    return [(k % fold) != fold - 1 for k in range(head)] + [True] * tail
-
-
 def max_over_ranks(value, device):
     """Max of a float over all ranks of the default process group (the job's
     time is its slowest rank's).  Plain value when there is no group."""
@@ -331,6 +319,7 @@ def run_ours(args):
     # accumulator is never stored; the norm pass and the step fold all of them)
     variant = None
     if not args.no_variant:
+        from mixed_precision_optimizer_bf16_gb300.optimizer import resident_pattern
         vpat = resident_pattern(G)
         for _ in range(2):
             one_step(pat=vpat)

@@ -145,6 +145,20 @@ class PinnedHostBuffer:
         self.tensor = None
 
 
+def resident_pattern(gas, fold=8):
+    """Per-micro-batch `defer` flags for a step whose micro-batch gradients all
+    stay resident (one buffer each): all deferred when gas <= fold (the FP32
+    accumulator is never stored); otherwise runs of `fold`, each folded into
+    the accumulator by its last micro-batch, and the final run deferred into
+    the norm pass and the step -- never more than `fold` pending, the library's
+    limit (8).  At GAS 32: 134 instead of 344 bytes per element per step."""
+    if gas <= fold:
+        return [True] * gas
+    tail = gas % fold or fold
+    head = gas - tail
+    return [(k % fold) != fold - 1 for k in range(head)] + [True] * tail
+
+
 def global_sumsq(local, group=None):
     """Sum of every rank's local sum of squares, in rank order (deterministic and
     identical on all ranks); `local` when torch.distributed is not initialised."""

@@ -162,9 +162,9 @@ def test_large_partition_full_size_sampled(pattern):
     every gradient resident with each run of 8 folded by its 8th and the last
     8 deferred into the norm pass and the step (32 gradient buffers, ~150 GB
     on the device; the 8-gradient fold kernels at full size)."""
-    import bench
+    from mixed_precision_optimizer_bf16_gb300.optimizer import resident_pattern
     wl = workloads.workload(3)
-    st = sampled_parity(wl, defer=True if pattern == "last" else bench.resident_pattern(wl.gas))
+    st = sampled_parity(wl, defer=True if pattern == "last" else resident_pattern(wl.gas))
     print("large partition", pattern, st)
 
 

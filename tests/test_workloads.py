@@ -69,3 +69,18 @@ def test_bytes_model():
     assert wl.bytes_per_step() == wl.n * 66
     assert workloads.workload(3).bytes_per_step() == workloads.workload(3).n * (6 + 310 + 30)
     np.testing.assert_equal(wl.tensor_of([0, 513_802_239, 513_802_240]), [0, 0, 1])
+
+
+def test_resident_pattern_respects_the_pending_limit():
+    """resident_pattern never leaves more than 8 micro-batches pending, defers
+    everything for GAS <= 8, and ends every pattern deferred."""
+    from mixed_precision_optimizer_bf16_gb300.optimizer import resident_pattern
+    for gas in range(1, 70):
+        pat = resident_pattern(gas)
+        assert len(pat) == gas and pat[-1]
+        run = worst = 0
+        for d in pat:
+            run = run + 1 if d else 0
+            worst = max(worst, run)
+        assert worst <= 8
+        assert all(pat) == (gas <= 8)
