@@ -11,7 +11,8 @@ Prints ONE JSON line (rank 0).  `value` is elements/s over all ranks with
 inputs resident in HBM; `e2e` is the same metric with every micro-batch
 gradient copied from pinned host memory inside the timed region and the norm
 read back; `roofline` is the dominant kernel (the fused step) against the
-measured HBM copy peak; `cpu_baseline` is the CPU oracle on a bounded sample.
+measured HBM copy peak; `cpu_baseline` is the CPU oracle on a bounded sample
+(rank 0 of a 1-GPU run only).
 `--impl reference` times that oracle instead, as the reference arm.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the shard
@@ -382,7 +383,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:   # the host cores' baseline belongs to the 1-GPU line
         cpu = cpu_oracle(wl, args.cpu_seconds, steps=None)
     traffic = profiled_traffic() if (args.workload == 2 and not args.elements) else None
     line = {
