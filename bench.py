@@ -84,6 +84,30 @@ def pass_bytes(pattern):
     return calls, step
 
 
+def host_memory_available():
+    """Bytes of host memory this process may still use: MemAvailable, capped
+    by the cgroup's limit minus its usage where one is set."""
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except (OSError, ValueError):
+        pass
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            lim = f.read().strip()
+        with open("/sys/fs/cgroup/memory.current") as f:
+            cur = int(f.read().strip())
+        if lim != "max":
+            left = int(lim) - cur
+            avail = left if avail is None else min(avail, left)
+    except (OSError, ValueError):
+        pass
+    return avail if avail is not None else 1 << 62
+
+
 def max_over_ranks(value, device):
     """Max of a float over all ranks of the default process group (the job's
     time is its slowest rank's).  Plain value when there is no group."""
@@ -425,9 +449,14 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     import torch
 
     from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
-    bufs = [PinnedHostBuffer(n, torch.int16) for _ in range(G)]
-    host = [hb.tensor for hb in bufs]
-    for k in range(G):
+    # One pinned buffer per micro-batch, unless that (on every rank of the node)
+    # would take more than half the host memory available: then micro-batches
+    # share buffers round-robin -- every step still copies G full gradients.
+    per_buf = 2 * n + (512 << 20)                   # bytes, with the huge-page rounding
+    nhost = max(1, min(G, int(0.5 * host_memory_available() // max(1, world * per_buf))))
+    bufs = [PinnedHostBuffer(n, torch.int16) for _ in range(nhost)]
+    host = [bufs[k % nhost].tensor for k in range(G)]
+    for k in range(nhost):
         host[k].copy_(grads[k])
     torch.cuda.synchronize(dev)
     comp = torch.cuda.current_stream(dev)
@@ -486,7 +515,8 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
             "h2d_bytes_per_step": 2 * n * G, "d2h_bytes_per_step": 8,
             "ms_per_step": round(dt * 1e3 / args.e2e_steps, 3), "steps": args.e2e_steps,
             "h2d_gbs": round(2 * n * G / (dt / args.e2e_steps) / 1e9, 1),
-            "host_buffers": "huge-page, cudaHostRegister" if huge else "torch pinned",
+            "host_buffers": ("huge-page, cudaHostRegister" if huge else "torch pinned")
+                            + ("" if nhost == G else f"; {nhost} shared by the {G} micro-batches (host memory)"),
             "host_huge_fraction": round(huge_frac, 3),
             "h2d_link_gbs_alone": round(max(link), 1),
             "step_wall_ms": [round((b - a) * 1e3, 1) for a, b in zip(marks, marks[1:])]}
