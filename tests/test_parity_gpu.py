@@ -1012,3 +1012,35 @@ def test_sixteen_groups(mode):
                         beta2=float(rng.uniform(0.9, 0.999)), eps=float(10.0 ** rng.uniform(-9, -6)),
                         weight_decay=float(rng.choice([0.0, 0.01, 0.1]))) for _ in range(16)]
     dense_parity(wl, defer=True)
+
+
+@needs_cuda
+def test_two_handles_on_two_streams_interleaved():
+    """Two independent shards (different layouts, sizes, GAS and deferral)
+    driven at the same time on two non-blocking streams, their calls
+    interleaved micro-batch by micro-batch: each equals the oracle, so handles
+    share no state."""
+    wa = workloads.custom(330, [70_001, 3], decay=[True, False], gas=3, steps=2, grad_sigma=0.2, misalign=1)
+    wb = workloads.custom(331, [9_000, 12_345, 7], decay=[False, True, True], gas=2, steps=2, grad_sigma=0.05,
+                          misalign=3, mode="list")
+    A, B = GpuShard(wa, defer=[False, True, True]), GpuShard(wb, defer=True)
+    torch.cuda.synchronize()                 # initial state written on the default stream
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in range(2):
+        for k in range(max(wa.gas, wb.gas)):
+            for sh, wl, st in ((A, wa, sa), (B, wb, sb)):
+                if k < wl.gas:
+                    buf = sh.gbufs[k % len(sh.gbufs)]
+                    sgpu.fill_grad(wl, s, k, buf, stream=st)
+                    sh.opt.accumulate(sh.grads_arg(buf), first=k == 0, last=k == wl.gas - 1,
+                                      defer=sh.pattern[k], stream=st)
+        for sh, st in ((A, sa), (B, sb)):
+            sh.opt.grad_norm(stream=st)
+        for sh, st in ((A, sa), (B, sb)):
+            sh.opt.step(stream=st)
+    torch.cuda.synchronize()
+    for sh, wl in ((A, wa), (B, wb)):
+        got = sh.states()
+        sh.close()
+        ref, scales = oracle_dense(wl, wl.steps)
+        compare(got, ref, scales, wl, check_acc=not sh.defer)
