@@ -448,13 +448,20 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     processes on one machine."""
     import torch
 
-    from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
+    from mixed_precision_optimizer_bf16_gb300.optimizer import fast_pinned_buffers
     # One pinned buffer per micro-batch, unless that (on every rank of the node)
     # would take more than half the host memory available: then micro-batches
     # share buffers round-robin -- every step still copies G full gradients.
+    # Buffers are chosen by their measured copy rate (the host is a virtual
+    # machine whose DMA speed differs from region to region); extra candidates
+    # stay within the same memory budget.
     per_buf = 2 * n + (512 << 20)                   # bytes, with the huge-page rounding
-    nhost = max(1, min(G, int(0.5 * host_memory_available() // max(1, world * per_buf))))
-    bufs = [PinnedHostBuffer(n, torch.int16) for _ in range(nhost)]
+    budget = int(0.5 * host_memory_available() // max(1, world * per_buf))
+    nhost = max(1, min(G, budget))
+    scratch = torch.empty_like(grads[0])            # probe target: the gradients stay intact
+    bufs, buf_gbs, rejected = fast_pinned_buffers(n, nhost, scratch, torch.int16,
+                                                  max_extra=max(0, min(12, budget - nhost)))
+    del scratch
     host = [bufs[k % nhost].tensor for k in range(G)]
     for k in range(nhost):
         host[k].copy_(grads[k])
@@ -518,6 +525,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
             "host_buffers": ("huge-page, cudaHostRegister" if huge else "torch pinned")
                             + ("" if nhost == G else f"; {nhost} shared by the {G} micro-batches (host memory)"),
             "host_huge_fraction": round(huge_frac, 3),
+            "host_buffer_gbs": buf_gbs, "host_buffers_rejected": rejected,
             "h2d_link_gbs_alone": round(max(link), 1),
             "step_wall_ms": [round((b - a) * 1e3, 1) for a, b in zip(marks, marks[1:])]}
 

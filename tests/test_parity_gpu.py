@@ -1044,3 +1044,23 @@ def test_two_handles_on_two_streams_interleaved():
         sh.close()
         ref, scales = oracle_dense(wl, wl.steps)
         compare(got, ref, scales, wl, check_acc=not sh.defer)
+
+
+@needs_cuda
+def test_fast_pinned_buffers():
+    """Rate-selected pinned host buffers: the requested count, pinned, with a
+    measured rate each, and data that round-trips."""
+    from mixed_precision_optimizer_bf16_gb300.optimizer import fast_pinned_buffers
+    n = 5_000_003
+    dst = torch.empty(n, dtype=torch.int16, device="cuda")
+    bufs, rates, rejected = fast_pinned_buffers(n, 2, dst, max_extra=2)
+    assert len(bufs) == 2 and len(rates) == 2 and 0 <= rejected <= 2
+    assert all(r > 0 for r in rates) and rates == sorted(rates, reverse=True)
+    src = torch.randint(-30000, 30000, (n,), dtype=torch.int16, device="cuda")
+    for hb in bufs:
+        assert hb.tensor.is_pinned() and hb.tensor.numel() == n
+        hb.tensor.copy_(src)
+        dst.copy_(hb.tensor, non_blocking=True)
+        torch.cuda.synchronize()
+        assert torch.equal(dst, src)
+        hb.close()
