@@ -1,12 +1,14 @@
 /*
  * step_parity.c -- the C ABI driven from plain C, checked against the oracle.
  *
- * Test program, not part of the library.  Two optimizer steps over a
- * 100,003-element FLAT shard in two parameter groups (weight decay 0.01 and
- * 0), every buffer one element past a 256-byte boundary, GAS 3 with the last
- * micro-batch deferred, run through include/bf16opt.h with device memory from
- * the CUDA runtime -- no Python, no PyTorch.  The same two steps run through
- * the FP64 CPU oracle (oracle/oracle.h) on the same seeded inputs
+ * Test program, not part of the library.  Two optimizer steps over 100,003
+ * elements in two parameter groups (weight decay 0.01 and 0), GAS 3 with the
+ * last micro-batch deferred, run through include/bf16opt.h with device memory
+ * from the CUDA runtime -- no Python, no PyTorch -- twice: as one FLAT shard
+ * (every buffer one element past a 256-byte boundary) and as a LIST of three
+ * separately allocated tensors (offsets of 1, 2 and 3 elements; the gradient
+ * list points into one flat buffer per micro-batch).  The same two steps run
+ * through the FP64 CPU oracle (oracle/oracle.h) on the same seeded inputs
  * (synth/synth.h).
  *
  * Tolerances are those of the parity tests: the norm within 1e-6 relative;
@@ -59,7 +61,7 @@ static void *dev_offset(size_t count, size_t size, void **base) {
     return (char *)*base + size;
 }
 
-int main(void) {
+static int run(int list_mode) {
     const bf16opt_group_t groups[2] = {{6e-5f, 0.9f, 0.95f, 1e-8f, 0.01f}, {6e-5f, 0.9f, 0.95f, 1e-8f, 0.0f}};
     orc_group_t ogroups[2];
     for (int g = 0; g < 2; ++g) {   /* the oracle gets the same FP32-rounded values */
@@ -84,32 +86,69 @@ int main(void) {
     }
     for (uint32_t k = 0; k < GAS; ++k) grads[k] = malloc(N * sizeof(uint16_t));
 
-    /* device state */
-    void *bases[5 + GAS];
-    float *d_p = dev_offset(N, 4, &bases[0]), *d_m = dev_offset(N, 4, &bases[1]);
-    float *d_v = dev_offset(N, 4, &bases[2]), *d_acc = dev_offset(N, 4, &bases[3]);
-    uint16_t *d_pb = dev_offset(N, 2, &bases[4]);
+    /* device state: FLAT = five shard buffers; LIST = five per tensor */
+    enum { NT = 3 };
+    const uint32_t tb[NT + 1] = {0, 40000, SPLIT, N};     /* tensor i = elements [tb[i], tb[i+1]) */
+    const uint32_t tgroup[NT] = {0, 0, 1};
+    void *bases[5 * NT + GAS];
+    int nb = 0;
+    float *d_p[NT], *d_m[NT], *d_v[NT], *d_acc[NT];
+    uint16_t *d_pb[NT];
+    const int parts = list_mode ? NT : 1;
+    for (int i = 0; i < parts; ++i) {
+        const uint32_t lo = list_mode ? tb[i] : 0, cnt = list_mode ? tb[i + 1] - tb[i] : N;
+        const size_t off = list_mode ? (size_t)i + 1 : 1;   /* elements past a 256-byte boundary */
+        void *b0, *b1, *b2, *b3, *b4;
+        cuda(cudaMalloc(&b0, (cnt + 64) * 4), "cudaMalloc");
+        cuda(cudaMalloc(&b1, (cnt + 64) * 4), "cudaMalloc");
+        cuda(cudaMalloc(&b2, (cnt + 64) * 4), "cudaMalloc");
+        cuda(cudaMalloc(&b3, (cnt + 64) * 4), "cudaMalloc");
+        cuda(cudaMalloc(&b4, (cnt + 64) * 2), "cudaMalloc");
+        bases[nb++] = b0; bases[nb++] = b1; bases[nb++] = b2; bases[nb++] = b3; bases[nb++] = b4;
+        d_p[i] = (float *)b0 + off;
+        d_m[i] = (float *)b1 + off;
+        d_v[i] = (float *)b2 + off;
+        d_acc[i] = (float *)b3 + off;
+        d_pb[i] = (uint16_t *)b4 + off;
+        cuda(cudaMemcpy(d_p[i], p + lo, (size_t)cnt * sizeof(float), cudaMemcpyHostToDevice), "upload masters");
+        cuda(cudaMemset(d_m[i], 0, (size_t)cnt * sizeof(float)), "memset");
+        cuda(cudaMemset(d_v[i], 0, (size_t)cnt * sizeof(float)), "memset");
+    }
     uint16_t *d_g[GAS];
-    for (uint32_t k = 0; k < GAS; ++k) d_g[k] = dev_offset(N, 2, &bases[5 + k]);
-    cuda(cudaMemcpy(d_p, p, N * sizeof(float), cudaMemcpyHostToDevice), "upload masters");
-    cuda(cudaMemset(d_m, 0, N * sizeof(float)), "memset");
-    cuda(cudaMemset(d_v, 0, N * sizeof(float)), "memset");
+    for (uint32_t k = 0; k < GAS; ++k) d_g[k] = dev_offset(N, 2, &bases[nb++]);
 
     bf16opt_desc_t d;
     memset(&d, 0, sizeof d);
-    d.mode = BF16OPT_FLAT;
     d.n_groups = 2;
     d.groups = groups;
-    d.n = N;
-    d.master = d_p;
-    d.exp_avg = d_m;
-    d.exp_avg_sq = d_v;
-    d.grad_accum = d_acc;
-    d.param_bf16 = d_pb;
-    d.ranges = ranges;
-    d.n_ranges = 2;
     d.max_grad_norm = 1.0f;
     d.grad_scale = 1.0f;
+    bf16opt_tensor_t tens[NT];
+    if (!list_mode) {
+        d.mode = BF16OPT_FLAT;
+        d.n = N;
+        d.master = d_p[0];
+        d.exp_avg = d_m[0];
+        d.exp_avg_sq = d_v[0];
+        d.grad_accum = d_acc[0];
+        d.param_bf16 = d_pb[0];
+        d.ranges = ranges;
+        d.n_ranges = 2;
+    } else {
+        memset(tens, 0, sizeof tens);
+        for (int i = 0; i < NT; ++i) {
+            tens[i].master = d_p[i];
+            tens[i].exp_avg = d_m[i];
+            tens[i].exp_avg_sq = d_v[i];
+            tens[i].grad_accum = d_acc[i];
+            tens[i].param_bf16 = d_pb[i];
+            tens[i].numel = tb[i + 1] - tb[i];
+            tens[i].group = tgroup[i];
+        }
+        d.mode = BF16OPT_LIST;
+        d.n_tensors = NT;
+        d.tensors = tens;
+    }
     bf16opt_t *h = NULL;
     api(bf16opt_create(&d, &h), "bf16opt_create", NULL);
 
@@ -121,7 +160,12 @@ int main(void) {
             for (uint32_t i = 0; i < N; ++i) grads[k][i] = synth_grad_bf16(key, i, synth_scale_for_sigma(0.05), 0, 0);
             cuda(cudaMemcpy(d_g[k], grads[k], N * sizeof(uint16_t), cudaMemcpyHostToDevice), "upload gradient");
             unsigned flags = (k == 0 ? BF16OPT_FIRST : 0u) | (k == GAS - 1 ? BF16OPT_LAST | BF16OPT_DEFER : 0u);
-            api(bf16opt_accumulate(h, d_g[k], NULL, flags, NULL), "bf16opt_accumulate", h);
+            if (!list_mode) {
+                api(bf16opt_accumulate(h, d_g[k], NULL, flags, NULL), "bf16opt_accumulate", h);
+            } else {
+                const uint16_t *glist[NT] = {d_g[k] + tb[0], d_g[k] + tb[1], d_g[k] + tb[2]};
+                api(bf16opt_accumulate(h, NULL, glist, flags, NULL), "bf16opt_accumulate", h);
+            }
             orc_accumulate(acc, grads[k], N, k == 0, 1);
         }
         double norm = 0.0;
@@ -151,10 +195,13 @@ int main(void) {
 
     float *gp = malloc(N * sizeof(float)), *gm = malloc(N * sizeof(float)), *gv = malloc(N * sizeof(float));
     uint16_t *gpb = malloc(N * sizeof(uint16_t));
-    cuda(cudaMemcpy(gp, d_p, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
-    cuda(cudaMemcpy(gm, d_m, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
-    cuda(cudaMemcpy(gv, d_v, N * sizeof(float), cudaMemcpyDeviceToHost), "download");
-    cuda(cudaMemcpy(gpb, d_pb, N * sizeof(uint16_t), cudaMemcpyDeviceToHost), "download");
+    for (int i = 0; i < parts; ++i) {
+        const uint32_t lo = list_mode ? tb[i] : 0, cnt = list_mode ? tb[i + 1] - tb[i] : N;
+        cuda(cudaMemcpy(gp + lo, d_p[i], (size_t)cnt * sizeof(float), cudaMemcpyDeviceToHost), "download");
+        cuda(cudaMemcpy(gm + lo, d_m[i], (size_t)cnt * sizeof(float), cudaMemcpyDeviceToHost), "download");
+        cuda(cudaMemcpy(gv + lo, d_v[i], (size_t)cnt * sizeof(float), cudaMemcpyDeviceToHost), "download");
+        cuda(cudaMemcpy(gpb + lo, d_pb[i], (size_t)cnt * sizeof(uint16_t), cudaMemcpyDeviceToHost), "download");
+    }
     int64_t steps_done = 0;
     api(bf16opt_get_step(h, &steps_done), "bf16opt_get_step", h);
     if (steps_done != STEPS) {
@@ -176,10 +223,20 @@ int main(void) {
         if (sv > 0 && ev / sv > worst_v) worst_v = ev / sv;
         if (sp > 0 && ep / sp > worst_p) worst_p = ep / sp;
     }
-    printf("c-abi step parity: %u elements, %u steps, GAS %u; norm rel err %.3g; scaled err m %.3g v %.3g p %.3g; %s\n",
-           N, STEPS, GAS, worst_norm, worst_m, worst_v, worst_p, bad ? "FAIL" : "ok");
+    printf("c-abi step parity (%s): %u elements, %u steps, GAS %u; norm rel err %.3g; scaled err m %.3g v %.3g "
+           "p %.3g; %s\n", list_mode ? "LIST, 3 tensors" : "FLAT", N, STEPS, GAS, worst_norm, worst_m, worst_v,
+           worst_p, bad ? "FAIL" : "ok");
 
     api(bf16opt_destroy(h), "bf16opt_destroy", NULL);
-    for (int k = 0; k < (int)(5 + GAS); ++k) cudaFree(bases[k]);
+    for (int k = 0; k < nb; ++k) cudaFree(bases[k]);
+    free(p); free(m); free(v); free(acc); free(pb); free(M); free(A);
+    free(gp); free(gm); free(gv); free(gpb);
+    for (uint32_t k = 0; k < GAS; ++k) free(grads[k]);
     return bad ? 1 : 0;
+}
+
+int main(void) {
+    const int flat = run(0);
+    const int list = run(1);
+    return flat || list ? 1 : 0;
 }
