@@ -77,6 +77,14 @@ extern "C" {
 #define BF16OPT_ERR_CUDA (-5)          /* a CUDA runtime call or kernel launch failed */
 #define BF16OPT_ERR_UNSUPPORTED (-6)   /* e.g. no usable CUDA device */
 
+/* ---- ABI version -------------------------------------------------------
+ * Raised whenever a declaration, a constant or a struct layout of this header
+ * changes.  bf16opt_abi_version() returns the value the library was built
+ * with; code compiled against a header with another value must not use it.
+ * No CUDA call; never fails. */
+#define BF16OPT_ABI_VERSION 1
+int bf16opt_abi_version(void);
+
 /* ---- modes and flags --------------------------------------------------- */
 #define BF16OPT_FLAT 0   /* one contiguous shard: five flat buffers + group ranges */
 #define BF16OPT_LIST 1   /* ragged list: five buffers per tensor (separate allocations) */

@@ -66,7 +66,9 @@ EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
            "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_skip_nonfinite",
-           "bf16opt_debug_faults")
+           "bf16opt_debug_faults", "bf16opt_abi_version")
+
+ABI_VERSION = 1   # BF16OPT_ABI_VERSION of the header these declarations mirror
 
 _lib = None
 
@@ -87,6 +89,10 @@ def load(path=None):
         raise RuntimeError(f"libbf16opt.so is not built ({path}); run __graft_entry__.build() -- "
                            "there is no fallback implementation")
     L = ctypes.CDLL(path)
+    L.bf16opt_abi_version.restype = ctypes.c_int
+    L.bf16opt_abi_version.argtypes = []
+    if L.bf16opt_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{path} has ABI version {L.bf16opt_abi_version()}, this binding {ABI_VERSION}: rebuild")
     hp = ctypes.c_void_p
     L.bf16opt_create.restype = ctypes.c_int
     L.bf16opt_create.argtypes = [ctypes.POINTER(bf16opt_desc_t), ctypes.POINTER(hp)]

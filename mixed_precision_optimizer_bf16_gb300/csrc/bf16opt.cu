@@ -154,28 +154,6 @@ uint32_t first_chunk_cut(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) 
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 
-#ifndef BF16K_ACC_U
-#define BF16K_ACC_U 8       // quads in flight per thread, accumulate family
-#endif
-#ifndef BF16K_STEP_U
-#define BF16K_STEP_U 2      // quads in flight per thread, fused step
-#endif
-#ifndef BF16K_FOLD4_ACC_U
-#define BF16K_FOLD4_ACC_U 4  // quads in flight, passes folding 2-4 gradients
-#endif
-#ifndef BF16K_FOLD8_ACC_U
-#define BF16K_FOLD8_ACC_U 1  // quads in flight, passes folding 5-8 gradients
-#endif
-#ifndef BF16K_FOLD4_STEP_U
-#define BF16K_FOLD4_STEP_U 2  // quads in flight, fused step folding 2-4 gradients
-#endif
-#ifndef BF16K_FOLD8_STEP_U
-#define BF16K_FOLD8_STEP_U 1  // quads in flight, fused step folding 5-8 gradients
-#endif
-#ifndef BF16K_MAX_CTAS_PER_SM
-#define BF16K_MAX_CTAS_PER_SM 64
-#endif
-
 template <class K>
 int grid_for(bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
     int per_sm = 0;
@@ -336,6 +314,8 @@ cudaError_t upload_params(bf16opt_t *h) {
 }  // namespace
 
 extern "C" {
+
+int bf16opt_abi_version(void) { return BF16OPT_ABI_VERSION; }
 
 const char *bf16opt_error_string(int code) {
     switch (code) {

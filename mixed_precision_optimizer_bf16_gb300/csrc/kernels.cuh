@@ -53,6 +53,29 @@ namespace bf16k {
 #ifndef BF16K_HEAD_ALIGN
 #define BF16K_HEAD_ALIGN 32
 #endif
+// Quads (4 elements) in flight per thread, by pass, and the cap on resident
+// CTAs per SM a launch is sized for.
+#ifndef BF16K_ACC_U
+#define BF16K_ACC_U 8         // accumulate family
+#endif
+#ifndef BF16K_STEP_U
+#define BF16K_STEP_U 2        // fused step
+#endif
+#ifndef BF16K_FOLD4_ACC_U
+#define BF16K_FOLD4_ACC_U 4   // passes folding 2-4 gradients
+#endif
+#ifndef BF16K_FOLD8_ACC_U
+#define BF16K_FOLD8_ACC_U 1   // passes folding 5-8 gradients
+#endif
+#ifndef BF16K_FOLD4_STEP_U
+#define BF16K_FOLD4_STEP_U 2  // fused step folding 2-4 gradients
+#endif
+#ifndef BF16K_FOLD8_STEP_U
+#define BF16K_FOLD8_STEP_U 1  // fused step folding 5-8 gradients
+#endif
+#ifndef BF16K_MAX_CTAS_PER_SM
+#define BF16K_MAX_CTAS_PER_SM 64
+#endif
 constexpr int kAccThreads = BF16K_ACC_THREADS;    // threads per CTA, accumulate / norm passes
 constexpr int kStepThreads = BF16K_STEP_THREADS;  // threads per CTA, fused step
 constexpr int kThreads = kAccThreads;

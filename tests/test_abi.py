@@ -178,3 +178,10 @@ def test_unknown_handles_are_rejected_without_dereference(lib):
     assert C.bf16opt_set_lr_schedule(fake, C.lr_schedule(10, 100, 0.1)) == E
     assert C.bf16opt_destroy(fake) == E
     assert "not a live" in C.bf16opt_last_error(fake)
+
+
+def test_abi_version_matches_header_and_binding(lib):
+    """The library, the header and the Python binding agree on the ABI version."""
+    src = open(HEADER).read()
+    m = re.search(r"#define BF16OPT_ABI_VERSION (\d+)", src)
+    assert m and int(m.group(1)) == C.ABI_VERSION == lib.bf16opt_abi_version()
