@@ -132,10 +132,16 @@ L2_BYTES = 129 * 1000 * 1000   # GB300 L2 (129 MB)
 
 
 def kernel_hash():
+    """First 16 hex digits of the sha256 of the kernel sources with comments
+    removed and whitespace collapsed: the code and its launch shape, so that
+    editing a comment does not void the recorded profile."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

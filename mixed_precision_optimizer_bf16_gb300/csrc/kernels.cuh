@@ -16,12 +16,14 @@
 //                    ("企业官网建设流程全解析", sections 1 and 3.3).
 //
 // Work decomposition.  A segment is one run of elements with one parameter
-// group and one set of base pointers (a flat range or a list tensor).  Each
-// segment is cut into chunks of kChunk elements; a persistent grid strides over
-// the chunks.  Inside a chunk, thread t handles 4-element quads t, t+T, ...
-// so that every warp-wide access is contiguous: FP32 as 16-byte and bf16 as
-// 8-byte vectors.  Leading elements up to the first 16-byte-aligned FP32
-// address, and the ragged tail, are done one element at a time.  If the
+// group and one set of base pointers (a flat range or a list tensor).  The
+// host cuts each segment into chunks of at most kChunk elements (the first one
+// shortened so that later chunks start on a 128-byte line of the master
+// buffer); a persistent grid strides over the chunk table.  Inside a chunk,
+// thread t handles 4-element quads t, t+T, ... so that every warp-wide access
+// is contiguous: FP32 as 16-byte and bf16 as 8-byte vectors.  Leading elements
+// up to the lead pointer's next kHeadAlign-element boundary, and the ragged
+// tail, are done one element at a time by a warp chosen per chunk.  If the
 // buffers of a segment do not share their offset modulo 16 bytes the whole
 // chunk runs element-wise (correct, slower).
 //
