@@ -58,3 +58,15 @@ def test_clocks_median_under_load_and_reasons():
 def test_clocks_no_reasons():
     r = _clocks_from([ROW.format(sm=2070, pw=850.0, hw="Not Active", cap="Not Active")] * 4)
     assert r["reasons"] == [] and r["samples_under_load"] == 4
+
+
+def test_kernel_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    """The recorded-profile hash follows the kernels' code, not their comments."""
+    f = tmp_path / "k.cuh"
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", [str(f)])
+    f.write_text("// header\n__global__ void k(float *p) { p[0] = 1.0f; }  /* body */\n")
+    h0 = bench.kernel_hash()
+    f.write_text("// another header\n/* reworded\n   block */ __global__ void k(float *p) {\n  p[0] = 1.0f;\n}\n")
+    assert bench.kernel_hash() == h0
+    f.write_text("__global__ void k(float *p) { p[0] = 2.0f; }\n")
+    assert bench.kernel_hash() != h0
