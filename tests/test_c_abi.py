@@ -47,3 +47,14 @@ def test_c_program_matches_oracle(tmp_path):
     print(r.stdout, r.stderr)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "ok" in r.stdout
+
+
+@pytest.mark.parametrize("lang, std", [("c", "c99"), ("c++", "c++11"), ("c++", "c++17")])
+def test_header_compiles_standalone(tmp_path, lang, std):
+    """include/bf16opt.h on its own: plain C99 (pedantic) and C++, warnings as errors."""
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "bf16opt.h"\n'
+                   "int probe(void) { bf16opt_desc_t d; (void)d; return BF16OPT_ABI_VERSION + BF16OPT_MAX_GROUPS; }\n")
+    cc = "gcc" if lang == "c" else "g++"
+    subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-c", str(src),
+                    "-I", os.path.join(ROOT, "include"), "-o", str(tmp_path / "use.o")], check=True)
