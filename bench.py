@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-variant", action="store_true", help="skip the all-deferred variant timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time of the CPU baseline")
+    ap.add_argument("--extra", default="3,4", help="other workloads timed after the headline one ('' = none)")
+    ap.add_argument("--extra-steps", type=int, default=10)
     return ap.parse_args()
 
 
@@ -218,13 +220,112 @@ class Clocks:
 
 # ------------------------------------------------------------------ our arm
 
+def build_shard(wl, dev):
+    """A workload's device state and one bf16 gradient buffer per micro-batch
+    (seeded masters and step-0 gradients, m = v = 0), and its optimizer handle.
+    Returns (optimizer, per-micro-batch gradient arguments, buffers to keep)."""
+    import torch
+
+    from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat
+    from synth import gpu as sgpu
+
+    n = wl.n
+
+    def buf(count, dtype):
+        return torch.empty(count + wl.misalign + 64, dtype=dtype, device=dev)[wl.misalign:wl.misalign + count]
+
+    gflat = []
+    for k in range(wl.gas):
+        g = buf(n, torch.int16)
+        sgpu.fill_grad(wl, 0, k, g)
+        gflat.append(g)
+    if wl.mode == "flat":
+        state = alloc_flat(n, dev, wl.misalign)
+        sgpu.fill_master(wl, state["master"])
+        for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+            state[k].zero_()
+        opt = BF16Optimizer(wl.groups, flat=state, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
+        grads = gflat
+    else:
+        state = []
+        for i, (t, off) in enumerate(zip(wl.tensors, wl.offsets)):
+            d = {k: buf(t.numel, torch.float32) for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum")}
+            d["param_bf16"] = buf(t.numel, torch.int16)
+            sgpu.fill_master(wl, d["master"], off)
+            for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
+                d[k].zero_()
+            d["group"] = wl.group_of_tensor(i)
+            state.append(d)
+        opt = BF16Optimizer(wl.groups, tensors=state, max_grad_norm=wl.max_norm)
+        grads = [[g[off:off + t.numel] for t, off in zip(wl.tensors, wl.offsets)] for g in gflat]
+    return opt, grads, (state, gflat)
+
+
+def groups_used(wl):
+    """Parameter groups that hold at least one element of the workload."""
+    return len({wl.group_of_tensor(i) for i, t in enumerate(wl.tensors) if t.numel})
+
+
+def extra_workload(wl_id, steps, warmup, dev, world, peak, no_clocks):
+    """ms per step, elements/s and algorithmic HBM GB/s of another single-GPU
+    workload, in two launch patterns: the last micro-batch deferred into the
+    fused step (one gradient buffer in flight), and every gradient resident
+    (runs of 8 folded by their 8th, the last run deferred).  Device-resident
+    inputs larger than L2, CUDA events on the launching stream, max over ranks."""
+    import torch
+    import torch.distributed as dist
+
+    from mixed_precision_optimizer_bf16_gb300.optimizer import resident_pattern
+    from synth import workloads
+
+    wl = workloads.workload(wl_id)
+    n, G = wl.n, wl.gas
+    opt, grads, held = build_shard(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    pats = {"last_deferred": [False] * (G - 1) + [True],
+            "resident" if G <= 8 else "resident_in_eights": resident_pattern(G)}
+    out = {"workload": wl.name, "elements": n, "tensors": len(wl.tensors), "groups": groups_used(wl), "gas": G,
+           "mode": wl.mode}
+    for name, pat in pats.items():
+        def one():
+            for k in range(G):
+                opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=pat[k], stream=stream)
+            opt.grad_norm(stream=stream)
+            opt.step(stream=stream)
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize(dev)
+        clocks = Clocks(dev.index, enabled=not no_clocks)
+        if world > 1:
+            dist.barrier()
+        clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        ms = max_over_ranks(e0.elapsed_time(e1), dev) / steps
+        calls, step_b = pass_bytes(pat)
+        bpe = sum(calls) + step_b
+        gbs = bpe * n / (ms * 1e-3) / 1e9
+        out[name] = {"value": round(n * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+                     "steps": steps, "warmup": warmup, "bytes_per_elem_per_step": bpe, "hbm_gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "clocks": clk}
+    opt.close()
+    del opt, grads, held
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
-    from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat
-    from synth import gpu as sgpu, workloads
+    from synth import workloads
 
     rank, world, local = rank_info()
     torch.cuda.set_device(local)
@@ -238,34 +339,7 @@ def run_ours(args):
         wl = workloads.prefix(wl, args.elements)
     n, G = wl.n, wl.gas
     defer = not args.no_defer
-
-    def buf(count, dtype):
-        return torch.empty(count + wl.misalign + 64, dtype=dtype, device=dev)[wl.misalign:wl.misalign + count]
-
-    gflat = []
-    for k in range(G):
-        g = buf(n, torch.int16)
-        sgpu.fill_grad(wl, 0, k, g)
-        gflat.append(g)
-    if wl.mode == "flat":
-        flat = alloc_flat(n, dev, wl.misalign)
-        sgpu.fill_master(wl, flat["master"])
-        for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
-            flat[k].zero_()
-        opt = BF16Optimizer(wl.groups, flat=flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
-        grads = gflat
-    else:
-        flat = []
-        for i, (t, off) in enumerate(zip(wl.tensors, wl.offsets)):
-            d = {k: buf(t.numel, torch.float32) for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum")}
-            d["param_bf16"] = buf(t.numel, torch.int16)
-            sgpu.fill_master(wl, d["master"], off)
-            for k in ("exp_avg", "exp_avg_sq", "grad_accum", "param_bf16"):
-                d[k].zero_()
-            d["group"] = wl.group_of_tensor(i)
-            flat.append(d)
-        opt = BF16Optimizer(wl.groups, tensors=flat, max_grad_norm=wl.max_norm)
-        grads = [[g[off:off + t.numel] for t, off in zip(wl.tensors, wl.offsets)] for g in gflat]
+    opt, grads, held = build_shard(wl, dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -405,8 +479,19 @@ def run_ours(args):
         e2e = run_e2e(args, opt, grads, G, defer, dev, world, n)
 
     opt.close()
-    del grads, flat, gflat
+    del opt, grads, held
+    torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
+
+    # the other single-GPU target shards, timed by the same run (config freed first)
+    extra = None
+    if args.extra and not args.elements:
+        extra = {}
+        for wid in (int(x) for x in args.extra.split(",") if x.strip()):
+            if wid != args.workload:
+                extra[f"workload_{wid}"] = extra_workload(wid, max(1, min(args.steps, args.extra_steps)),
+                                                          max(3, min(args.warmup, 3)), dev, world, peak,
+                                                          args.no_clocks or rank != 0)
 
     if rank != 0:
         if world > 1:
@@ -415,13 +500,23 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the host cores' baseline belongs to the 1-GPU line
         cpu = cpu_oracle(wl, args.cpu_seconds, steps=None)
+        cpu["cpu_model"] = cpu_model()
+        if not args.elements:
+            # the other workloads: one thread on the tiny and clip-edge shards, every
+            # core on bounded samples of the two other large shards
+            by = {}
+            for wid, th in ((1, 1), (5, 1), (3, None), (4, None)):
+                r = cpu_oracle(workloads.workload(wid), max(2.0, args.cpu_seconds / 5), steps=None, threads=th)
+                by[f"workload_{wid}"] = {k: r[k] for k in ("value", "unit", "cores", "sample", "seconds",
+                                                            "generation_seconds")}
+            cpu["by_workload"] = by
     traffic = profiled_traffic() if (args.workload == 2 and not args.elements) else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded counter-based bf16 grads ~N(0,1e-4) (Irwin-Hall), masters N(0,0.02)/LN 1/0",
-        "config": {"workload": wl.name, "elements": n, "tensors": len(wl.tensors), "groups": 2, "gas": G,
+        "config": {"workload": wl.name, "elements": n, "tensors": len(wl.tensors), "groups": groups_used(wl), "gas": G,
                    "mode": f"{wl.mode}; " + ("last micro-batch deferred into the fused step" if defer else "norm fused into last accumulate"),
                    "bytes_per_elem_per_step": sum(bpe.values()), "hbm_gbs_per_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
@@ -431,6 +526,7 @@ def run_ours(args):
         "kernels": kern,
         "norm_and_step": norm_and_step,
         "variants": variant,
+        "workloads": extra,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
@@ -454,7 +550,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
     processes on one machine."""
     import torch
 
-    from mixed_precision_optimizer_bf16_gb300.optimizer import fast_pinned_buffers
+    from host_buffers import fast_pinned_buffers
     # One pinned buffer per micro-batch, unless that (on every rank of the node)
     # would take more than half the host memory available: then micro-batches
     # share buffers round-robin -- every step still copies G full gradients.
@@ -538,21 +634,43 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
 
 # ------------------------------------------------------------ CPU oracle arm
 
-def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_oracle(wl, seconds, steps=1, warmup=0, threads=None):
     """The CPU oracle, as it stands, on a bounded contiguous sample of the
     workload: `steps` whole optimizer steps (GAS accumulates, norm, clip,
     AdamW per group) over S elements, S sized from a pilot to about `seconds`
     (at most 2^28 elements).  steps=None: as many whole steps over the largest
-    sample as fill about `seconds` (1 to 100)."""
+    sample as fill about `seconds` (1 to 100).  The input generation is not
+    timed; its time is reported beside (`generation_seconds`)."""
     import numpy as np
 
     import oracle
     import synth
 
-    threads = oracle.nthreads()
+    threads = threads or oracle.nthreads()
     G = [oracle.group(*(float(np.float32(g[k])) for k in ("lr", "beta1", "beta2", "eps", "weight_decay")))
          for g in wl.groups]
-    off0 = wl.offsets[1] - (1 << 20) if len(wl.offsets) > 1 else 0
+    # a sample that starts 2^20 elements before the second tensor when there is
+    # room (on the scaled-BLOOM shard: the embedding's tail, then the first layers)
+    off0 = max(0, wl.offsets[1] - (1 << 20)) if len(wl.offsets) > 1 else 0
 
     def ranges_for(lo, hi):
         out = []
@@ -594,17 +712,20 @@ def cpu_oracle(wl, seconds, steps=1, warmup=0, return_line=False):
     per_elem = dt0 / S0
     S = int(min(max(seconds / (1 if auto else max(steps, 1)) / per_elem, S0), 1 << 28, wl.n - off0))
     S -= S % 4096
+    tg = time.perf_counter()
     p, gr = make(S)
+    gen_s = time.perf_counter() - tg
     if auto:   # one untimed step at the full sample size sets the step count
         steps = int(min(100, max(1, round(seconds / timed(S, p, gr, 1)))))
     if warmup:
         timed(S, p.copy(), gr, warmup)
     dt = timed(S, p, gr, steps)
     val = S * steps / dt
+    where = (f" (spans the end of {wl.tensors[0].name} and the tensors after it)" if off0 else "")
     return {"value": round(val, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{S} contiguous elements of the {wl.n}-element shard from element {off0} "
-                      f"(spans the embedding tail and the first layers, both groups), {steps} whole step(s) of "
-                      f"GAS {wl.gas}; input generation untimed", "seconds": round(dt, 3)}
+            "sample": f"{S} contiguous elements of the {wl.n}-element shard from element {off0}{where}, "
+                      f"{steps} whole step(s) of GAS {wl.gas}; input generation untimed", "seconds": round(dt, 3),
+            "generation_seconds": round(gen_s, 3)}
 
 
 def run_reference(args):

@@ -52,10 +52,11 @@
  *   accumulate(FIRST) ... accumulate(LAST) -> grad_norm -> step
  *   FIRST marks the first micro-batch (the accumulator is overwritten, not
  *   added to); LAST marks the last one (the norm's partial sums are fused
- *   into that pass).  FIRST|LAST is a single micro-batch.  grad_norm may also
- *   follow a non-LAST accumulate; it then reads the accumulator once more.
- *   Any micro-batch may carry BF16OPT_DEFER (see there); LAST|DEFER is the
- *   plain "fuse the last micro-batch into the step" case.
+ *   into that pass).  FIRST|LAST is a single micro-batch.  grad_norm (or
+ *   grad_norm_local) needs the LAST micro-batch: after FIRST without LAST it
+ *   returns BF16OPT_ERR_SEQUENCE.  Any micro-batch may carry BF16OPT_DEFER (see
+ *   there); LAST|DEFER is the plain "fuse the last micro-batch into the step"
+ *   case.
  */
 #ifndef BF16OPT_H
 #define BF16OPT_H
@@ -82,7 +83,7 @@ extern "C" {
  * changes.  bf16opt_abi_version() returns the value the library was built
  * with; code compiled against a header with another value must not use it.
  * No CUDA call; never fails. */
-#define BF16OPT_ABI_VERSION 1
+#define BF16OPT_ABI_VERSION 2
 int bf16opt_abi_version(void);
 
 /* ---- modes and flags --------------------------------------------------- */
@@ -195,26 +196,49 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
  * host_norm != NULL: waits for `stream` and stores the norm (FP64); returns
  * BF16OPT_WARN_NONFINITE if it is Inf or NaN (the caller decides whether to
  * call bf16opt_step; the library skips nothing unless bf16opt_set_skip_nonfinite
- * asked it to).  Errors: SEQUENCE (no completed accumulation), INVALID_ARG
- * (not a live handle), CUDA. */
+ * asked it to).  Errors: SEQUENCE (no completed accumulation FIRST ... LAST
+ * since the last step), INVALID_ARG (not a live handle), CUDA. */
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm);
 
 /* Multi-rank use.  Under ZeRO every rank owns one partition of the parameters
  * and the clipping norm is global over all of them ("BLOOM 176B 训练技术概览",
  * section 并行细节 / ZeRO: each GPU holds only its part; "企业官网建设流程全解析",
- * section 4.3: the global norm).  The exchange is one FP64 scalar per rank and
- * belongs to the caller's communication library:
+ * section 4.3: the global norm).  The exchange is one FP64 scalar per rank;
+ * moving it belongs to the caller's communication library, the arithmetic to
+ * this one:
  *   1. bf16opt_grad_norm_local: in place of bf16opt_grad_norm, finishes this
  *      rank's sum of squares, waits for `stream` and stores it in *local_sumsq;
- *   2. the caller gathers every rank's value and sums them in rank order (the
- *      same order on every rank, so every rank clips by the same bits);
- *   3. bf16opt_set_global_sumsq: turns that sum into the norm and clip
- *      coefficient on the device (enqueued on `stream`); bf16opt_step follows.
- * Sequence: local needs a completed accumulation (as grad_norm); set_global
- * needs local.  Errors: INVALID_ARG (NULL pointer), SEQUENCE (out of order),
- * CUDA.  A non-finite local or global sum is passed through unchanged and
- * reported as BF16OPT_WARN_NONFINITE (the caller decides whether to step). */
+ *   2. the caller gathers every rank's value into an array in rank order
+ *      (an all-gather);
+ *   3. bf16opt_set_rank_sumsqs: sums that array in rank order (FP64, rank 0
+ *      first: every rank gets the same bits, so every rank clips alike) and
+ *      turns the sum into the norm and clip coefficient on the device
+ *      (enqueued on `stream`); bf16opt_step follows.
+ * Sequence: local needs a completed accumulation (as grad_norm); set_rank
+ * and set_global need local.  A non-finite local or global sum is passed
+ * through unchanged and reported as BF16OPT_WARN_NONFINITE (the caller decides
+ * whether to step). */
 int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq);
+
+/* per_rank: HOST array of the n_ranks gathered local sums, in rank order;
+ * rank: this handle's rank, whose entry must equal, bit for bit, the value
+ * bf16opt_grad_norm_local returned (a gather that put the values out of order
+ * is refused).  global_norm: NULL, or receives sqrt of the rank-ordered sum
+ * (no synchronisation).  Errors: INVALID_ARG (not a live handle, NULL
+ * per_rank, n_ranks == 0, rank >= n_ranks, per_rank[rank] not this rank's
+ * value), SEQUENCE (no grad_norm_local since the accumulation), CUDA. */
+int bf16opt_set_rank_sumsqs(bf16opt_t *h, const double *per_rank, uint32_t n_ranks, uint32_t rank, void *stream,
+                            double *global_norm);
+
+/* The rank-ordered sum that bf16opt_set_rank_sumsqs uses:
+ * *global_sumsq = ((per_rank[0] + per_rank[1]) + ...) + per_rank[n_ranks-1]
+ * in FP64.  Host-only; needs no device or handle.  Errors: INVALID_ARG (NULL
+ * pointer, n_ranks == 0). */
+int bf16opt_sum_rank_sumsqs(const double *per_rank, uint32_t n_ranks, double *global_sumsq);
+
+/* For callers that reduce the sums themselves: sets the norm and clip
+ * coefficient from an already summed global_sumsq (enqueued on `stream`).
+ * Every rank must pass the same bits.  Errors as bf16opt_set_rank_sumsqs. */
 int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream);
 
 /* CUDA graphs.  The step counter, the hyper-parameters and the LR schedule
@@ -306,8 +330,13 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t);
  * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard (whose
  * master buffer has the accumulator's offset modulo 128 bytes), and the
  * clip coefficient c = max_grad_norm / norm if norm > max_grad_norm (> 0),
- * else 1.  `out` is device-accessible memory owned by the caller; the result
- * is written there on `stream` (nothing is synchronised).
+ * else 1.  `out` is owned by the caller; the result is written there on
+ * `stream` (nothing is synchronised).  `out` and `grad_accum` must be memory
+ * the current device can use: its own device memory, managed memory, or
+ * page-locked host memory (cudaMallocHost / cudaHostRegister, used through
+ * its mapped device address); anything else (pageable host memory, another
+ * device's memory) is refused with BF16OPT_ERR_INVALID_ARG before any work is
+ * enqueued.
  *
  * Scratch: one FP64 partial per chunk of up to 32,768 elements, kept in a file-scope
  * device array of 65,536 entries (512 KiB) that every GPU loading this
@@ -317,13 +346,15 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t);
  * partials it later reads, so nothing has to start at zero.  All calls on a
  * device share that one array: calls whose work overlaps on the GPU (e.g. on
  * two streams without ordering between them) race and give wrong results.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Errors: INVALID_ARG (NULL pointers, n too large,
- * non-finite or zero grad_scale, non-finite max_grad_norm), ALIGNMENT
- * (grad_accum not 4-B aligned, out not 8-B aligned), UNSUPPORTED (no device),
- * CUDA (symbol lookup or launch failed); bf16opt_last_error(NULL) has the
- * message. */
+ * The array's device address belongs to the context that loaded the library's
+ * kernels: the first call on each device, and the first call after that
+ * device's context was reset (cudaDeviceReset), looks it up
+ * (cudaGetSymbolAddress) with the device current; make those calls before any
+ * stream capture.  Errors: INVALID_ARG (NULL pointers, n too large,
+ * non-finite or zero grad_scale, non-finite max_grad_norm, memory the device
+ * cannot use), ALIGNMENT (grad_accum not 4-B aligned, out not 8-B aligned),
+ * UNSUPPORTED (no device), CUDA (symbol lookup or launch failed);
+ * bf16opt_last_error(NULL) has the message. */
 #define BF16OPT_STATIC_NORM_MAX_ELEMS (((uint64_t)1) << 30)
 
 typedef struct {

@@ -65,10 +65,11 @@ class bf16opt_norm_result_t(ctypes.Structure):
 EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
-           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_skip_nonfinite",
-           "bf16opt_debug_faults", "bf16opt_abi_version")
+           "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_rank_sumsqs",
+           "bf16opt_sum_rank_sumsqs", "bf16opt_set_skip_nonfinite", "bf16opt_debug_faults",
+           "bf16opt_abi_version")
 
-ABI_VERSION = 1   # BF16OPT_ABI_VERSION of the header these declarations mirror
+ABI_VERSION = 2   # BF16OPT_ABI_VERSION of the header these declarations mirror
 
 _lib = None
 
@@ -116,6 +117,11 @@ def load(path=None):
     L.bf16opt_grad_norm_local.argtypes = [hp, c_vp, ctypes.POINTER(ctypes.c_double)]
     L.bf16opt_set_global_sumsq.restype = ctypes.c_int
     L.bf16opt_set_global_sumsq.argtypes = [hp, ctypes.c_double, c_vp]
+    L.bf16opt_set_rank_sumsqs.restype = ctypes.c_int
+    L.bf16opt_set_rank_sumsqs.argtypes = [hp, ctypes.POINTER(ctypes.c_double), c_u32, c_u32, c_vp,
+                                          ctypes.POINTER(ctypes.c_double)]
+    L.bf16opt_sum_rank_sumsqs.restype = ctypes.c_int
+    L.bf16opt_sum_rank_sumsqs.argtypes = [ctypes.POINTER(ctypes.c_double), c_u32, ctypes.POINTER(ctypes.c_double)]
     L.bf16opt_set_skip_nonfinite.restype = ctypes.c_int
     L.bf16opt_set_skip_nonfinite.argtypes = [hp, ctypes.c_int]
     L.bf16opt_debug_faults.restype = ctypes.c_int
@@ -184,6 +190,23 @@ def bf16opt_grad_norm_local(h, stream=0):
 
 def bf16opt_set_global_sumsq(h, global_sumsq, stream=0):
     return load().bf16opt_set_global_sumsq(h, float(global_sumsq), c_vp(int(stream)) if stream else None)
+
+
+def bf16opt_set_rank_sumsqs(h, per_rank, rank, stream=0):
+    """per_rank: every rank's local sum of squares, in rank order.  Returns (status, global norm)."""
+    arr = (ctypes.c_double * max(1, len(per_rank)))(*[float(x) for x in per_rank])
+    norm = ctypes.c_double(0.0)
+    rc = load().bf16opt_set_rank_sumsqs(h, arr if len(per_rank) else None, len(per_rank), int(rank),
+                                        c_vp(int(stream)) if stream else None, ctypes.byref(norm))
+    return rc, norm.value
+
+
+def bf16opt_sum_rank_sumsqs(per_rank):
+    """Returns (status, the rank-ordered FP64 sum)."""
+    arr = (ctypes.c_double * max(1, len(per_rank)))(*[float(x) for x in per_rank])
+    out = ctypes.c_double(0.0)
+    rc = load().bf16opt_sum_rank_sumsqs(arr if len(per_rank) else None, len(per_rank), ctypes.byref(out))
+    return rc, out.value
 
 
 def bf16opt_set_skip_nonfinite(h, enable):

@@ -17,6 +17,7 @@
 #include <mutex>
 #include <unordered_set>
 
+#include <cuda.h>   // driver types only (CUcontext, CUresult); no libcuda link
 #include <nvtx3/nvToolsExt.h>
 
 #include "../../include/bf16opt.h"
@@ -55,7 +56,7 @@ struct bf16opt {
     float gscale = 1.0f;
     State state = S_IDLE;
     bool acc_valid = false;              // acc holds the fold of the micro-batches folded so far
-    bool partials_ready = false;
+    double local_sumsq = 0.0;            // this partition's sum of squares, as grad_norm_local returned it
     // Deferred micro-batches not yet folded into acc, in micro-batch order:
     // FLAT one pointer each, LIST one pointer per tensor each.
     std::vector<const uint16_t *> pend_flat;
@@ -233,7 +234,7 @@ int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
 template <bool WRITE, bool NORM>
 int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st) {
     switch (kmax_for(fs.count())) {
-    case 0: return launch_accum_k<true, 0, false, true>(h, fs, st);   // norm over the stored acc
+    case 0: return fail(h, BF16OPT_ERR_INVALID_ARG, "internal: an accumulate pass without a gradient");
     case 1: return has_acc ? launch_accum_k<true, 1, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 1, WRITE, NORM>(h, fs, st);
     case 4: return has_acc ? launch_accum_k<true, 4, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 4, WRITE, NORM>(h, fs, st);
     default: return has_acc ? launch_accum_k<true, 8, WRITE, NORM>(h, fs, st) : launch_accum_k<false, 8, WRITE, NORM>(h, fs, st);
@@ -621,33 +622,22 @@ int bf16opt_accumulate(bf16opt_t *h, const uint16_t *grad_flat, const uint16_t *
         h->pend_flat = std::move(pf);
         h->pend_list = std::move(pl);
     }
-    if (!last) {
-        h->state = S_ACC;
-        h->partials_ready = false;
-    } else {
-        h->state = defer ? S_ACC_DEFERRED : S_ACC_DONE;
-        h->partials_ready = true;
-    }
+    h->state = !last ? S_ACC : (defer ? S_ACC_DEFERRED : S_ACC_DONE);
     return BF16OPT_OK;
 }
 
 int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
     NvtxRange nvtx("bf16opt_grad_norm");
     if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
-    if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
-        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm needs a completed accumulation");
+    if (h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
+        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm needs a completed accumulation (FIRST ... LAST)");
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
-    if (!h->partials_ready) {
-        // norm of fold(acc, pending) without storing it; the step folds the same set
-        int rc = launch_accum<false, true>(h, h->acc_valid, pending_set(h), st);
-        if (rc) return rc;
-    }
+    // the chunk partials were written by the LAST pass
     k_norm_final<<<1, kFinalThreads, 0, st>>>(h->partials_d, h->n_chunks, h->max_norm, h->norm_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");
-    h->partials_ready = true;
     h->state = S_NORMED;
     if (host_norm) {
         double nrm = 0.0;
@@ -667,8 +657,8 @@ int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
     NvtxRange nvtx("bf16opt_grad_norm_local");
     if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
     if (!local_sumsq) return fail(h, BF16OPT_ERR_INVALID_ARG, "grad_norm_local: local_sumsq is NULL");
-    if (h->state != S_ACC && h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
-        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm_local needs a completed accumulation");
+    if (h->state != S_ACC_DONE && h->state != S_ACC_DEFERRED)
+        return fail(h, BF16OPT_ERR_SEQUENCE, "grad_norm_local needs a completed accumulation (FIRST ... LAST)");
     double nrm = 0.0;
     int rc = bf16opt_grad_norm(h, stream, &nrm);
     if (rc < 0) return rc;
@@ -678,6 +668,7 @@ int bf16opt_grad_norm_local(bf16opt_t *h, void *stream, double *local_sumsq) {
     if ((e = cudaMemcpy(&S, &h->norm_d->sumsq, sizeof(double), cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(h, e, "reading the local sum of squares");
     *local_sumsq = S;
+    h->local_sumsq = S;
     h->state = S_LOCAL_NORMED;
     return BF16OPT_OK;
 }
@@ -697,6 +688,36 @@ int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
         return BF16OPT_WARN_NONFINITE;
     }
     return BF16OPT_OK;
+}
+
+int bf16opt_sum_rank_sumsqs(const double *per_rank, uint32_t n_ranks, double *global_sumsq) {
+    if (!per_rank || !global_sumsq || n_ranks == 0) return BF16OPT_ERR_INVALID_ARG;
+    // one FP64 add per rank, rank 0 first: every rank that sums the same
+    // gathered values gets the same bits
+    double S = 0.0;
+    for (uint32_t r = 0; r < n_ranks; ++r) S += per_rank[r];
+    *global_sumsq = S;
+    return BF16OPT_OK;
+}
+
+int bf16opt_set_rank_sumsqs(bf16opt_t *h, const double *per_rank, uint32_t n_ranks, uint32_t rank, void *stream,
+                            double *global_norm) {
+    NvtxRange nvtx("bf16opt_set_rank_sumsqs");
+    if (!live(h)) return BF16OPT_ERR_INVALID_ARG;
+    if (!per_rank || n_ranks == 0 || rank >= n_ranks)
+        return fail(h, BF16OPT_ERR_INVALID_ARG, "set_rank_sumsqs: need per_rank[n_ranks], n_ranks >= 1, rank < n_ranks");
+    if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_rank_sumsqs needs grad_norm_local first");
+    // this rank's entry must be the value grad_norm_local handed out: a gather
+    // that placed the values out of rank order is caught here
+    if (std::memcmp(&per_rank[rank], &h->local_sumsq, sizeof(double)) != 0)
+        return fail(h, BF16OPT_ERR_INVALID_ARG,
+                    "set_rank_sumsqs: per_rank[rank] is not this partition's sum of squares (gathered out of order?)");
+    double S = 0.0;
+    bf16opt_sum_rank_sumsqs(per_rank, n_ranks, &S);
+    int rc = bf16opt_set_global_sumsq(h, S, stream);
+    if (rc < 0) return rc;
+    if (global_norm) *global_norm = std::sqrt(S);
+    return rc;
 }
 
 int bf16opt_lr_factor(const bf16opt_lr_schedule_t *s, int64_t t, double *factor) {
@@ -772,7 +793,6 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     h->acc_valid = false;
     h->pend_flat.clear();
     h->pend_list.clear();
-    h->partials_ready = false;
     return BF16OPT_OK;
 }
 
@@ -792,8 +812,6 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
 // loads this library and stays allocated until the process exits.
 // ---------------------------------------------------------------------------
 
-#include <mutex>
-
 namespace {
 
 constexpr uint32_t kStaticMaxChunks = 65536;  // 512 KiB of FP64 partials
@@ -803,25 +821,91 @@ static_assert((BF16OPT_STATIC_NORM_MAX_ELEMS + kHeadAlign - 1 + kChunk - 1) / kC
 
 static __device__ __align__(256) double g_static_partials[kStaticMaxChunks];
 
-std::mutex g_static_mu;
-double *g_static_ptr[kStaticMaxDevices] = {};
+// The array's device address depends on the context that loaded this module:
+// after cudaDeviceReset (or a reset of the primary context) the next context
+// loads it again, possibly elsewhere.  The address is therefore cached per
+// device together with the id of the context it was looked up in (context ids
+// are never reused within a process, unlike context handles) and looked up
+// again when the current context's id differs.  The two driver calls are
+// fetched through the runtime, so the library does not link libcuda.
+struct DriverCtx {
+    CUresult (*get_current)(CUcontext *) = nullptr;
+    CUresult (*get_id)(CUcontext, unsigned long long *) = nullptr;
+};
 
-// Device address of g_static_partials on device `dev` (the current device),
-// looked up once per device.  In host code the array's name is only a host
+const DriverCtx &driver_ctx() {
+    static const DriverCtx d = [] {
+        DriverCtx r;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            r.get_current = reinterpret_cast<CUresult (*)(CUcontext *)>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            r.get_id = reinterpret_cast<CUresult (*)(CUcontext, unsigned long long *)>(p);
+        cudaGetLastError();
+        return r;
+    }();
+    return d;
+}
+
+// Id of the current context; 0 when there is none yet or it cannot be read.
+unsigned long long current_ctx_id() {
+    const DriverCtx &d = driver_ctx();
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!d.get_current || !d.get_id || d.get_current(&c) != CUDA_SUCCESS || !c || d.get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+struct StaticSlot {
+    unsigned long long ctx_id;
+    double *ptr;
+};
+std::mutex g_static_mu;
+StaticSlot g_static_slot[kStaticMaxDevices] = {};
+
+// Device address of g_static_partials in the current context of device `dev`
+// (the current device).  In host code the array's name is only a host-side
 // stand-in, so the kernels must be given this address.
 int static_scratch(int dev, double **out, std::string &msg) {
+    const unsigned long long id = current_ctx_id();
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    StaticSlot &sl = g_static_slot[dev];
+    if (!sl.ptr || id == 0 || sl.ctx_id != id) {
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_static_partials);
         if (e != cudaSuccess || !p) {
+            cudaGetLastError();
             msg = std::string("cudaGetSymbolAddress of the static norm scratch failed: ") + cudaGetErrorString(e);
             return BF16OPT_ERR_CUDA;
         }
-        g_static_ptr[dev] = static_cast<double *>(p);
+        sl.ptr = static_cast<double *>(p);
+        sl.ctx_id = current_ctx_id();   // the lookup makes the primary context current if it was not
     }
-    *out = g_static_ptr[dev];
+    *out = sl.ptr;
     return BF16OPT_OK;
+}
+
+// Address under which the kernels on device `dev` may use `p`: device memory
+// of that device or managed memory as is, page-locked host memory through its
+// mapped device address.  Anything else -- pageable host memory, another
+// device's memory, an unknown pointer -- gives nullptr.
+void *device_view(const void *p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice: return a.device == dev ? const_cast<void *>(p) : nullptr;
+    case cudaMemoryTypeManaged: return const_cast<void *>(p);
+    case cudaMemoryTypeHost: return a.devicePointer;
+    default: return nullptr;
+    }
 }
 
 // Partial sums of squares of implicit chunks (sized and cut as in the handle's chunk table) of
@@ -881,26 +965,17 @@ k_static_partials(const float *__restrict__ acc, uint64_t n, uint32_t nchunks, u
     }
 }
 
-// Fixed-order sum of the partials, norm and clip coefficient into the caller's result.
+// Fixed-order sum of the partials, norm and clip coefficient into the
+// caller's result: the same helpers as the handle's k_norm_final.
 __global__ void __launch_bounds__(kFinalThreads)
 k_static_final(const double *__restrict__ partials, uint32_t n, float max_norm, bf16opt_norm_result_t *out) {
     __shared__ double sh[kFinalThreads];
-    double s = 0.0;
-    for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) s += partials[i];
-    sh[threadIdx.x] = s;
-    __syncthreads();
-    for (int w = kFinalThreads / 2; w > 0; w >>= 1) {
-        if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
-        __syncthreads();
-    }
+    const double S = final_sum(partials, n, sh);
     if (threadIdx.x == 0) {
-        const double S = sh[0];
-        const double norm = sqrt(S);
-        double c = 1.0;
-        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
-        out->sumsq = S;
-        out->norm = norm;
-        out->clip_coef = c;
+        const NormClip r = norm_and_clip(S, max_norm);
+        out->sumsq = r.sumsq;
+        out->norm = r.norm;
+        out->clip_coef = r.c;
     }
 }
 
@@ -919,27 +994,36 @@ extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, flo
     if (mis4(grad_accum)) return fail(nullptr, BF16OPT_ERR_ALIGNMENT, "grad_norm_static: grad_accum must be 4-B aligned");
     if (!finite_f(grad_scale) || grad_scale == 0.f || !finite_f(max_grad_norm))
         return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "grad_norm_static: grad_scale and max_grad_norm must be finite, grad_scale != 0");
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    int dev = 0, ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1 || cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "grad_norm_static: no CUDA device");
     }
     if (dev < 0 || dev >= kStaticMaxDevices) return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "grad_norm_static: device ordinal too large");
+    // The kernels write `out` and read `grad_accum` directly: both must be
+    // memory the device can use (checked here; a pageable host pointer would
+    // otherwise fault inside the kernel instead of returning an error).
+    auto *out_d = static_cast<bf16opt_norm_result_t *>(device_view(out, dev));
+    if (!out_d) return fail(nullptr, BF16OPT_ERR_INVALID_ARG,
+                            "grad_norm_static: out must be device, managed or page-locked host memory of the current device");
+    const float *acc_d = nullptr;
+    if (n > 0 && !(acc_d = static_cast<const float *>(device_view(grad_accum, dev))))
+        return fail(nullptr, BF16OPT_ERR_INVALID_ARG,
+                    "grad_norm_static: grad_accum must be device, managed or page-locked host memory of the current device");
     double *partials = nullptr;
     std::string msg;
     int rc = static_scratch(dev, &partials, msg);
     if (rc) return fail(nullptr, rc, msg);
     int sms = 1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
-    const uint32_t chunk = chunk_elems(n), cut = first_chunk_cut(grad_accum);
+    const uint32_t chunk = chunk_elems(n), cut = first_chunk_cut(acc_d);
     const uint32_t nchunks = n == 0 ? 0u : (uint32_t)((n + cut + chunk - 1) / chunk);
     cudaStream_t st = (cudaStream_t)stream;
     if (nchunks > 0) {
         const uint32_t grid = std::min<uint32_t>(nchunks, (uint32_t)sms * 8u);
-        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(grad_accum, n, nchunks, chunk, cut, grad_scale,
-                                                                   partials);
+        k_static_partials<BF16K_ACC_U><<<grid, kThreads, 0, st>>>(acc_d, n, nchunks, chunk, cut, grad_scale, partials);
     }
-    k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out);
+    k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "grad_norm_static kernel launch");
     return BF16OPT_OK;

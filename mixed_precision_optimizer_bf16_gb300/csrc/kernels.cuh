@@ -454,11 +454,11 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
 
 // ---------------------------------------------------------------- norm final
 
-// Sum of the chunk partials in a fixed order, then norm = sqrt(S) and
-// c = max_norm / norm if norm > max_norm (max_norm > 0), else 1.
-__global__ void __launch_bounds__(kFinalThreads)
-k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out) {
-    __shared__ double sh[kFinalThreads];
+// Fixed-order FP64 sum of n partials by one CTA of kFinalThreads threads:
+// thread i adds partials i, i + kFinalThreads, ... in index order, then a
+// halving tree over the threads.  The order depends only on n, so every call
+// over the same partials gives the same bits.  Result valid in thread 0.
+__device__ __forceinline__ double final_sum(const double *__restrict__ partials, uint32_t n, double *sh) {
     double s = 0.0;
     for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) s += partials[i];
     sh[threadIdx.x] = s;
@@ -467,36 +467,47 @@ k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, No
         if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        const double S = sh[0];
-        const double norm = sqrt(S);
-        double c = 1.0;
-        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
-        const float hi = __double2float_rn(c);
-        out->sumsq = S;
-        out->norm = norm;
-        out->c_hi = hi;
-        out->c_lo = __double2float_rn(c - (double)hi);
-        out->finite = isfinite(S) ? 1 : 0;
-        out->pad = 0;
-    }
+    return sh[0];
+}
+
+// norm = sqrt(S) and the clip coefficient c = max_norm / norm if norm >
+// max_norm (max_norm > 0), else exactly 1 ("企业官网建设流程全解析", section 4.3).
+struct NormClip {
+    double sumsq, norm, c;
+};
+__device__ __forceinline__ NormClip norm_and_clip(double S, float max_norm) {
+    NormClip r;
+    r.sumsq = S;
+    r.norm = sqrt(S);
+    r.c = 1.0;
+    if (max_norm > 0.0f && r.norm > (double)max_norm) r.c = (double)max_norm / r.norm;
+    return r;
+}
+
+// The handle's norm state from a norm and clip coefficient: c kept as a
+// float-float pair so that acc * c is rounded once in the step.
+__device__ __forceinline__ void store_norm_state(const NormClip &r, NormState *__restrict__ out) {
+    const float hi = __double2float_rn(r.c);
+    out->sumsq = r.sumsq;
+    out->norm = r.norm;
+    out->c_hi = hi;
+    out->c_lo = __double2float_rn(r.c - (double)hi);
+    out->finite = isfinite(r.sumsq) ? 1 : 0;
+    out->pad = 0;
+}
+
+// Sum of the chunk partials in a fixed order, then norm and clip coefficient.
+__global__ void __launch_bounds__(kFinalThreads)
+k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out) {
+    __shared__ double sh[kFinalThreads];
+    const double S = final_sum(partials, n, sh);
+    if (threadIdx.x == 0) store_norm_state(norm_and_clip(S, max_norm), out);
 }
 
 // Norm and clip coefficient from a sum of squares given by the host (the
 // all-rank sum under ZeRO): same formula as k_norm_final.
 __global__ void k_norm_from_sumsq(double S, float max_norm, NormState *__restrict__ out) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) {
-        const double norm = sqrt(S);
-        double c = 1.0;
-        if (max_norm > 0.0f && norm > (double)max_norm) c = (double)max_norm / norm;
-        const float hi = __double2float_rn(c);
-        out->sumsq = S;
-        out->norm = norm;
-        out->c_hi = hi;
-        out->c_lo = __double2float_rn(c - (double)hi);
-        out->finite = isfinite(S) ? 1 : 0;
-        out->pad = 0;
-    }
+    if (threadIdx.x == 0 && blockIdx.x == 0) store_norm_state(norm_and_clip(S, max_norm), out);
 }
 
 // t <- t + 1 and the per-group FP32 scalars of step t, computed in FP64 from

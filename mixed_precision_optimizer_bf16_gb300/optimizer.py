@@ -8,10 +8,7 @@ arithmetic is in libbf16opt.so.  State layout for one rank's shard:
   LIST: the same five buffers per tensor (separate allocations).
 """
 import contextlib
-import ctypes
-import mmap
 
-import numpy as np
 import torch
 
 from . import bf16opt as C
@@ -63,130 +60,6 @@ def alloc_flat(n, device="cuda", misalign=0):
                 grad_accum=one(torch.float32), param_bf16=one(torch.int16))
 
 
-def _thp_size():
-    """Size of a transparent huge page (512 MiB on 64 KiB-page Arm kernels, 2 MiB on 4 KiB ones)."""
-    try:
-        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
-            return int(f.read().strip())
-    except (OSError, ValueError):
-        return 2 << 20
-
-
-def _huge_fraction(start, nbytes):
-    """Fraction of [start, start + nbytes) backed by transparent huge pages (from /proc/self/smaps)."""
-    try:
-        huge, lo, hi = 0, None, None
-        with open("/proc/self/smaps") as f:
-            for line in f:
-                head = line.split()[0]
-                if "-" in head and ":" not in head:
-                    lo, hi = (int(x, 16) for x in head.split("-"))
-                elif head == "AnonHugePages:" and lo is not None and lo <= start < hi:
-                    huge = int(line.split()[1]) * 1024
-        return huge / nbytes if nbytes else 1.0
-    except (OSError, ValueError):
-        return 0.0
-
-
-class PinnedHostBuffer:
-    """Page-locked host memory for gradients that stream to the GPU.
-
-    The region is aligned to the transparent-huge-page size and rounded up to
-    whole huge pages, advised as huge (MADV_HUGEPAGE), faulted in and registered
-    with cudaHostRegister.  Large pages keep the address translations of the
-    host-to-device copies few: on a host whose memory is fragmented by earlier
-    large jobs, small-page pinned buffers slowed copies that overlap HBM-bound
-    kernels by almost 2x, huge-page ones far less.  Whole huge pages leave no
-    small-page tail, which the kernel's background collapse (khugepaged) would
-    keep trying, and failing, to merge while it is pinned.  `tensor` is a CPU
-    tensor over the first numel elements (is_pinned()).  Falls back to the
-    driver's pinned allocator (torch pin_memory) when the kernel cannot back at
-    least 90 % of the region with huge pages (small-page registered memory was
-    measured slower still) or registration is refused.
-    """
-
-    MADV_HUGEPAGE = 14
-
-    def __init__(self, numel, dtype=torch.int16):
-        itemsize = torch.empty(0, dtype=dtype).element_size()
-        nbytes = int(numel) * itemsize
-        self._registered = None
-        self.huge_fraction = 0.0
-        try:
-            align = _thp_size()
-            span = max(align, (nbytes + align - 1) // align * align)          # whole huge pages
-            self._map = mmap.mmap(-1, span + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-            addr = ctypes.addressof(ctypes.c_char.from_buffer(self._map))
-            start = (addr + align - 1) & ~(align - 1)
-            libc = ctypes.CDLL(None, use_errno=True)
-            libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
-            libc.madvise(ctypes.c_void_p(start), span, self.MADV_HUGEPAGE)     # advisory
-            whole = np.frombuffer(self._map, dtype=np.uint8, count=span, offset=start - addr)
-            whole[:] = 0                                                        # fault every page in now
-            self.huge_fraction = _huge_fraction(start, span)
-            if self.huge_fraction < 0.9:
-                raise RuntimeError("not backed by huge pages")
-            if int(torch.cuda.cudart().cudaHostRegister(start, span, 0)) != 0:
-                raise RuntimeError("cudaHostRegister refused")
-            self._registered = start
-            self.tensor = torch.from_numpy(whole[:nbytes]).view(dtype)
-            self.huge_pages = True
-        except Exception:
-            self._map = None
-            self.tensor = torch.empty(int(numel), dtype=dtype, pin_memory=True)
-            self.huge_pages = False
-
-    def close(self):
-        """Unregister the region (the tensor must not be used afterwards)."""
-        if self._registered is not None:
-            torch.cuda.synchronize()
-            torch.cuda.cudart().cudaHostUnregister(self._registered)
-            self._registered = None
-        self.tensor = None
-
-
-def _h2d_gbs(src, dst, reps=2):
-    """Best host-to-device copy rate (GB/s) of pinned `src` into device `dst`
-    over `reps` whole-buffer copies on a side stream (the first may pay for
-    lazy mappings)."""
-    s = torch.cuda.Stream(dst.device)
-    best = 0.0
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            e0.record(s)
-            dst[:src.numel()].copy_(src, non_blocking=True)
-            e1.record(s)
-        e1.synchronize()
-        best = max(best, src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9)
-    return best
-
-
-def fast_pinned_buffers(numel, count, dst, dtype=torch.int16, min_gbs=150.0, max_extra=12):
-    """`count` PinnedHostBuffers of `numel` elements chosen by their measured
-    host-to-device copy rate into the device tensor `dst` (at least numel
-    elements; its contents are overwritten).  On a virtual machine the DMA rate
-    of pinned host memory depends on how the hypervisor backs each region:
-    3.4 GB buffers pinned side by side in one process copied at 211 GB/s or at
-    12-136 GB/s.  A buffer below `min_gbs` is kept aside (so its memory is not
-    handed out again at once) and another is pinned, up to `max_extra` extra
-    buffers; the fastest `count` are kept and the rest freed.
-    Returns (buffers, their rates in GB/s, number rejected)."""
-    got, tries = [], 0
-    while True:
-        hb = PinnedHostBuffer(numel, dtype)
-        got.append((_h2d_gbs(hb.tensor, dst), hb))
-        fast = sum(1 for r, _ in got if r >= min_gbs)
-        if fast >= count or len(got) >= count + max_extra:
-            break
-        tries += 1
-    got.sort(key=lambda x: -x[0])
-    keep, drop = got[:count], got[count:]
-    for _, hb in drop:
-        hb.close()
-    return [hb for _, hb in keep], [round(r, 1) for r, _ in keep], len(drop)
-
-
 def resident_pattern(gas, fold=8):
     """Per-micro-batch `defer` flags for a step whose micro-batch gradients all
     stay resident (one buffer each): all deferred when gas <= fold (the FP32
@@ -201,22 +74,19 @@ def resident_pattern(gas, fold=8):
     return [(k % fold) != fold - 1 for k in range(head)] + [True] * tail
 
 
-def global_sumsq(local, group=None):
-    """Sum of every rank's local sum of squares, in rank order (deterministic and
-    identical on all ranks); `local` when torch.distributed is not initialised."""
+def gather_sumsqs(local, group=None):
+    """Every rank's local sum of squares, in rank order (an all-gather of one
+    FP64 scalar per rank); [local] when torch.distributed is not initialised.
+    Only moves the values: the library sums them (bf16opt_set_rank_sumsqs)."""
     import torch.distributed as dist
     if not (dist.is_available() and dist.is_initialized()):
-        return float(local)
+        return [float(local)]
     world = dist.get_world_size(group)
-    backend = dist.get_backend(group)
-    dev = "cuda" if backend == "nccl" else "cpu"
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
     mine = torch.tensor([float(local)], dtype=torch.float64, device=dev)
     parts = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(parts, mine, group=group)
-    total = 0.0
-    for p in parts:
-        total += float(p.item())
-    return total
+    return [float(p.item()) for p in parts]
 
 
 class BF16Optimizer:
@@ -351,13 +221,17 @@ class BF16Optimizer:
 
     def grad_norm_distributed(self, group=None, stream=None):
         """Global norm over every rank's partition: this rank's FP64 sum of squares
-        is all-gathered and summed in rank order (identical on every rank), then
-        handed back to the library.  Returns the global norm."""
+        is all-gathered; the library sums the gathered values in rank order
+        (the same bits on every rank) and sets the norm and clip coefficient.
+        Returns the global norm the library computed."""
+        import torch.distributed as dist
         rc, local = C.bf16opt_grad_norm_local(self.h, _stream_handle(stream))
         C.check(rc, self.h)
-        total = global_sumsq(local, group)
-        C.check(C.bf16opt_set_global_sumsq(self.h, total, _stream_handle(stream)), self.h)
-        return total ** 0.5
+        parts = gather_sumsqs(local, group)
+        rank = dist.get_rank(group) if dist.is_available() and dist.is_initialized() else 0
+        rc, norm = C.bf16opt_set_rank_sumsqs(self.h, parts, rank, _stream_handle(stream))
+        C.check(rc, self.h)
+        return norm
 
     def set_skip_nonfinite(self, enable=True):
         """Skip (on the device) any step whose global norm is Inf or NaN."""

@@ -64,12 +64,12 @@ def _ptr(a):
     return ctypes.c_void_p(a.ctypes.data)
 
 
-def fill_grad(wl, step, micro, out, first=0):
+def fill_grad(wl, step, micro, out, first=0, threads=None):
     """out[j] = bf16 bits of gradient element first+j of (step, micro) of workload wl."""
     assert out.dtype == np.uint16 and out.flags.c_contiguous
     lib().synth_fill_grad_bf16(_ptr(out), out.size, first, key(wl.id, KIND_GRAD, step, micro),
                                sigma_scale(wl.grad_sigma), key(wl.id, KIND_ZERO_MASK),
-                               zero_thresh(wl.zero_frac), nthreads())
+                               zero_thresh(wl.zero_frac), threads or nthreads())
     return out
 
 
@@ -82,30 +82,30 @@ def gather_grad(wl, step, micro, idx):
     return out
 
 
-def _fill_tensor_master(wl, t, out, lo, hi, first):
+def _fill_tensor_master(wl, t, out, lo, hi, first, threads):
     """Fill out[lo-first : hi-first] with the initial masters of tensor t on [lo, hi)."""
     seg = out[lo - first:hi - first]
     kind = t.init[0]
     if kind == "normal":
         lib().synth_fill_normal_f32(_ptr(seg), seg.size, lo, key(wl.id, KIND_MASTER),
-                                    sigma_scale(t.init[1]), nthreads())
+                                    sigma_scale(t.init[1]), threads)
     elif kind == "const":
         seg[:] = np.float32(t.init[1])
     elif kind == "loguniform":
         lib().synth_fill_loguniform_f32(_ptr(seg), seg.size, lo, key(wl.id, KIND_MASTER),
-                                        t.init[1], t.init[2], nthreads())
+                                        t.init[1], t.init[2], threads)
     else:
         raise ValueError(kind)
 
 
-def fill_master(wl, out, first=0):
+def fill_master(wl, out, first=0, threads=None):
     """out[j] = initial FP32 master of element first+j of workload wl."""
     assert out.dtype == np.float32 and out.flags.c_contiguous
     end = first + out.size
     for t, off in zip(wl.tensors, wl.offsets):
         lo, hi = max(first, off), min(end, off + t.numel)
         if lo < hi:
-            _fill_tensor_master(wl, t, out, lo, hi, first)
+            _fill_tensor_master(wl, t, out, lo, hi, first, threads or nthreads())
     return out
 
 

@@ -63,16 +63,20 @@ def _gather_worker(rank, world, port, q):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
-    from mixed_precision_optimizer_bf16_gb300.optimizer import global_sumsq
+    from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
+    from mixed_precision_optimizer_bf16_gb300.optimizer import gather_sumsqs
     # values whose sum depends on the order: rank order must be used on every rank
     local = [1.0, 1e-16, -1.0][rank]
-    q.put((rank, global_sumsq(local)))
+    parts = gather_sumsqs(local)
+    rc, total = C.bf16opt_sum_rank_sumsqs(parts)
+    q.put((rank, parts, rc, total))
     dist.destroy_process_group()
 
 
 def test_global_sumsq_rank_order_gloo():
-    """Each rank's local sum of squares is all-gathered and summed in rank order,
-    so every rank clips with the same bits."""
+    """Each rank's local sum of squares is all-gathered in rank order and the
+    library sums the gathered values in that order, so every rank clips with
+    the same bits."""
     world = 3
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
@@ -85,7 +89,9 @@ def test_global_sumsq_rank_order_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     want = (1.0 + 1e-16) + -1.0          # = 0.0 in rank order (1 + 1e-16 rounds to 1)
-    assert [r[1] for r in res] == [want] * world
+    assert want == 0.0 and (1.0 + (1e-16 + -1.0)) != 0.0
+    assert [r[1] for r in res] == [[1.0, 1e-16, -1.0]] * world
+    assert [(r[2], r[3]) for r in res] == [(0, want)] * world
 
 
 def test_max_over_ranks_without_group():

@@ -229,6 +229,8 @@ def test_sequence_errors():
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, 8) == C.BF16OPT_ERR_INVALID_ARG   # unknown flag
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_FIRST) == 0
     assert C.bf16opt_step(h) == C.BF16OPT_ERR_SEQUENCE
+    assert C.bf16opt_grad_norm(h, 0, True)[0] == C.BF16OPT_ERR_SEQUENCE        # no LAST micro-batch yet
+    assert C.bf16opt_grad_norm_local(h)[0] == C.BF16OPT_ERR_SEQUENCE
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == 0
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == C.BF16OPT_ERR_SEQUENCE
     rc, nrm = C.bf16opt_grad_norm(h, 0, True)
@@ -446,11 +448,16 @@ def test_two_partitions_share_the_global_norm():
             rc, loc = C.bf16opt_grad_norm_local(o.h, torch.cuda.current_stream().cuda_stream)
             assert rc == 0
             locs.append(loc)
-        total = locs[0] + locs[1]
-        for o in opts:
-            assert C.bf16opt_set_global_sumsq(o.h, total, torch.cuda.current_stream().cuda_stream) == 0
+        got_norms = []
+        for r, o in enumerate(opts):
+            if locs[0] != locs[1]:   # values gathered out of rank order are refused
+                assert C.bf16opt_set_rank_sumsqs(o.h, locs[::-1], r)[0] == C.BF16OPT_ERR_INVALID_ARG
+            rc, nrm = C.bf16opt_set_rank_sumsqs(o.h, locs, r, torch.cuda.current_stream().cuda_stream)
+            assert rc == 0, C.bf16opt_last_error(o.h)
+            got_norms.append(nrm)
             o.step()
-        norms.append(total ** 0.5)
+        assert got_norms[0] == got_norms[1] == math.sqrt(locs[0] + locs[1])
+        norms.append(got_norms[0])
     torch.cuda.synchronize()
     got = dict(p=flat["master"].cpu().numpy(), m=flat["exp_avg"].cpu().numpy(),
                v=flat["exp_avg_sq"].cpu().numpy(), acc=flat["grad_accum"].cpu().numpy(),
@@ -573,7 +580,7 @@ def test_cuda_graph_replay_matches_eager(mode):
 
 @needs_cuda
 def test_pinned_host_buffer_round_trip():
-    from mixed_precision_optimizer_bf16_gb300.optimizer import PinnedHostBuffer
+    from host_buffers import PinnedHostBuffer
     hb = PinnedHostBuffer(5_000_003, torch.int16)
     assert hb.tensor.is_pinned() and hb.tensor.numel() == 5_000_003
     d = torch.randint(-30000, 30000, (5_000_003,), dtype=torch.int16, device="cuda")
@@ -738,23 +745,21 @@ def _big_gradient_workload():
 
 
 @needs_cuda
-@pytest.mark.parametrize("variant", ["stored_last", "defer_last", "all_deferred", "no_last_flag"])
+@pytest.mark.parametrize("variant", ["stored_last", "defer_last", "all_deferred"])
 def test_gradients_whose_squares_overflow_fp32(variant):
     """The definition's sum of squares is FP64, where 2.5e30 squared is an
     ordinary number: the norm must be finite and equal the oracle's, the clip
     must bring the gradient to norm 1, and the step must match element by
     element -- on every pass that computes the norm's partials (stored LAST,
-    deferred LAST, all deferred, and the norm pass over the stored acc)."""
+    deferred LAST, all deferred)."""
     import harness
     wl, grads = _big_gradient_workload()
-    pattern = {"stored_last": [False, False], "defer_last": [False, True], "all_deferred": [True, True],
-               "no_last_flag": [False, False]}[variant]
+    pattern = {"stored_last": [False, False], "defer_last": [False, True], "all_deferred": [True, True]}[variant]
     sh = GpuShard(wl, defer=pattern)
     for k in range(wl.gas):
         buf = sh.gbufs[k % len(sh.gbufs)]
         buf.copy_(torch.from_numpy(grads[k].view(np.int16)))
-        sh.opt.accumulate(sh.grads_arg(buf), first=k == 0,
-                          last=k == wl.gas - 1 and variant != "no_last_flag", defer=pattern[k])
+        sh.opt.accumulate(sh.grads_arg(buf), first=k == 0, last=k == wl.gas - 1, defer=pattern[k])
     norm = sh.opt.grad_norm(sync=True)
     sh.opt.step()
     torch.cuda.synchronize()
@@ -769,7 +774,7 @@ def test_gradients_whose_squares_overflow_fp32(variant):
     sc = {"M": np.zeros(wl.n), "A": np.abs(p0.astype(np.float64))}
     harness._update_scales(sc, wl, wl.group_of(np.arange(wl.n)), ref["acc"], ref["clip"][0], ref["m"], ref["v"],
                            1, 1.0)
-    compare(got, ref, sc, wl, check_acc=variant in ("stored_last", "no_last_flag"))
+    compare(got, ref, sc, wl, check_acc=variant == "stored_last")
 
 
 @needs_cuda
@@ -1050,7 +1055,7 @@ def test_two_handles_on_two_streams_interleaved():
 def test_fast_pinned_buffers():
     """Rate-selected pinned host buffers: the requested count, pinned, with a
     measured rate each, and data that round-trips."""
-    from mixed_precision_optimizer_bf16_gb300.optimizer import fast_pinned_buffers
+    from host_buffers import fast_pinned_buffers
     n = 5_000_003
     dst = torch.empty(n, dtype=torch.int16, device="cuda")
     bufs, rates, rejected = fast_pinned_buffers(n, 2, dst, max_extra=2)

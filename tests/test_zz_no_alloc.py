@@ -8,7 +8,6 @@ array.  This file is collected last so that a run stopping at its first
 failure has already run every other test; it must pass alone in a fresh
 process as well as after the other tests.
 """
-import ctypes
 import math
 
 import numpy as np
@@ -16,6 +15,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import oracle  # noqa: E402
 from mixed_precision_optimizer_bf16_gb300 import bf16opt as C  # noqa: E402
 from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat  # noqa: E402
 from synth import gpu as sgpu, workloads  # noqa: E402
@@ -32,6 +32,10 @@ def _read(res):
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
 def test_static_norm_matches_handle_norm_twice():
+    """Two calls in a row on the same accumulator give the handle's own sum of
+    squares bit for bit (the same chunking, thread map and fixed-order sums),
+    and the oracle's FP64 sum of squares of the copied-back accumulator within
+    the norm tolerance."""
     C.load()
     # 3,000,011 elements (ragged last chunk), misaligned by 1 element, clipping active
     wl = workloads.custom(199, [3_000_011], gas=2, steps=1, grad_sigma=0.05, misalign=1)
@@ -44,12 +48,15 @@ def test_static_norm_matches_handle_norm_twice():
     for k in range(2):
         sgpu.fill_grad(wl, 0, k, g)
         opt.accumulate(g, first=k == 0, last=k == 1)
-    ref_norm = opt.grad_norm(sync=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    rc, handle_sumsq = C.bf16opt_grad_norm_local(opt.h, stream)
+    assert rc == 0
+    acc = flat["grad_accum"]
+    ref_sumsq = oracle.sumsq(acc.cpu().numpy(), 0.5)
+    ref_norm = math.sqrt(ref_sumsq)
     assert ref_norm > 1.0  # clipping is active
 
     res = torch.zeros(3, dtype=torch.float64, device="cuda")   # caller-owned output
-    stream = torch.cuda.current_stream().cuda_stream
-    acc = flat["grad_accum"]
     outs = []
     for _ in range(2):  # two calls in a row share the static scratch
         rc = C.bf16opt_grad_norm_static(acc.data_ptr(), acc.numel(), 0.5, 1.0, res.data_ptr(), stream)
@@ -58,8 +65,10 @@ def test_static_norm_matches_handle_norm_twice():
         outs.append(_read(res))
         res.zero_()
     for sumsq, norm, clip in outs:
+        assert sumsq == handle_sumsq                        # the handle's reduction, bit for bit
+        assert norm == math.sqrt(handle_sumsq) and clip == 1.0 / norm
+        assert abs(sumsq - ref_sumsq) <= REL * ref_sumsq    # and the oracle's sum
         assert abs(norm - ref_norm) <= REL * ref_norm
-        assert abs(sumsq - ref_norm ** 2) <= 2 * REL * ref_norm ** 2
         assert abs(clip - 1.0 / ref_norm) <= REL / ref_norm
     assert outs[0] == outs[1]
 
@@ -68,7 +77,7 @@ def test_static_norm_matches_handle_norm_twice():
     rc = C.bf16opt_grad_norm_static(part.data_ptr(), part.numel(), 1.0, 1.0, res.data_ptr(), stream)
     assert rc == 0
     torch.cuda.synchronize()
-    s_small = float((part.double() ** 2).sum())
+    s_small = oracle.sumsq(part.cpu().numpy())
     assert abs(_read(res)[0] - s_small) <= REL * s_small
 
     # empty input and the size limit
@@ -80,6 +89,32 @@ def test_static_norm_matches_handle_norm_twice():
         C.BF16OPT_ERR_INVALID_ARG
     assert "exceeds" in C.bf16opt_last_error(None)
     opt.close()
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+def test_static_norm_refuses_memory_the_device_cannot_use():
+    """The kernels write `out` and read `grad_accum` directly, so ordinary
+    (pageable) host memory is refused with an error instead of being handed to
+    a kernel; page-locked host memory works through its mapped address."""
+    C.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    acc = torch.full((100_003,), 0.25, dtype=torch.float32, device="cuda")
+    res = torch.zeros(3, dtype=torch.float64, device="cuda")
+    host_out = np.zeros(3, np.float64)
+    host_acc = np.full(100_003, 0.25, np.float32)
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), acc.numel(), 1.0, 1.0, host_out.ctypes.data, stream) == \
+        C.BF16OPT_ERR_INVALID_ARG
+    assert "out must be" in C.bf16opt_last_error(None)
+    assert C.bf16opt_grad_norm_static(host_acc.ctypes.data, host_acc.size, 1.0, 1.0, res.data_ptr(), stream) == \
+        C.BF16OPT_ERR_INVALID_ARG
+    assert "grad_accum must be" in C.bf16opt_last_error(None)
+    assert host_out.tolist() == [0.0, 0.0, 0.0]
+    pinned = torch.zeros(3, dtype=torch.float64, pin_memory=True)
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), acc.numel(), 1.0, 1.0, pinned.data_ptr(), stream) == 0
+    assert C.bf16opt_grad_norm_static(acc.data_ptr(), acc.numel(), 1.0, 1.0, res.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    want = 100_003 * 0.0625
+    assert tuple(pinned.tolist()) == _read(res) and pinned[0].item() == want
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
@@ -103,6 +138,7 @@ def test_static_norm_of_values_whose_squares_overflow_fp32():
     torch.cuda.synchronize()
     sumsq, norm, clip = _read(res)
     ref = math.fsum(float(x) * float(x) for x in host.tolist())
+    assert abs(oracle.sumsq(host) - ref) <= 1e-15 * ref
     assert abs(sumsq - ref) <= REL * ref
     assert abs(norm - math.sqrt(ref)) <= REL * math.sqrt(ref)
     assert abs(clip - 1.0 / math.sqrt(ref)) <= REL / math.sqrt(ref)
