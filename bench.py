@@ -530,7 +530,10 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": K * (sum(1 for c in calls if c) + 3),
+        # per step: the accumulate passes that launch (a deferred non-last one
+        # launches nothing), the norm finish (which also prepares the step's
+        # scalars) and the fused step
+        "gpu_launches": K * (sum(1 for c in calls if c) + 2),
     }
     print(json.dumps(line))
     sys.stdout.flush()

@@ -67,6 +67,8 @@ struct bf16opt {
     std::vector<std::pair<const void *, int>> occ;  // resident CTAs per SM, per kernel (queried once)
     bool has_sched = false;
     bool skip_nonfinite = false;
+    bool pdl = true;                     // launch with programmatic stream serialization (BF16OPT_PDL=0: off)
+    bool scalars_ready = false;          // the norm kernel prepared this step's scalars (groups' own lr)
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
 };
@@ -174,6 +176,26 @@ int grid_for(bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
     return (int)std::max<uint64_t>(1, std::min<uint64_t>(g, nchunks));
 }
 
+// Launches `kernel` on `st`, with programmatic stream serialization unless
+// the handle has it switched off: the kernel may then be scheduled while its
+// predecessor drains, and waits on the device (griddepcontrol.wait) before
+// its first memory access -- see pdl_enter in kernels.cuh.
+template <class... KArgs, class... Args>
+cudaError_t launch(const bf16opt_t *h, void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                   Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = h->pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Gradients a pass folds: K micro-batches (FLAT: one pointer each; LIST: one
 // per tensor each), in micro-batch order.
 struct FoldSet {
@@ -220,13 +242,16 @@ int for_each_launch(bf16opt_t *h, const FoldSet &fs, F &&launch) {
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
 int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
     constexpr int U = KMAX <= 1 ? BF16K_ACC_U : (KMAX <= 4 ? BF16K_FOLD4_ACC_U : BF16K_FOLD8_ACC_U);
+    cudaError_t e = cudaSuccess;
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
-        k<<<grid_for(h, k, c1 - c0), kThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt, h->partials_d, h->gscale);
+        const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0), kThreads, st, (const Seg *)h->segs_d,
+                                      (const Chunk *)h->chunks_d, c0, c1, gt, h->partials_d, h->gscale);
+        if (e == cudaSuccess) e = e1;
     });
     if (rc) return rc;
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? 0 : cuda_fail(h, e, "accumulate kernel launch");
 }
 
@@ -241,26 +266,33 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
     }
 }
 
+// commit_t: the first launch advances the device step counter (the step's
+// scalars were prepared by the norm kernel; otherwise k_step_scalars did both).
 template <bool HAS_ACC, int KMAX>
-int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
+int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_t) {
     constexpr int U = KMAX <= 1 ? BF16K_STEP_U : (KMAX <= 4 ? BF16K_FOLD4_STEP_U : BF16K_FOLD8_STEP_U);
+    cudaError_t e = cudaSuccess;
+    bool first = true;
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
-        k<<<grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, 0, st>>>(h->segs_d, h->chunks_d, c0, c1, gt,
-                                                                          h->step_d, h->norm_d, h->gscale);
+        const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, st,
+                                      (const Seg *)h->segs_d, (const Chunk *)h->chunks_d, c0, c1, gt, h->step_d,
+                                      (const NormState *)h->norm_d, h->gscale, (commit_t && first) ? 1 : 0);
+        first = false;
+        if (e == cudaSuccess) e = e1;
     });
     if (rc) return rc;
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? 0 : cuda_fail(h, e, "step kernel launch");
 }
 
-int launch_step(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st) {
+int launch_step(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st, bool commit_t) {
     switch (kmax_for(fs.count())) {
-    case 0: return launch_step_k<true, 0>(h, fs, st);
-    case 1: return has_acc ? launch_step_k<true, 1>(h, fs, st) : launch_step_k<false, 1>(h, fs, st);
-    case 4: return has_acc ? launch_step_k<true, 4>(h, fs, st) : launch_step_k<false, 4>(h, fs, st);
-    default: return has_acc ? launch_step_k<true, 8>(h, fs, st) : launch_step_k<false, 8>(h, fs, st);
+    case 0: return launch_step_k<true, 0>(h, fs, st, commit_t);
+    case 1: return has_acc ? launch_step_k<true, 1>(h, fs, st, commit_t) : launch_step_k<false, 1>(h, fs, st, commit_t);
+    case 4: return has_acc ? launch_step_k<true, 4>(h, fs, st, commit_t) : launch_step_k<false, 4>(h, fs, st, commit_t);
+    default: return has_acc ? launch_step_k<true, 8>(h, fs, st, commit_t) : launch_step_k<false, 8>(h, fs, st, commit_t);
     }
 }
 
@@ -482,6 +514,8 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     // Optional cap on the CTAs of every launch (testing that results do not
     // depend on the grid: the norm's partials are per chunk, not per CTA).
     if (const char *mg = std::getenv("BF16OPT_MAX_GRID")) h->max_grid = std::max(0, std::atoi(mg));
+    // Programmatic dependent launch is on unless BF16OPT_PDL=0 (to compare).
+    if (const char *pd = std::getenv("BF16OPT_PDL")) h->pdl = std::atoi(pd) != 0;
 
     cudaError_t e = cudaSuccess;
     const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());
@@ -559,6 +593,7 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t) {
     if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
     e = cudaMemcpy(&h->step_d->t, &t, sizeof t, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(h, e, "writing the step counter");
+    h->scalars_ready = false;   // prepared for the old counter
     return BF16OPT_OK;
 }
 
@@ -635,10 +670,12 @@ int bf16opt_grad_norm(bf16opt_t *h, void *stream, double *host_norm) {
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
     // the chunk partials were written by the LAST pass
-    k_norm_final<<<1, kFinalThreads, 0, st>>>(h->partials_d, h->n_chunks, h->max_norm, h->norm_d);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(h, k_norm_final, 1, kFinalThreads, st, (const double *)h->partials_d, h->n_chunks,
+                           h->max_norm, h->norm_d, (const StepParams *)h->params_d, h->step_d);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");
     h->state = S_NORMED;
+    h->scalars_ready = true;
     if (host_norm) {
         double nrm = 0.0;
         if ((e = cudaMemcpyAsync(&nrm, &h->norm_d->norm, sizeof(double), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
@@ -679,10 +716,12 @@ int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
     if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_global_sumsq needs grad_norm_local first");
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
-    k_norm_from_sumsq<<<1, 32, 0, (cudaStream_t)stream>>>(global_sumsq, h->max_norm, h->norm_d);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(h, k_norm_from_sumsq, 1, 32, (cudaStream_t)stream, global_sumsq, h->max_norm, h->norm_d,
+                           (const StepParams *)h->params_d, h->step_d);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");
     h->state = S_NORMED;
+    h->scalars_ready = true;
     if (!std::isfinite(global_sumsq)) {
         h->last_error = "global gradient norm is not finite";
         return BF16OPT_WARN_NONFINITE;
@@ -745,6 +784,7 @@ int bf16opt_set_skip_nonfinite(bf16opt_t *h, int enable) {
     cudaError_t e = quiesce();
     if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
     h->skip_nonfinite = enable != 0;
+    h->scalars_ready = false;   // the skip decision was prepared with the old setting
     e = upload_params(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "uploading the skip setting");
     return BF16OPT_OK;
@@ -761,6 +801,7 @@ int bf16opt_set_lr_schedule(bf16opt_t *h, const bf16opt_lr_schedule_t *s) {
     if (e != cudaSuccess) return cuda_fail(h, e, "waiting for the device");
     h->has_sched = s != nullptr;
     if (s) h->sched = *s;
+    h->scalars_ready = false;   // prepared with the old schedule
     e = upload_params(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "uploading the schedule");
     return BF16OPT_OK;
@@ -783,12 +824,21 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
-    // t <- t + 1 and this step's scalars, on the device (a captured step replays correctly)
-    k_step_scalars<<<1, 32, 0, st>>>(h->params_d, h->step_d, ov, h->norm_d);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(h, e, "step scalars launch");
-    int rc = launch_step(h, h->acc_valid, pending_set(h), st);
+    // The norm kernel prepared the scalars of step t + 1 with the groups' own
+    // learning rates; the step kernel then advances t itself.  A learning-rate
+    // override, a setting changed since the norm, or an empty shard take one
+    // more one-warp kernel that computes them (and advances t).  Either way
+    // everything is computed on the device, so a captured step replays right.
+    const bool prepared = !lr_override && h->scalars_ready && h->n_chunks > 0;
+    if (!prepared) {
+        cudaError_t e = launch(h, k_step_scalars, 1, 32, st, (const StepParams *)h->params_d, h->step_d, ov,
+                               (const NormState *)h->norm_d);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(h, e, "step scalars launch");
+    }
+    int rc = launch_step(h, h->acc_valid, pending_set(h), st, prepared);
     if (rc) return rc;
+    h->scalars_ready = false;
     h->state = S_IDLE;
     h->acc_valid = false;
     h->pend_flat.clear();

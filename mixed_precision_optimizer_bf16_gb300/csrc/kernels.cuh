@@ -197,6 +197,19 @@ __device__ __forceinline__ bool check_fails(bool bad, uint32_t bit) {
 __device__ __forceinline__ bool mis16(const void *p) { return ((uintptr_t)p & 15u) != 0; }
 __device__ __forceinline__ bool mis8(const void *p) { return ((uintptr_t)p & 7u) != 0; }
 
+// -------------------------------------------------- programmatic dependent launch
+// Every kernel of a step is launched with programmatic stream serialization:
+// it may be scheduled while its predecessor on the stream is still draining,
+// so its CTAs are resident and past their launch latency when that work ends.
+// It therefore waits here, before its first global-memory access, until every
+// prerequisite grid has completed with its writes visible (a no-op when it was
+// launched the ordinary way), and at once allows its own successor to be
+// scheduled.  The wait is the hardware's; no kernel spins on a flag.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -375,6 +388,7 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
     __shared__ double sh[kThreads / 32];
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
+    pdl_enter();
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
@@ -496,56 +510,81 @@ __device__ __forceinline__ void store_norm_state(const NormClip &r, NormState *_
     out->pad = 0;
 }
 
-// Sum of the chunk partials in a fixed order, then norm and clip coefficient.
+// The per-group FP32 scalars of step t, computed in FP64 from the FP32
+// hyper-parameters: bias corrections 1 - b^t (Kingma & Ba, Algorithm 1),
+// step_size = lr / bc1, 1 / sqrt(bc2), decay = lr * wd, with lr times the
+// warmup + cosine factor when a schedule is attached.
+__device__ __forceinline__ void group_scalars(const StepParams *__restrict__ P, int64_t t, float lr_g, int g,
+                                              GroupK &o) {
+    double f = 1.0;
+    if (P->has_sched) {
+        const double r = (double)P->min_ratio;
+        if (t <= P->warmup) {
+            f = (double)t / (double)P->warmup;
+        } else if (t <= P->decay) {
+            const double x = (double)(t - P->warmup) / (double)(P->decay - P->warmup);
+            f = r + (1.0 - r) * 0.5 * (1.0 + cos(3.141592653589793 * x));
+        } else {
+            f = r;
+        }
+    }
+    const double lr = (double)lr_g * f;
+    const double b1 = (double)P->beta1[g], b2 = (double)P->beta2[g];
+    const double bc1 = 1.0 - pow(b1, (double)t);
+    const double bc2 = 1.0 - pow(b2, (double)t);
+    o.b1 = (float)b1;
+    o.omb1 = (float)(1.0 - b1);
+    o.b2 = (float)b2;
+    o.omb2 = (float)(1.0 - b2);
+    o.eps = P->eps[g];
+    o.decay = (float)(lr * (double)P->wd[g]);
+    o.step_size = (float)(lr / bc1);
+    o.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+}
+
+// The scalars of the next step (t + 1, the groups' own learning rates) and its
+// skip decision, prepared as soon as the norm is known so that the step needs
+// no kernel of its own: thread g < n_groups writes group g, thread 0 the skip
+// flag.  The step counter itself advances only when the step runs.
+__device__ __forceinline__ void prepare_step(const StepParams *__restrict__ P, StepState *S, double sumsq) {
+    const int g = threadIdx.x;
+    const int64_t t = S->t + 1;
+    if (g < P->n_groups && g < kMaxGroups) group_scalars(P, t, P->lr[g], g, S->gtab.g[g]);
+    if (g == 0) S->skip = (P->skip_nonfinite && !isfinite(sumsq)) ? 1 : 0;
+}
+
+// Sum of the chunk partials in a fixed order, then norm and clip coefficient,
+// and the scalars of the step that follows.
 __global__ void __launch_bounds__(kFinalThreads)
-k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out) {
+k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out,
+             const StepParams *__restrict__ P, StepState *S) {
     __shared__ double sh[kFinalThreads];
-    const double S = final_sum(partials, n, sh);
-    if (threadIdx.x == 0) store_norm_state(norm_and_clip(S, max_norm), out);
+    pdl_enter();
+    const double sumsq = final_sum(partials, n, sh);
+    prepare_step(P, S, sumsq);
+    if (threadIdx.x == 0) store_norm_state(norm_and_clip(sumsq, max_norm), out);
 }
 
 // Norm and clip coefficient from a sum of squares given by the host (the
-// all-rank sum under ZeRO): same formula as k_norm_final.
-__global__ void k_norm_from_sumsq(double S, float max_norm, NormState *__restrict__ out) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) store_norm_state(norm_and_clip(S, max_norm), out);
+// all-rank sum under ZeRO): same formula as k_norm_final.  One warp.
+__global__ void k_norm_from_sumsq(double sumsq, float max_norm, NormState *__restrict__ out,
+                                  const StepParams *__restrict__ P, StepState *S) {
+    pdl_enter();
+    prepare_step(P, S, sumsq);
+    if (threadIdx.x == 0) store_norm_state(norm_and_clip(sumsq, max_norm), out);
 }
 
-// t <- t + 1 and the per-group FP32 scalars of step t, computed in FP64 from
-// the FP32 hyper-parameters: bias corrections 1 - b^t (Kingma & Ba, Algorithm
-// 1), step_size = lr / bc1, 1 / sqrt(bc2), decay = lr * wd; lr times the
-// warmup + cosine factor when a schedule is attached.  One CTA of 32 threads.
-__global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *__restrict__ S, LrOverride ov,
+// t <- t + 1 (unless the step is skipped) and the per-group scalars of step t
+// with the per-call learning rates, for a step whose scalars were not prepared
+// with the norm (a learning-rate override, settings changed since the norm, or
+// an empty shard).  One warp.
+__global__ void k_step_scalars(const StepParams *__restrict__ P, StepState *S, LrOverride ov,
                                const NormState *__restrict__ ns) {
+    pdl_enter();
     const int skip = (P->skip_nonfinite && !ns->finite) ? 1 : 0;
     const int64_t t = S->t + 1;
     const int g = threadIdx.x;
-    if (g < P->n_groups && g < kMaxGroups) {
-        double f = 1.0;
-        if (P->has_sched) {
-            const double r = (double)P->min_ratio;
-            if (t <= P->warmup) {
-                f = (double)t / (double)P->warmup;
-            } else if (t <= P->decay) {
-                const double x = (double)(t - P->warmup) / (double)(P->decay - P->warmup);
-                f = r + (1.0 - r) * 0.5 * (1.0 + cos(3.141592653589793 * x));
-            } else {
-                f = r;
-            }
-        }
-        const double lr = (double)(ov.use ? ov.lr[g] : P->lr[g]) * f;
-        const double b1 = (double)P->beta1[g], b2 = (double)P->beta2[g];
-        const double bc1 = 1.0 - pow(b1, (double)t);
-        const double bc2 = 1.0 - pow(b2, (double)t);
-        GroupK &o = S->gtab.g[g];
-        o.b1 = (float)b1;
-        o.omb1 = (float)(1.0 - b1);
-        o.b2 = (float)b2;
-        o.omb2 = (float)(1.0 - b2);
-        o.eps = P->eps[g];
-        o.decay = (float)(lr * (double)P->wd[g]);
-        o.step_size = (float)(lr / bc1);
-        o.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
-    }
+    if (g < P->n_groups && g < kMaxGroups) group_scalars(P, t, ov.use ? ov.lr[g] : P->lr[g], g, S->gtab.g[g]);
     __syncwarp();
     if (g == 0) {
         S->skip = skip;
@@ -584,10 +623,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool HAS_ACC, int KMAX, class GT, int U>
 __global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
-       const StepState *__restrict__ st, const NormState *__restrict__ ns, float gscale) {
+       StepState *st, const NormState *__restrict__ ns, float gscale, int commit_t) {
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
+    pdl_enter();
     if (st->skip) return;                                      // non-finite norm, skipping enabled
+    // the step counter advances with the step whose scalars the norm prepared
+    // (nothing in this kernel reads it)
+    if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
     const GroupTable *__restrict__ gtab = &st->gtab;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
     for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {

@@ -509,7 +509,7 @@ def test_too_many_deferred():
     for _ in range(C.BF16OPT_MAX_DEFERRED - 1):
         assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == 0
     assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_DEFER) == C.BF16OPT_ERR_INVALID_ARG
-    assert C.bf16opt_accumulate(h, g.data_ptr(), None, 0) == 0      # a stored pass folds all nine
+    assert C.bf16opt_accumulate(h, g.data_ptr(), None, C.BF16OPT_LAST) == 0   # a stored pass folds all nine
     assert C.bf16opt_grad_norm(h, 0, True) == (0, 0.0)
     assert C.bf16opt_step(h) == 0
     torch.cuda.synchronize()
