@@ -89,6 +89,70 @@ def gather_sumsqs(local, group=None):
     return [float(p.item()) for p in parts]
 
 
+def partition_bounds(n, world):
+    """ZeRO flat partitioning: rank r owns elements [b[r], b[r+1]) of the n
+    elements of the flat buffer, contiguous slices of ceil(n / world) elements
+    (the last ones shorter or empty)."""
+    part = -(-int(n) // int(world)) if world > 0 else 0
+    return [min(int(n), r * part) for r in range(int(world) + 1)]
+
+
+def exchange_gradient_slices(full_grad, bounds, group=None):
+    """The exchange half of a ZeRO-2 gradient reduce-scatter.
+
+    full_grad: this rank's bf16 gradient (bf16 or int16 tensor) of the whole
+    flat buffer; bounds: partition_bounds(n, world).  Every rank sends
+    partition p of its gradient to rank p and receives its own partition from
+    every rank.  Returns a tensor [world, own partition size] on full_grad's
+    device: row q is rank q's gradient over this rank's partition, so the rows
+    are in rank order.  Point-to-point sends of byte views (gloo has no
+    all-to-all and no 16-bit types); with gloo a CUDA gradient is staged
+    through host memory.  Without an initialised process group the only row is
+    the gradient itself."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return full_grad.reshape(1, -1)
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    if len(bounds) != world + 1 or bounds[-1] != full_grad.numel():
+        raise ValueError("bounds must be partition_bounds(full_grad.numel(), world)")
+    stage = full_grad.is_cuda and dist.get_backend(group) != "nccl"
+    src = full_grad.detach().cpu() if stage else full_grad.detach()
+    src = src.contiguous().view(torch.uint8)
+    lo, hi = bounds[rank], bounds[rank + 1]
+    # rows padded to whole 128-byte lines, so that every row starts where the
+    # state buffers do (vector-aligned) whatever the partition size
+    stride = -(-(hi - lo) // 64) * 64
+    out = torch.empty((world, max(stride, 1)), dtype=full_grad.dtype, device=full_grad.device)
+    recv = torch.empty_like(out, device="cpu") if stage else out
+    ops = []
+    for q in range(world):
+        peer = dist.get_global_rank(group, q) if group is not None else q
+        if q == rank:
+            recv[q, :hi - lo].view(torch.uint8).copy_(src[2 * lo:2 * hi])
+            continue
+        if bounds[q + 1] > bounds[q]:
+            ops.append(dist.P2POp(dist.isend, src[2 * bounds[q]:2 * bounds[q + 1]], peer, group))
+        if hi > lo:
+            ops.append(dist.P2POp(dist.irecv, recv[q, :hi - lo].view(torch.uint8), peer, group))
+    if ops:
+        for w in dist.batch_isend_irecv(ops):
+            w.wait()
+    if stage:
+        out.copy_(recv)
+    return out[:, :hi - lo]
+
+
+def fold_pattern(slices, last):
+    """Deferral flags for folding `slices` received gradient slices of one
+    micro-batch: every run of 8 is folded by its 8th (the library keeps at most
+    8 pending); within the last micro-batch the final run stays deferred into
+    the norm pass and the step, otherwise the final slice folds it."""
+    flags = resident_pattern(slices)
+    if not last:
+        flags[-1] = False
+    return flags
+
+
 class BF16Optimizer:
     """One handle over a FLAT shard (`flat` = dict of the five tensors, `ranges`)
     or a LIST of tensors (`tensors` = list of such dicts with a "group" key)."""
@@ -214,6 +278,38 @@ class BF16Optimizer:
                                       _stream_handle(stream))
         return C.check(rc, self.h)
 
+    def accumulate_reduce_scatter(self, full_grad, first=False, last=False, group=None, stream=None):
+        """ZeRO-2 gradient reduction feeding the FP32 accumulation.
+
+        This optimizer holds one rank's partition (FLAT) of a flat buffer split
+        by partition_bounds; full_grad is this rank's bf16 gradient of the whole
+        buffer for one micro-batch.  The partitions are exchanged
+        (exchange_gradient_slices) and the world received slices of this
+        rank's partition are folded into the FP32 accumulator in rank order --
+        one FP32 add per slice, micro-batch by micro-batch, rank by rank, the
+        same arithmetic as accumulating them as consecutive micro-batches.
+        The slices ride on DEFER (runs of at most 8 folded in one pass); those
+        of the last micro-batch stay deferred until the step, which keeps the
+        received buffer alive until then.  first/last: as for accumulate()."""
+        import torch.distributed as dist
+        if self.mode != C.BF16OPT_FLAT:
+            raise ValueError("accumulate_reduce_scatter needs a FLAT partition")
+        world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
+        bounds = partition_bounds(full_grad.numel(), world)
+        rank = dist.get_rank(group) if world > 1 else 0
+        if bounds[rank + 1] - bounds[rank] != self.n:
+            raise ValueError(f"partition of rank {rank} has {bounds[rank + 1] - bounds[rank]} elements, "
+                             f"this optimizer {self.n}")
+        with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+            recv = exchange_gradient_slices(full_grad, bounds, group)
+        flags = fold_pattern(world, last)
+        for q in range(world):
+            self.accumulate(recv[q], first=first and q == 0, last=last and q == world - 1, defer=flags[q],
+                            stream=stream)
+        # deferred slices are read by a later pass: keep their buffer until then
+        self._recv_alive = recv if any(flags) else None
+        return recv
+
     def grad_norm(self, stream=None, sync=False):
         rc, norm = C.bf16opt_grad_norm(self.h, _stream_handle(stream), want_norm=sync)
         C.check(rc, self.h)
@@ -287,7 +383,11 @@ class BF16Optimizer:
         lrs = None if lr is None else ([float(lr)] * len(self.groups) if not hasattr(lr, "__len__") else list(lr))
         if lrs is not None and len(lrs) != len(self.groups):
             raise ValueError(f"lr: {len(lrs)} rates for {len(self.groups)} groups")
-        return C.check(C.bf16opt_step(self.h, lrs, _stream_handle(stream)), self.h)
+        rc = C.check(C.bf16opt_step(self.h, lrs, _stream_handle(stream)), self.h)
+        # received gradient slices the step folded may be freed once it has run
+        # (the caching allocator reuses them in stream order)
+        self._recv_alive = None
+        return rc
 
     @property
     def t(self):
