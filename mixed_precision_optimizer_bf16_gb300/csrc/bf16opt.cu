@@ -49,6 +49,7 @@ struct bf16opt {
     Chunk *chunks_d = nullptr;
     double *partials_d = nullptr;
     NormState *norm_d = nullptr;
+    unsigned *queue_d = nullptr;         // chunk counter of the pass in flight (0 between passes)
     StepParams *params_d = nullptr;      // hyper-parameters + schedule (device)
     StepState *step_d = nullptr;         // device step counter + this step's scalars
     std::vector<bf16opt_group_t> groups;
@@ -68,6 +69,7 @@ struct bf16opt {
     bool has_sched = false;
     bool skip_nonfinite = false;
     bool pdl = true;                     // launch with programmatic stream serialization (BF16OPT_PDL=0: off)
+    bool claim = true;                   // CTAs claim chunks from queue_d (BF16OPT_SCHEDULE=static: fixed stride)
     bool scalars_ready = false;          // the norm kernel prepared this step's scalars (groups' own lr)
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
@@ -247,7 +249,8 @@ int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
         const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0), kThreads, st, (const Seg *)h->segs_d,
-                                      (const Chunk *)h->chunks_d, c0, c1, gt, h->partials_d, h->gscale);
+                                      (const Chunk *)h->chunks_d, c0, c1, gt, h->partials_d, h->gscale,
+                                      h->claim ? h->queue_d : nullptr);
         if (e == cudaSuccess) e = e1;
     });
     if (rc) return rc;
@@ -278,7 +281,8 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
         const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, st,
                                       (const Seg *)h->segs_d, (const Chunk *)h->chunks_d, c0, c1, gt, h->step_d,
-                                      (const NormState *)h->norm_d, h->gscale, (commit_t && first) ? 1 : 0);
+                                      (const NormState *)h->norm_d, h->gscale, (commit_t && first) ? 1 : 0,
+                                      h->claim ? h->queue_d : nullptr);
         first = false;
         if (e == cudaSuccess) e = e1;
     });
@@ -308,6 +312,8 @@ void free_scratch(bf16opt_t *h) {
     if (h->chunks_d) cudaFree(h->chunks_d);
     if (h->partials_d) cudaFree(h->partials_d);
     if (h->norm_d) cudaFree(h->norm_d);
+    if (h->queue_d) cudaFree(h->queue_d);
+    h->queue_d = nullptr;
     if (h->params_d) cudaFree(h->params_d);
     if (h->step_d) cudaFree(h->step_d);
     h->params_d = nullptr;
@@ -516,6 +522,13 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     if (const char *mg = std::getenv("BF16OPT_MAX_GRID")) h->max_grid = std::max(0, std::atoi(mg));
     // Programmatic dependent launch is on unless BF16OPT_PDL=0 (to compare).
     if (const char *pd = std::getenv("BF16OPT_PDL")) h->pdl = std::atoi(pd) != 0;
+    // Chunks are claimed from a counter on shards of full-size chunks (from 2^25
+    // elements): there a CTA works through tens to hundreds of chunks and the
+    // balance pays; a smaller shard gives each CTA one to a few short chunks,
+    // where the claim's round trip would cost more than it balances.
+    // BF16OPT_SCHEDULE=static / claim overrides (to compare).
+    h->claim = total >= (uint64_t(1) << 25);
+    if (const char *sc = std::getenv("BF16OPT_SCHEDULE")) h->claim = std::strcmp(sc, "static") != 0;
 
     cudaError_t e = cudaSuccess;
     const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());
@@ -523,6 +536,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
         (e = cudaMalloc(&h->chunks_d, nch * sizeof(Chunk))) != cudaSuccess ||
         (e = cudaMalloc(&h->partials_d, nch * sizeof(double))) != cudaSuccess ||
         (e = cudaMalloc(&h->norm_d, sizeof(NormState))) != cudaSuccess ||
+        (e = cudaMalloc(&h->queue_d, sizeof(unsigned))) != cudaSuccess ||
         (e = cudaMalloc(&h->params_d, sizeof(StepParams))) != cudaSuccess ||
         (e = cudaMalloc(&h->step_d, sizeof(StepState))) != cudaSuccess) {
         free_scratch(h);
@@ -534,6 +548,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     if ((!segs.empty() && (e = cudaMemcpy(h->segs_d, segs.data(), segs.size() * sizeof(Seg), cudaMemcpyHostToDevice)) != cudaSuccess) ||
         (!chunks.empty() && (e = cudaMemcpy(h->chunks_d, chunks.data(), chunks.size() * sizeof(Chunk), cudaMemcpyHostToDevice)) != cudaSuccess) ||
         (e = cudaMemset(h->norm_d, 0, sizeof(NormState))) != cudaSuccess ||
+        (e = cudaMemset(h->queue_d, 0, sizeof(unsigned))) != cudaSuccess ||
         (e = cudaMemset(h->step_d, 0, sizeof(StepState))) != cudaSuccess ||
         (e = upload_params(h)) != cudaSuccess) {
         free_scratch(h);

@@ -210,6 +210,41 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------ chunk claiming
+// The CTAs of a pass take chunks from a counter instead of a fixed stride:
+// under a fixed stride a pass lasts as long as its slowest CTAs, and on GB300
+// some CTAs stream from HBM measurably slower than others (the two dies), so
+// a write-heavy pass ran at 0.95 of the copy peak with fixed strides and at
+// 1.02 with claiming.  A chunk's results depend only on the chunk (partials
+// are indexed by chunk), so the results stay bit-identical whatever CTA takes
+// which chunk.  The counter resets itself: every CTA makes exactly one claim
+// past the last chunk, and the CTA whose claim is the very last one (index
+// nch + gridDim.x - 1) stores 0 -- after it no CTA of the grid touches the
+// counter, and the next kernel on the stream starts after this grid has
+// completed.  Hence no memset between passes, also inside a captured graph.
+// ctr == nullptr: fixed stride (c0 + blockIdx.x, then + gridDim.x).
+__device__ __forceinline__ uint32_t claim_chunk(unsigned *ctr, uint32_t c0, uint32_t prev, uint32_t *sh) {
+    if (!ctr) return prev == 0xffffffffu ? c0 + blockIdx.x : prev + gridDim.x;
+    __syncthreads();                               // every thread is done with the previous index
+    if (threadIdx.x == 0) *sh = atomicAdd(ctr, 1u);
+    __syncthreads();
+    return c0 + *sh;
+}
+// The same, for a kernel that runs one CTA per SM: thread 0 claims the next
+// chunk when the current one starts (nxt), so the atomic's round trip overlaps
+// the chunk's work instead of stalling the SM between chunks.
+__device__ __forceinline__ uint32_t take_claimed(unsigned *ctr, uint32_t c0, uint32_t prev, uint32_t nxt,
+                                                 uint32_t *sh) {
+    if (!ctr) return prev + gridDim.x;
+    __syncthreads();
+    if (threadIdx.x == 0) *sh = nxt;
+    __syncthreads();
+    return c0 + *sh;
+}
+__device__ __forceinline__ void release_chunks(unsigned *ctr, uint32_t c0, uint32_t c1, uint32_t last) {
+    if (ctr && threadIdx.x == 0 && last - c0 == (c1 - c0) + gridDim.x - 1) atomicExch(ctr, 0u);
+}
+
 // ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -381,15 +416,26 @@ __device__ __forceinline__ uint32_t chunk_head(const void *fp32_ptr, bool use_fp
 // One pass over chunks [c0, c1): v = fold(acc?, g_0..g_{K-1}), stored back to
 // acc if WRITE, and its per-chunk sum of squares (times gscale, rounded to
 // FP32 first) written to partials[c] if NORM.  KMAX = 0 reads acc alone.
+// Resident CTAs per SM the single-gradient passes are built for (the register
+// budget of their measured launch shape): 8 for the FIRST pass, 3 for a pass
+// that computes the norm's partials, 4 for the other stored passes.  Passes
+// that fold several deferred gradients keep whatever registers they need.
+template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
+constexpr int accum_min_blocks() {
+    return KMAX != 1 ? 1 : ((!HAS_ACC && WRITE && !NORM) ? 8 : (NORM ? 3 : 4));
+}
+
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM, class GT, int U>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (accum_min_blocks<HAS_ACC, KMAX, WRITE, NORM>()))
 k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
-        double *__restrict__ partials, float gscale) {
+        double *__restrict__ partials, float gscale, unsigned *queue) {
     __shared__ double sh[kThreads / 32];
+    __shared__ uint32_t sh_claim;
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     pdl_enter();
-    for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+    uint32_t c = claim_chunk(queue, c0, 0xffffffffu, &sh_claim);
+    for (; c < c1; c = claim_chunk(queue, c0, c, &sh_claim)) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         float *a = s.acc + ch.start;
@@ -464,6 +510,7 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
             if (threadIdx.x == 0) partials[c] = tot;
         }
     }
+    release_chunks(queue, c0, c1, c);
 }
 
 // ---------------------------------------------------------------- norm final
@@ -623,17 +670,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool HAS_ACC, int KMAX, class GT, int U>
 __global__ void __launch_bounds__(kStepThreads, BF16K_STEP_MIN_BLOCKS)
 k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t c0, uint32_t c1, GT gt,
-       StepState *st, const NormState *__restrict__ ns, float gscale, int commit_t) {
+       StepState *st, const NormState *__restrict__ ns, float gscale, int commit_t, unsigned *queue) {
+    __shared__ uint32_t sh_claim;
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     pdl_enter();
-    if (st->skip) return;                                      // non-finite norm, skipping enabled
+    if (st->skip) return;                   // non-finite norm, skipping enabled (no CTA claims a chunk)
     // the step counter advances with the step whose scalars the norm prepared
     // (nothing in this kernel reads it)
     if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
     const GroupTable *__restrict__ gtab = &st->gtab;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
-    for (uint32_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+    uint32_t c = claim_chunk(queue, c0, 0xffffffffu, &sh_claim), nxt = 0;
+    for (; c < c1; c = take_claimed(queue, c0, c, nxt, &sh_claim)) {
+        if (queue && threadIdx.x == 0) nxt = atomicAdd(queue, 1u);   // the next chunk, claimed ahead
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         const GroupK G = gtab->g[s.group];
@@ -717,6 +767,7 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             }
         }
     }
+    release_chunks(queue, c0, c1, c);
 }
 
 }  // namespace bf16k

@@ -519,11 +519,15 @@ def test_too_many_deferred():
 @needs_cuda
 def test_results_do_not_depend_on_the_grid(monkeypatch):
     """The norm's partials belong to chunks, not CTAs, and the step is
-    element-wise: one CTA per launch gives the same bits as the full grid."""
+    element-wise: one CTA per launch gives the same bits as the full grid,
+    and so does any grid whose CTAs claim their chunks from the counter (in
+    whatever order the claims land) instead of taking a fixed stride."""
     wl = workloads.custom(250, [300_001, 4097, 77], decay=[True, False, True], gas=3, steps=2, grad_sigma=0.1,
                           misalign=1)
     outs = []
-    for cap in (None, "1", "7"):
+    for cap, sched in ((None, "static"), ("1", "static"), ("7", "static"), (None, "claim"), ("1", "claim"),
+                       ("7", "claim")):
+        monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
         if cap is None:
             monkeypatch.delenv("BF16OPT_MAX_GRID", raising=False)
         else:
@@ -541,12 +545,17 @@ def test_results_do_not_depend_on_the_grid(monkeypatch):
 # ------------------------------------------------------------ CUDA graphs
 
 @needs_cuda
+@pytest.mark.parametrize("sched", ["auto", "claim"])
 @pytest.mark.parametrize("mode", ["flat", "list"])
-def test_cuda_graph_replay_matches_eager(mode):
+def test_cuda_graph_replay_matches_eager(mode, sched, monkeypatch):
     """One step captured into a CUDA graph and replayed for the later steps
     (fresh gradients written into the same buffers before each replay) gives
     the same bits as calling the API eagerly: the step counter and the
-    per-step scalars live on the device."""
+    per-step scalars live on the device.  With chunk claiming forced on, the
+    replays also show that the claim counter is back at zero after every pass
+    (it resets itself; no memset node sits in the graph)."""
+    if sched == "claim":
+        monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
     wl = workloads.custom(260, [40_000, 3, 16_385, 999], decay=[True, False, True, False], gas=3, steps=4,
                           grad_sigma=0.1, misalign=2, mode=mode)
     eager = GpuShard(wl, defer=[False, True, True])
@@ -1069,3 +1078,28 @@ def test_fast_pinned_buffers():
         torch.cuda.synchronize()
         assert torch.equal(dst, src)
         hb.close()
+
+
+@needs_cuda
+def test_claimed_chunks_on_a_full_chunk_shard(monkeypatch):
+    """A shard of 2^25 + 4099 elements (full 32,768-element chunks, so its CTAs
+    claim chunks by default) over many passes -- every deferral pattern the
+    bench uses, two steps each -- equals the fixed-stride schedule bit for bit
+    and the oracle within the tolerance."""
+    wl = workloads.custom(280, [(1 << 25) - 1000, 5099], decay=[True, False], gas=4, steps=2, grad_sigma=0.01,
+                          misalign=3)
+    outs = []
+    for sched in ("claim", "static"):
+        monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
+        for pat in ([False, False, False, True], [True] * 4, [True, False, True, True]):
+            sh = GpuShard(wl, defer=pat)
+            sh.run(wl.steps)
+            outs.append((sched, pat, sh.states(), list(sh.norms)))
+            sh.close()
+    for sched, pat, st, nr in outs[1:]:
+        assert nr == outs[0][3], (sched, pat)
+        for k in ("p", "m", "v", "p_bf16"):
+            assert np.array_equal(st[k].view(np.uint8), outs[0][2][k].view(np.uint8)), (sched, pat, k)
+    ref, scales = oracle_dense(wl, wl.steps)
+    check_norms(outs[0][3], ref["sumsq"])
+    compare(outs[0][2], ref, scales, wl, check_acc=False)
