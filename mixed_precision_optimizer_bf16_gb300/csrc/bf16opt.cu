@@ -269,6 +269,8 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
     }
 }
 
+constexpr uint64_t kStepClaimChunksPerCta = 64;
+
 // commit_t: the first launch advances the device step counter (the step's
 // scalars were prepared by the norm kernel; otherwise k_step_scalars did both).
 template <bool HAS_ACC, int KMAX>
@@ -279,10 +281,14 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
-        const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0, kStepThreads), kStepThreads, st,
-                                      (const Seg *)h->segs_d, (const Chunk *)h->chunks_d, c0, c1, gt, h->step_d,
+        const int grid = grid_for(h, k, c1 - c0, kStepThreads);
+        // one CTA per SM: claiming pays once every CTA has many chunks to go
+        // through (on a 134M-element shard, 27 per CTA, it cost 3 %)
+        const bool claim = h->claim && (uint64_t)(c1 - c0) >= kStepClaimChunksPerCta * (uint64_t)grid;
+        const cudaError_t e1 = launch(h, k, grid, kStepThreads, st, (const Seg *)h->segs_d,
+                                      (const Chunk *)h->chunks_d, c0, c1, gt, h->step_d,
                                       (const NormState *)h->norm_d, h->gscale, (commit_t && first) ? 1 : 0,
-                                      h->claim ? h->queue_d : nullptr);
+                                      claim ? h->queue_d : nullptr);
         first = false;
         if (e == cudaSuccess) e = e1;
     });

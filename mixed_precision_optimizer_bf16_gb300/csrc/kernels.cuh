@@ -33,6 +33,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -210,40 +211,60 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ------------------------------------------------------------ chunk claiming
-// The CTAs of a pass take chunks from a counter instead of a fixed stride:
-// under a fixed stride a pass lasts as long as its slowest CTAs, and on GB300
-// some CTAs stream from HBM measurably slower than others (the two dies), so
-// a write-heavy pass ran at 0.95 of the copy peak with fixed strides and at
-// 1.02 with claiming.  A chunk's results depend only on the chunk (partials
-// are indexed by chunk), so the results stay bit-identical whatever CTA takes
-// which chunk.  The counter resets itself: every CTA makes exactly one claim
-// past the last chunk, and the CTA whose claim is the very last one (index
-// nch + gridDim.x - 1) stores 0 -- after it no CTA of the grid touches the
-// counter, and the next kernel on the stream starts after this grid has
-// completed.  Hence no memset between passes, also inside a captured graph.
-// ctr == nullptr: fixed stride (c0 + blockIdx.x, then + gridDim.x).
-__device__ __forceinline__ uint32_t claim_chunk(unsigned *ctr, uint32_t c0, uint32_t prev, uint32_t *sh) {
-    if (!ctr) return prev == 0xffffffffu ? c0 + blockIdx.x : prev + gridDim.x;
-    __syncthreads();                               // every thread is done with the previous index
-    if (threadIdx.x == 0) *sh = atomicAdd(ctr, 1u);
-    __syncthreads();
-    return c0 + *sh;
-}
-// The same, for a kernel that runs one CTA per SM: thread 0 claims the next
-// chunk when the current one starts (nxt), so the atomic's round trip overlaps
-// the chunk's work instead of stalling the SM between chunks.
-__device__ __forceinline__ uint32_t take_claimed(unsigned *ctr, uint32_t c0, uint32_t prev, uint32_t nxt,
-                                                 uint32_t *sh) {
-    if (!ctr) return prev + gridDim.x;
-    __syncthreads();
-    if (threadIdx.x == 0) *sh = nxt;
-    __syncthreads();
-    return c0 + *sh;
-}
-__device__ __forceinline__ void release_chunks(unsigned *ctr, uint32_t c0, uint32_t c1, uint32_t last) {
-    if (ctr && threadIdx.x == 0 && last - c0 == (c1 - c0) + gridDim.x - 1) atomicExch(ctr, 0u);
-}
+// ------------------------------------------------------------ chunk schedule
+// Under a fixed chunk stride a pass lasts as long as its slowest CTAs, and on
+// GB300 some CTAs stream from HBM measurably slower than others: on the
+// 1.72B-element shard the write-heavy FIRST pass ran at 0.93 of the copy peak
+// with fixed strides and at 1.01 with the CTAs claiming chunks from a counter
+// (the whole step 16.5 -> 15.8 ms).  Giving only the last quarter of the
+// chunks out by claims was slower (15.96 ms): the CTAs' speed difference is
+// larger than such a pool.  A chunk's results depend only on the chunk (the
+// norm's partials are indexed by chunk), so they are bit-identical whatever
+// CTA takes which chunk.
+// The counter resets itself: every CTA makes exactly one claim past the last
+// chunk, and the CTA whose claim is the very last one (nch + gridDim.x - 1)
+// stores 0 -- after it no CTA of the grid touches the counter, and the next
+// kernel on the stream starts after this grid has completed.  Hence no memset
+// between passes, also inside a captured graph.
+// ctr == nullptr: the fixed stride c0 + b, c0 + b + G, ...
+struct ClaimSched {
+    unsigned *ctr;
+    uint32_t c0, c1;
+    uint32_t *sh;          // shared slot for the claimed index
+
+    __device__ __forceinline__ ClaimSched(unsigned *q, uint32_t a, uint32_t b, uint32_t *slot)
+        : ctr(q), c0(a), c1(b), sh(slot) {}
+    // All threads of the CTA call it; `ahead`: the value thread 0 claimed
+    // while the previous chunk ran (use_ahead), else claimed now.
+    __device__ __forceinline__ uint32_t claim(bool use_ahead, uint32_t ahead) {
+        __syncthreads();                           // every thread is done with the previous index
+        if (threadIdx.x == 0) *sh = use_ahead ? ahead : atomicAdd(ctr, 1u);
+        __syncthreads();
+        return c0 + *sh;
+    }
+    __device__ __forceinline__ uint32_t first() { return ctr ? claim(false, 0) : c0 + blockIdx.x; }
+    __device__ __forceinline__ bool claims() const { return ctr != nullptr; }
+    __device__ __forceinline__ uint32_t next(uint32_t c, bool use_ahead = false, uint32_t ahead = 0) {
+        return ctr ? claim(use_ahead, ahead) : c + gridDim.x;
+    }
+    // c_end: the chunk index that ended the CTA's loop, i.e. its claim past the end
+    __device__ __forceinline__ void release(uint32_t c_end) {
+        if (ctr && threadIdx.x == 0 && c_end - c0 == (c1 - c0) + gridDim.x - 1) atomicExch(ctr, 0u);
+    }
+};
+// The fixed stride alone, for the passes that fold several deferred gradients
+// (they run at two or three CTAs per SM, and the claiming code's registers
+// would cost them a resident CTA; measured slower).
+struct StrideSched {
+    uint32_t c0;
+    __device__ __forceinline__ StrideSched(unsigned *, uint32_t a, uint32_t, uint32_t *) : c0(a) {}
+    __device__ __forceinline__ uint32_t first() const { return c0 + blockIdx.x; }
+    __device__ __forceinline__ bool claims() const { return false; }
+    __device__ __forceinline__ uint32_t next(uint32_t c, bool = false, uint32_t = 0) const { return c + gridDim.x; }
+    __device__ __forceinline__ void release(uint32_t) const {}
+};
+template <int KMAX>
+using SchedFor = typename std::conditional<(KMAX <= 1), ClaimSched, StrideSched>::type;
 
 // ------------------------------------------------------------------ helpers
 
@@ -417,12 +438,15 @@ __device__ __forceinline__ uint32_t chunk_head(const void *fp32_ptr, bool use_fp
 // acc if WRITE, and its per-chunk sum of squares (times gscale, rounded to
 // FP32 first) written to partials[c] if NORM.  KMAX = 0 reads acc alone.
 // Resident CTAs per SM the single-gradient passes are built for (the register
-// budget of their measured launch shape): 8 for the FIRST pass, 3 for a pass
-// that computes the norm's partials, 4 for the other stored passes.  Passes
-// that fold several deferred gradients keep whatever registers they need.
+// budget of their measured launch shape, which the chunk-claiming code would
+// otherwise exceed): 8 for the FIRST pass, 4 for the other stored pass, 3 for
+// a norm pass.  0 for the passes that fold several deferred gradients: no
+// minimum, the compiler's own choice (a minimum of 1 is not the same -- it
+// lets the compiler spend registers up to one CTA per SM, and those passes
+// lost a resident CTA).
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
 constexpr int accum_min_blocks() {
-    return KMAX != 1 ? 1 : ((!HAS_ACC && WRITE && !NORM) ? 8 : (NORM ? 3 : 4));
+    return KMAX == 1 ? ((!HAS_ACC && WRITE && !NORM) ? 8 : (NORM ? 3 : 4)) : 0;
 }
 
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM, class GT, int U>
@@ -434,8 +458,9 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
     constexpr int KA = KMAX > 0 ? KMAX : 1;
     const int K = KMAX <= 1 ? KMAX : (int)gt.k;
     pdl_enter();
-    uint32_t c = claim_chunk(queue, c0, 0xffffffffu, &sh_claim);
-    for (; c < c1; c = claim_chunk(queue, c0, c, &sh_claim)) {
+    SchedFor<KMAX> sch(queue, c0, c1, &sh_claim);
+    uint32_t c = sch.first();
+    for (; c < c1; c = sch.next(c)) {
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         float *a = s.acc + ch.start;
@@ -510,7 +535,7 @@ k_accum(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t
             if (threadIdx.x == 0) partials[c] = tot;
         }
     }
-    release_chunks(queue, c0, c1, c);
+    sch.release(c);
 }
 
 // ---------------------------------------------------------------- norm final
@@ -681,9 +706,13 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
     if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
     const GroupTable *__restrict__ gtab = &st->gtab;
     const float c_hi = ns->c_hi, c_lo = ns->c_lo;
-    uint32_t c = claim_chunk(queue, c0, 0xffffffffu, &sh_claim), nxt = 0;
-    for (; c < c1; c = take_claimed(queue, c0, c, nxt, &sh_claim)) {
-        if (queue && threadIdx.x == 0) nxt = atomicAdd(queue, 1u);   // the next chunk, claimed ahead
+    // one CTA per SM: the next pooled chunk is claimed when the current one
+    // starts, so the atomic's round trip overlaps the chunk's work
+    SchedFor<KMAX> sch(queue, c0, c1, &sh_claim);
+    uint32_t ahead = 0;
+    uint32_t c = sch.first();
+    for (; c < c1; c = sch.next(c, true, ahead)) {
+        if (sch.claims() && threadIdx.x == 0) ahead = atomicAdd(queue, 1u);
         const Chunk ch = chunks[c];
         const Seg s = segs[ch.seg];
         const GroupK G = gtab->g[s.group];
@@ -767,7 +796,7 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
             }
         }
     }
-    release_chunks(queue, c0, c1, c);
+    sch.release(c);
 }
 
 }  // namespace bf16k
