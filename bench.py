@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--extra", default="3,4", help="other workloads timed after the headline one ('' = none)")
     ap.add_argument("--extra-steps", type=int, default=10)
+    ap.add_argument("--no-offload", action="store_true", help="skip the ZeRO-Offload variant")
     return ap.parse_args()
 
 
@@ -320,6 +321,58 @@ def extra_workload(wl_id, steps, warmup, dev, world, peak, no_clocks):
     return out
 
 
+def offload_variant(wl, dev, steps, elements=1 << 27):
+    """ZeRO-Offload step (bf16opt_create_offload) on the first `elements`
+    elements of the workload: FP32 master and moments in host memory updated by
+    every host core, accumulator and bf16 parameters on the GPU, last
+    micro-batch deferred.  The step returns when the host holds the new state,
+    so its time is wall-clock around whole steps (gradients resident in HBM)."""
+    import torch
+
+    from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer
+    from synth import gpu as sgpu, workloads
+
+    w = workloads.prefix(wl, min(wl.n, elements)) if wl.mode == "flat" else None
+    if w is None:
+        return None
+    n, G = w.n, w.gas
+    master = torch.empty(n, dtype=torch.float32, device=dev)
+    sgpu.fill_master(w, master)
+    state = dict(master=master.cpu(), exp_avg=torch.zeros(n, dtype=torch.float32),
+                 exp_avg_sq=torch.zeros(n, dtype=torch.float32),
+                 grad_accum=torch.empty(n, dtype=torch.float32, device=dev),
+                 param_bf16=torch.empty(n, dtype=torch.int16, device=dev))
+    del master
+    grads = []
+    for k in range(G):
+        g = torch.empty(n, dtype=torch.int16, device=dev)
+        sgpu.fill_grad(w, 0, k, g)
+        grads.append(g)
+    opt = BF16Optimizer(w.groups, flat=state, ranges=w.ranges(), max_grad_norm=w.max_norm, offload=True)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for k in range(G):
+            opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=k == G - 1, stream=stream)
+        opt.grad_norm(stream=stream)
+        opt.step(stream=stream)
+
+    one()
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t) / steps
+    opt.close()
+    del opt, state, grads
+    torch.cuda.empty_cache()
+    return {"value": round(n / dt, 1), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3), "steps": steps,
+            "elements": n, "host_threads": os.cpu_count(), "link_bytes_per_elem": 6,
+            "note": "FP32 master and moments in host memory, AdamW on the host cores; the accumulator goes to "
+                    "the host (4 B/element) and the bf16 parameters back (2 B/element) in pipelined blocks"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -450,6 +503,10 @@ def run_ours(args):
                     + "; same FP32 adds in the same order"}}
     if graph_variant is not None:
         variant = dict(variant or {}, cuda_graph_replay=graph_variant)
+    if not args.no_variant and not args.no_offload:
+        off = offload_variant(wl, dev, 5)
+        if off is not None:
+            variant = dict(variant or {}, zero_offload=off)
     kern = {}
     for nm in names:
         ms = statistics.mean(per[nm])

@@ -174,6 +174,30 @@ typedef struct bf16opt bf16opt_t;    /* opaque handle */
  * bf16opt_last_error(NULL) has the message. */
 int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out);
 
+/* ZeRO-Offload variant ("企业官网建设流程全解析" (cf-1.com), section 3.3: the
+ * DeepSpeed configuration with offload_optimizer on the CPU; "单机多卡实战：
+ * Megatron-DeepSpeed训练类BLOOM模型全流程解析", section 6: offloading optimizer
+ * state to host memory to fit larger models).  Explicitly selected, never a
+ * fallback: a FLAT handle whose FP32 master, exp_avg and exp_avg_sq are HOST
+ * memory (12 bytes per element off the device), while grad_accum and
+ * param_bf16 are memory of the current device.  accumulate, grad_norm (and the
+ * multi-rank calls), get/set_step, the LR schedule and skipping work as for
+ * bf16opt_create.  bf16opt_step then: completes the accumulator if
+ * micro-batches are still deferred; computes the step's scalars, advances the
+ * step counter and takes the skip decision on the device (the same kernel as
+ * the device step); copies the accumulator to the host in blocks of 2^24
+ * elements, updates master and moments with the same FP32 operations as the
+ * device step on n_threads host threads (<= 0: one per core) while the next
+ * block is copied, and enqueues the copy of each block's bf16 parameters back
+ * to param_bf16 on `stream`.  It returns when the host arrays hold the new
+ * state; the bf16 parameters are on the device when `stream` reaches those
+ * copies.  Results: the same bits as a device handle over the same values.
+ * The library allocates 192 MiB of page-locked staging (less for a smaller
+ * shard) and the threads.  Not during a stream capture.  Errors: as
+ * bf16opt_create, and INVALID_ARG (not FLAT; master/moments not host memory;
+ * grad_accum/param_bf16 not memory of the current device), OOM. */
+int bf16opt_create_offload(const bf16opt_desc_t *d, int n_threads, bf16opt_t **out);
+
 /* Adds one micro-batch of bf16 gradients into the FP32 accumulator
  * ("BLOOM 176B 训练技术概览", "BF16 优化器").
  *   FLAT: grad_flat = device bf16 buffer of n elements, grad_list = NULL.

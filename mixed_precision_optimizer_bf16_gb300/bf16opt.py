@@ -62,7 +62,7 @@ class bf16opt_norm_result_t(ctypes.Structure):
 
 
 # Functions the header declares (the tests check the library exports them all).
-EXPORTS = ("bf16opt_create", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
+EXPORTS = ("bf16opt_create", "bf16opt_create_offload", "bf16opt_accumulate", "bf16opt_grad_norm", "bf16opt_step", "bf16opt_destroy",
            "bf16opt_get_step", "bf16opt_set_step", "bf16opt_error_string", "bf16opt_last_error",
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
            "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_rank_sumsqs",
@@ -97,6 +97,8 @@ def load(path=None):
     hp = ctypes.c_void_p
     L.bf16opt_create.restype = ctypes.c_int
     L.bf16opt_create.argtypes = [ctypes.POINTER(bf16opt_desc_t), ctypes.POINTER(hp)]
+    L.bf16opt_create_offload.restype = ctypes.c_int
+    L.bf16opt_create_offload.argtypes = [ctypes.POINTER(bf16opt_desc_t), ctypes.c_int, ctypes.POINTER(hp)]
     L.bf16opt_accumulate.restype = ctypes.c_int
     L.bf16opt_accumulate.argtypes = [hp, c_vp, ctypes.POINTER(c_vp), ctypes.c_uint, c_vp]
     L.bf16opt_grad_norm.restype = ctypes.c_int
@@ -143,6 +145,13 @@ def load(path=None):
 def bf16opt_create(desc):
     h = ctypes.c_void_p()
     rc = load().bf16opt_create(ctypes.byref(desc), ctypes.byref(h))
+    return rc, h
+
+
+def bf16opt_create_offload(desc, n_threads=0):
+    """FLAT descriptor whose master and moments are host addresses (ZeRO-Offload)."""
+    h = ctypes.c_void_p()
+    rc = load().bf16opt_create_offload(ctypes.byref(desc), int(n_threads), ctypes.byref(h))
     return rc, h
 
 

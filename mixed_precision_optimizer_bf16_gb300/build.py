@@ -6,10 +6,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "libbf16opt.so")
 SOURCES = [os.path.join(HERE, "csrc", "bf16opt.cu")]
-DEPS = SOURCES + [os.path.join(HERE, "csrc", "kernels.cuh"), os.path.join(ROOT, "include", "bf16opt.h")]
+DEPS = SOURCES + [os.path.join(HERE, "csrc", "kernels.cuh"), os.path.join(HERE, "csrc", "host_adam.h"),
+                  os.path.join(ROOT, "include", "bf16opt.h")]
 
+# -ffp-contract=off: host code rounds every product on its own (the offloaded
+# step's host update repeats the device kernel's operations exactly)
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared"]
+              "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off", "-shared"]
 
 
 def nvcc():

@@ -21,6 +21,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "../../include/bf16opt.h"
+#include "host_adam.h"
 #include "kernels.cuh"
 
 using namespace bf16k;
@@ -73,6 +74,19 @@ struct bf16opt {
     bool scalars_ready = false;          // the norm kernel prepared this step's scalars (groups' own lr)
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
+    // ZeRO-Offload handle (bf16opt_create_offload): master and moments in host
+    // memory, updated by the host cores; the accumulator and the bf16
+    // parameters stay on the device.
+    bool offload = false;
+    float *host_p = nullptr, *host_m = nullptr, *host_v = nullptr;
+    float *dev_acc = nullptr;
+    uint16_t *dev_bf = nullptr;
+    float *stage_acc[2] = {nullptr, nullptr};        // page-locked, one block each
+    uint16_t *stage_bf[2] = {nullptr, nullptr};
+    StepState *stage_step = nullptr;                 // page-locked copies of the step's scalars
+    NormState *stage_norm = nullptr;
+    cudaEvent_t ev_d2h[2] = {nullptr, nullptr}, ev_h2d[2] = {nullptr, nullptr};
+    bf16host::Pool *pool = nullptr;
 };
 
 namespace {
@@ -313,7 +327,26 @@ FoldSet pending_set(const bf16opt_t *h) {
     return fs;
 }
 
+void free_offload(bf16opt_t *h) {
+    for (int i = 0; i < 2; ++i) {
+        if (h->stage_acc[i]) cudaFreeHost(h->stage_acc[i]);
+        if (h->stage_bf[i]) cudaFreeHost(h->stage_bf[i]);
+        if (h->ev_d2h[i]) cudaEventDestroy(h->ev_d2h[i]);
+        if (h->ev_h2d[i]) cudaEventDestroy(h->ev_h2d[i]);
+        h->stage_acc[i] = nullptr;
+        h->stage_bf[i] = nullptr;
+        h->ev_d2h[i] = h->ev_h2d[i] = nullptr;
+    }
+    if (h->stage_step) cudaFreeHost(h->stage_step);
+    if (h->stage_norm) cudaFreeHost(h->stage_norm);
+    h->stage_step = nullptr;
+    h->stage_norm = nullptr;
+    delete h->pool;
+    h->pool = nullptr;
+}
+
 void free_scratch(bf16opt_t *h) {
+    free_offload(h);
     if (h->segs_d) cudaFree(h->segs_d);
     if (h->chunks_d) cudaFree(h->chunks_d);
     if (h->partials_d) cudaFree(h->partials_d);
@@ -354,6 +387,81 @@ cudaError_t upload_params(bf16opt_t *h) {
     p.min_ratio = h->sched.min_lr_ratio;
     p.skip_nonfinite = h->skip_nonfinite ? 1 : 0;
     return cudaMemcpy(h->params_d, &p, sizeof p, cudaMemcpyHostToDevice);
+}
+
+// Elements per block of the offloaded step's pipeline: the accumulator of
+// block k + 1 is copied to the host while the host cores update block k, and
+// the bf16 parameters of block k go back to the device while block k + 1 is
+// updated.  2^24 elements: 64 MiB + 32 MiB of page-locked staging per buffer.
+constexpr uint64_t kOffloadBlock = uint64_t(1) << 24;
+
+// The step of an offload handle: the scalars, the step counter and the skip
+// decision come from the same device kernel as the device step; the update
+// itself runs on the host over the host-resident master and moments.
+int offload_step(bf16opt_t *h, const LrOverride &ov, cudaStream_t st) {
+    if (!h->pend_flat.empty()) {      // fold micro-batches still deferred: the host reads a complete accumulator
+        int rc = launch_accum<true, false>(h, h->acc_valid, pending_set(h), st);
+        if (rc) return rc;
+        h->acc_valid = true;
+        h->pend_flat.clear();
+    }
+    cudaError_t e = launch(h, k_step_scalars, 1, 32, st, (const StepParams *)h->params_d, h->step_d, ov,
+                           (const NormState *)h->norm_d);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->stage_step, h->step_d, sizeof(StepState), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->stage_norm, h->norm_d, sizeof(NormState), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "offloaded step: step scalars");
+    if (h->stage_step->skip) return BF16OPT_OK;        // non-finite norm, skipping enabled
+    const float c_hi = h->stage_norm->c_hi, c_lo = h->stage_norm->c_lo;
+    bf16host::HostGroup G[kMaxGroups];
+    for (size_t g = 0; g < h->groups.size(); ++g) {
+        const GroupK &k = h->stage_step->gtab.g[g];
+        G[g] = {k.b1, k.omb1, k.b2, k.omb2, k.eps, k.decay, k.step_size, k.inv_sqrt_bc2};
+    }
+    const uint64_t n = h->n, nb = (n + kOffloadBlock - 1) / kOffloadBlock;
+    auto fetch = [&](uint64_t k) {
+        const uint64_t lo = k * kOffloadBlock, len = std::min(kOffloadBlock, n - lo);
+        cudaError_t r = cudaMemcpyAsync(h->stage_acc[k & 1], h->dev_acc + lo, len * sizeof(float),
+                                        cudaMemcpyDeviceToHost, st);
+        return r == cudaSuccess ? cudaEventRecord(h->ev_d2h[k & 1], st) : r;
+    };
+    if (nb > 0 && (e = fetch(0)) != cudaSuccess) return cuda_fail(h, e, "offloaded step: copy to host");
+    for (uint64_t k = 0; k < nb; ++k) {
+        const uint64_t lo = k * kOffloadBlock, len = std::min(kOffloadBlock, n - lo);
+        if (k + 1 < nb && (e = fetch(k + 1)) != cudaSuccess) return cuda_fail(h, e, "offloaded step: copy to host");
+        // this block's gradient has arrived; its bf16 staging buffer (two blocks
+        // ago, or the previous step) has been copied out
+        if ((e = cudaEventSynchronize(h->ev_d2h[k & 1])) != cudaSuccess ||
+            (e = cudaEventSynchronize(h->ev_h2d[k & 1])) != cudaSuccess)
+            return cuda_fail(h, e, "offloaded step: waiting for a copy");
+        const float *acc = h->stage_acc[k & 1];
+        uint16_t *bf = h->stage_bf[k & 1];
+        h->pool->run([&](int w, int nw) {
+            const uint64_t a = lo + len * (uint64_t)w / (uint64_t)nw, b = lo + len * (uint64_t)(w + 1) / (uint64_t)nw;
+            for (const Seg &sg : h->segs) {
+                const uint64_t s0 = std::max(a, sg.grad_off), s1 = std::min(b, sg.grad_off + sg.numel);
+                if (s0 < s1)
+                    bf16host::adam_range(acc + (s0 - lo), h->host_p + s0, h->host_m + s0, h->host_v + s0,
+                                         bf + (s0 - lo), s1 - s0, h->gscale, c_hi, c_lo, G[sg.group]);
+            }
+        });
+        if ((e = cudaMemcpyAsync(h->dev_bf + lo, bf, len * sizeof(uint16_t), cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+            (e = cudaEventRecord(h->ev_h2d[k & 1], st)) != cudaSuccess)
+            return cuda_fail(h, e, "offloaded step: copy to device");
+    }
+    return BF16OPT_OK;
+}
+
+// cudaPointerGetAttributes' kind of p; cudaMemoryTypeUnregistered when it fails.
+cudaMemoryType memory_kind(const void *p, int *device) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaMemoryTypeUnregistered;
+    }
+    if (device) *device = a.device;
+    return a.type;
 }
 
 }  // namespace
@@ -566,6 +674,64 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
         g_live.insert(h);
     }
     g_create_error.clear();
+    *out = h;
+    return BF16OPT_OK;
+}
+
+int bf16opt_create_offload(const bf16opt_desc_t *d, int n_threads, bf16opt_t **out) {
+    NvtxRange nvtx("bf16opt_create_offload");
+    if (out) *out = nullptr;
+    if (!d || !out) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "desc and out must be non-NULL");
+    if (d->mode != BF16OPT_FLAT) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "offload: FLAT mode only");
+    bf16opt_t *h = nullptr;
+    int rc = bf16opt_create(d, &h);      // validates the descriptor, builds the tables and the device scratch
+    if (rc) return rc;
+    auto bail = [&](int code, const std::string &msg) {
+        bf16opt_destroy(h);
+        return fail(nullptr, code, msg);
+    };
+    if (d->n > 0) {
+        // master and moments: host memory the host threads read and write;
+        // accumulator and bf16 parameters: memory of the handle's device
+        for (const void *p : {(const void *)d->master, (const void *)d->exp_avg, (const void *)d->exp_avg_sq}) {
+            const cudaMemoryType k = memory_kind(p, nullptr);
+            if (k != cudaMemoryTypeUnregistered && k != cudaMemoryTypeHost)
+                return bail(BF16OPT_ERR_INVALID_ARG, "offload: master, exp_avg and exp_avg_sq must be host memory");
+        }
+        for (const void *p : {(const void *)d->grad_accum, (const void *)d->param_bf16}) {
+            int dev = -1;
+            if (memory_kind(p, &dev) != cudaMemoryTypeDevice || dev != h->device)
+                return bail(BF16OPT_ERR_INVALID_ARG, "offload: grad_accum and param_bf16 must be memory of the current device");
+        }
+    }
+    h->offload = true;
+    h->host_p = d->master;
+    h->host_m = d->exp_avg;
+    h->host_v = d->exp_avg_sq;
+    h->dev_acc = d->grad_accum;
+    h->dev_bf = d->param_bf16;
+    const uint64_t blk = std::max<uint64_t>(1, std::min<uint64_t>(kOffloadBlock, d->n));
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        if ((e = cudaMallocHost(&h->stage_acc[i], blk * sizeof(float))) == cudaSuccess &&
+            (e = cudaMallocHost(&h->stage_bf[i], blk * sizeof(uint16_t))) == cudaSuccess &&
+            (e = cudaEventCreateWithFlags(&h->ev_d2h[i], cudaEventDisableTiming)) == cudaSuccess)
+            e = cudaEventCreateWithFlags(&h->ev_h2d[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess && (e = cudaMallocHost(&h->stage_step, sizeof(StepState))) == cudaSuccess)
+        e = cudaMallocHost(&h->stage_norm, sizeof(NormState));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return bail(e == cudaErrorMemoryAllocation ? BF16OPT_ERR_OOM : BF16OPT_ERR_CUDA,
+                    std::string("offload staging: ") + cudaGetErrorString(e));
+    }
+    int nt = n_threads;
+    if (nt <= 0) nt = (int)std::max(1u, std::thread::hardware_concurrency());
+    try {
+        h->pool = new bf16host::Pool(std::min(nt, 256));
+    } catch (...) {
+        return bail(BF16OPT_ERR_OOM, "offload: cannot start the host threads");
+    }
     *out = h;
     return BF16OPT_OK;
 }
@@ -845,6 +1011,15 @@ int bf16opt_step(bf16opt_t *h, const float *lr_override, void *stream) {
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
     cudaStream_t st = (cudaStream_t)stream;
+    if (h->offload) {
+        int rc = offload_step(h, ov, st);
+        if (rc) return rc;
+        h->state = S_IDLE;
+        h->acc_valid = false;
+        h->pend_flat.clear();
+        h->scalars_ready = false;
+        return BF16OPT_OK;
+    }
     // The norm kernel prepared the scalars of step t + 1 with the groups' own
     // learning rates; the step kernel then advances t itself.  A learning-rate
     // override, a setting changed since the norm, or an empty shard take one

@@ -35,12 +35,23 @@ def _check_buffer(t, what, dtypes, numel=None):
         raise ValueError(f"{what}: {t.numel()} elements, expected {numel}")
 
 
-def _check_state(d, what):
+def _check_state(d, what, offload=False):
     n = d["master"].numel()
     for k in ("master", "exp_avg", "exp_avg_sq", "grad_accum"):
-        _check_buffer(d[k], f"{what}[{k!r}]", (torch.float32,), n)
+        if offload and k != "grad_accum":
+            _check_host_buffer(d[k], f"{what}[{k!r}]", n)
+        else:
+            _check_buffer(d[k], f"{what}[{k!r}]", (torch.float32,), n)
     _check_buffer(d["param_bf16"], f"{what}['param_bf16']", _BF16_BITS, n)
     return n
+
+
+def _check_host_buffer(t, what, numel):
+    """An FP32 host tensor the library's host threads read and write (offload)."""
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{what}: must be a CPU tensor (offloaded state)")
+    if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{what}: must be a contiguous float32 tensor of {numel} elements")
 
 
 def _stream_handle(stream):
@@ -157,12 +168,19 @@ class BF16Optimizer:
     """One handle over a FLAT shard (`flat` = dict of the five tensors, `ranges`)
     or a LIST of tensors (`tensors` = list of such dicts with a "group" key)."""
 
-    def __init__(self, groups, flat=None, ranges=None, tensors=None, max_grad_norm=1.0, grad_scale=1.0):
+    def __init__(self, groups, flat=None, ranges=None, tensors=None, max_grad_norm=1.0, grad_scale=1.0,
+                 offload=False, offload_threads=0):
+        """offload=True (FLAT only): ZeRO-Offload -- flat master, exp_avg and
+        exp_avg_sq are CPU tensors updated by offload_threads host threads
+        (0: one per core); grad_accum and param_bf16 stay on the GPU."""
         if (flat is None) == (tensors is None):
             raise ValueError("give exactly one of flat= or tensors=")
+        if offload and flat is None:
+            raise ValueError("offload needs a FLAT shard (flat=)")
         self.groups = [dict(g) for g in groups]
+        self.offload = bool(offload)
         if flat is not None:
-            n = _check_state(flat, "flat")
+            n = _check_state(flat, "flat", offload=self.offload)
             self.n, self.numels = n, None
             self.desc = C.flat_desc(n, _ptr(flat["master"]), _ptr(flat["exp_avg"]), _ptr(flat["exp_avg_sq"]),
                                     _ptr(flat["grad_accum"]), _ptr(flat["param_bf16"]), self.groups, ranges,
@@ -178,7 +196,10 @@ class BF16Optimizer:
         self._state = [flat] if flat is not None else list(tensors)
         self._sched_args = None
         self._skip = False
-        rc, self.h = C.bf16opt_create(self.desc)
+        if self.offload:
+            rc, self.h = C.bf16opt_create_offload(self.desc, offload_threads)
+        else:
+            rc, self.h = C.bf16opt_create(self.desc)
         C.check(rc, None)
 
     @classmethod

@@ -116,6 +116,30 @@ def test_create_validation(lib, desc, code):
     assert C.bf16opt_last_error(None)
 
 
+def test_offload_create_validation(lib):
+    """The offload variant validates its descriptor like bf16opt_create, before
+    any CUDA call, and takes FLAT shards only."""
+    for d in (flat(groups=[dict(G[0], beta1=1.0)]), flat(master=BASE + 2)):
+        rc, h = C.bf16opt_create_offload(d)
+        assert rc in (C.BF16OPT_ERR_INVALID_ARG, C.BF16OPT_ERR_ALIGNMENT) and not h.value
+    lst = C.list_desc([(BASE, BASE + 4096, BASE + 8192, BASE + 12288, BASE + 16384, 1000, 0)], G)
+    rc, h = C.bf16opt_create_offload(lst)
+    assert rc == C.BF16OPT_ERR_INVALID_ARG and "FLAT" in C.bf16opt_last_error(None) and not h.value
+    h = ctypes.c_void_p()
+    assert lib.bf16opt_create_offload(None, 0, ctypes.byref(h)) == C.BF16OPT_ERR_INVALID_ARG
+
+
+def test_rank_sum_is_rank_ordered(lib):
+    """bf16opt_sum_rank_sumsqs adds the per-rank values left to right in FP64
+    (host only): here the order decides the result."""
+    assert C.bf16opt_sum_rank_sumsqs([1.0, 1e-16, -1.0]) == (0, 0.0)
+    assert C.bf16opt_sum_rank_sumsqs([1e-16, 1.0, -1.0]) == (0, 0.0)
+    assert C.bf16opt_sum_rank_sumsqs([1.0, -1.0, 1e-16]) == (0, 1e-16)
+    assert C.bf16opt_sum_rank_sumsqs([]) [0] == C.BF16OPT_ERR_INVALID_ARG
+    assert C.bf16opt_sum_rank_sumsqs([2.5]) == (0, 2.5)
+    assert C.bf16opt_set_rank_sumsqs(None, [1.0], 0)[0] == C.BF16OPT_ERR_INVALID_ARG
+
+
 def test_null_arguments(lib):
     h = ctypes.c_void_p()
     assert lib.bf16opt_create(None, ctypes.byref(h)) == C.BF16OPT_ERR_INVALID_ARG
