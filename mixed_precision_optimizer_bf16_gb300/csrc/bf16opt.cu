@@ -155,14 +155,27 @@ bool overlaps(std::vector<Interval> &iv) {
 
 // Elements per chunk of a shard of `total` elements: kChunk from 2^25
 // elements up; smaller shards get proportionally smaller chunks (a power of
-// two, at least kMinChunk), so that they still spread over every SM -- a
-// 1M-element shard in 32,768-element chunks kept 32 of 152 SMs busy.  Depends
-// only on the shard's size, never on the GPU.
+// two, at least kMinChunk) so that they still spread over every SM -- about
+// kChunkTarget chunks (a 1M-element shard in 32,768-element chunks kept 32 of
+// 152 SMs busy), or about kSmallChunkTarget on shards of at most
+// kSmallShard elements, where a pass is one wave of CTAs and a CTA that walks
+// several short chunks pays their descriptor loads one after another.
+// Depends only on the shard's size, never on the GPU.
+#ifndef BF16K_CHUNK_TARGET
+#define BF16K_CHUNK_TARGET 1024
+#endif
+#ifndef BF16K_SMALL_CHUNK_TARGET
+#define BF16K_SMALL_CHUNK_TARGET 1024
+#endif
+#ifndef BF16K_SMALL_SHARD
+#define BF16K_SMALL_SHARD (uint64_t(1) << 22)
+#endif
 constexpr uint32_t kMinChunk = 2048;
 static_assert(kMinChunk % kHeadAlign == 0 && kMinChunk <= kChunk, "chunk sizes are multiples of kHeadAlign");
 uint32_t chunk_elems(uint64_t total) {
+    const uint64_t target = total <= BF16K_SMALL_SHARD ? BF16K_SMALL_CHUNK_TARGET : BF16K_CHUNK_TARGET;
     uint64_t c = kMinChunk;
-    while (c < kChunk && c * 1024 < total) c <<= 1;
+    while (c < kChunk && c * target < total) c <<= 1;
     return (uint32_t)c;
 }
 
@@ -903,7 +916,7 @@ int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream) {
     if (h->state != S_LOCAL_NORMED) return fail(h, BF16OPT_ERR_SEQUENCE, "set_global_sumsq needs grad_norm_local first");
     DeviceGuard dg(h->device);
     if (!dg.ok) return fail(h, BF16OPT_ERR_CUDA, "cannot select the handle's device");
-    cudaError_t e = launch(h, k_norm_from_sumsq, 1, 32, (cudaStream_t)stream, global_sumsq, h->max_norm, h->norm_d,
+    cudaError_t e = launch(h, k_norm_from_sumsq, 1, 64, (cudaStream_t)stream, global_sumsq, h->max_norm, h->norm_d,
                            (const StepParams *)h->params_d, h->step_d);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(h, e, "norm kernel launch");

@@ -582,6 +582,20 @@ __device__ __forceinline__ void store_norm_state(const NormClip &r, NormState *_
     out->pad = 0;
 }
 
+// b^t for an integer t >= 0 by binary exponentiation in FP64: about 2 log2(t)
+// multiplications (GB300's FP64 pipe is slow; a general pow costs far more),
+// a fixed function of t, so every path that reaches step t -- eager, replayed
+// graph, resumed run -- gets the same bits.  Relative error below
+// 2 log2(t) units of 2^-53, far inside what the FP32 scalars keep.
+__device__ __forceinline__ double pow_int(double b, int64_t t) {
+    double r = 1.0, x = b;
+    for (uint64_t e = (uint64_t)t; e != 0; e >>= 1) {
+        if (e & 1) r *= x;
+        x *= x;
+    }
+    return r;
+}
+
 // The per-group FP32 scalars of step t, computed in FP64 from the FP32
 // hyper-parameters: bias corrections 1 - b^t (Kingma & Ba, Algorithm 1),
 // step_size = lr / bc1, 1 / sqrt(bc2), decay = lr * wd, with lr times the
@@ -602,8 +616,8 @@ __device__ __forceinline__ void group_scalars(const StepParams *__restrict__ P, 
     }
     const double lr = (double)lr_g * f;
     const double b1 = (double)P->beta1[g], b2 = (double)P->beta2[g];
-    const double bc1 = 1.0 - pow(b1, (double)t);
-    const double bc2 = 1.0 - pow(b2, (double)t);
+    const double bc1 = 1.0 - pow_int(b1, t);
+    const double bc2 = 1.0 - pow_int(b2, t);
     o.b1 = (float)b1;
     o.omb1 = (float)(1.0 - b1);
     o.b2 = (float)b2;
@@ -627,23 +641,25 @@ __device__ __forceinline__ void prepare_step(const StepParams *__restrict__ P, S
 
 // Sum of the chunk partials in a fixed order, then norm and clip coefficient,
 // and the scalars of the step that follows.
+// Warp 0 computes the group scalars, warp 1 the norm and clip coefficient, at
+// the same time.
 __global__ void __launch_bounds__(kFinalThreads)
 k_norm_final(const double *__restrict__ partials, uint32_t n, float max_norm, NormState *__restrict__ out,
              const StepParams *__restrict__ P, StepState *S) {
     __shared__ double sh[kFinalThreads];
     pdl_enter();
     const double sumsq = final_sum(partials, n, sh);
-    prepare_step(P, S, sumsq);
-    if (threadIdx.x == 0) store_norm_state(norm_and_clip(sumsq, max_norm), out);
+    if (threadIdx.x < 32) prepare_step(P, S, sumsq);
+    else if (threadIdx.x == 32) store_norm_state(norm_and_clip(sumsq, max_norm), out);
 }
 
 // Norm and clip coefficient from a sum of squares given by the host (the
-// all-rank sum under ZeRO): same formula as k_norm_final.  One warp.
+// all-rank sum under ZeRO): same formula as k_norm_final.  Two warps.
 __global__ void k_norm_from_sumsq(double sumsq, float max_norm, NormState *__restrict__ out,
                                   const StepParams *__restrict__ P, StepState *S) {
     pdl_enter();
-    prepare_step(P, S, sumsq);
-    if (threadIdx.x == 0) store_norm_state(norm_and_clip(sumsq, max_norm), out);
+    if (threadIdx.x < 32) prepare_step(P, S, sumsq);
+    else if (threadIdx.x == 32) store_norm_state(norm_and_clip(sumsq, max_norm), out);
 }
 
 // t <- t + 1 (unless the step is skipped) and the per-group scalars of step t
