@@ -165,7 +165,7 @@ bool overlaps(std::vector<Interval> &iv) {
 #define BF16K_CHUNK_TARGET 1024
 #endif
 #ifndef BF16K_SMALL_CHUNK_TARGET
-#define BF16K_SMALL_CHUNK_TARGET 1024
+#define BF16K_SMALL_CHUNK_TARGET 128
 #endif
 #ifndef BF16K_SMALL_SHARD
 #define BF16K_SMALL_SHARD (uint64_t(1) << 22)
