@@ -129,6 +129,24 @@ def test_offload_create_validation(lib):
     assert lib.bf16opt_create_offload(None, 0, ctypes.byref(h)) == C.BF16OPT_ERR_INVALID_ARG
 
 
+def test_static_norm_without_device_touches_nothing(lib):
+    """Without a GPU the allocation-free norm refuses before any pointer is used
+    (host arrays here stand for memory a kernel could not reach); argument
+    errors are reported first, as with a device."""
+    import numpy as np
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    acc, out = np.ones(1000, np.float32), np.zeros(3, np.float64)
+    assert C.bf16opt_grad_norm_static(acc.ctypes.data, acc.size, 1.0, 1.0, out.ctypes.data) == \
+        C.BF16OPT_ERR_UNSUPPORTED
+    assert out.tolist() == [0.0, 0.0, 0.0]
+    assert C.bf16opt_grad_norm_static(acc.ctypes.data, acc.size, 1.0, 1.0, out.ctypes.data + 4) == \
+        C.BF16OPT_ERR_ALIGNMENT
+    assert C.bf16opt_grad_norm_static(acc.ctypes.data, C.BF16OPT_STATIC_NORM_MAX_ELEMS + 1, 1.0, 1.0,
+                                      out.ctypes.data) == C.BF16OPT_ERR_INVALID_ARG
+
+
 def test_rank_sum_is_rank_ordered(lib):
     """bf16opt_sum_rank_sumsqs adds the per-rank values left to right in FP64
     (host only): here the order decides the result."""
