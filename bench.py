@@ -15,8 +15,10 @@ measured HBM copy peak; `cpu_baseline` is the CPU oracle on a bounded sample
 (rank 0 of a 1-GPU run only).
 `--impl reference` times that oracle instead, as the reference arm.
 
-Multi-GPU (torchrun): every rank runs an independent replica of the shard
-(no collective on the data path: replicas only), timing is max over ranks.
+Multi-GPU (torchrun): every rank steps its own shard as one partition of a
+larger model (weak scaling) and all ranks clip by the global norm: one FP64
+sum of squares per rank is all-gathered each step (NCCL) and summed in rank
+order by the library; timing is max over ranks.
 """
 import argparse
 import hashlib
@@ -221,6 +223,17 @@ class Clocks:
 
 # ------------------------------------------------------------------ our arm
 
+def global_norm(opt, world, stream, sync=False):
+    """The step's clipping norm.  One rank: the shard's own.  Several ranks:
+    every rank owns one partition (its own shard: weak scaling) and all clip by
+    the global norm -- this partition's FP64 sum of squares is all-gathered
+    (one scalar per rank, the only exchange on the path) and the library sums
+    the values in rank order."""
+    if world > 1:
+        return opt.grad_norm_distributed(stream=stream)
+    return opt.grad_norm(stream=stream, sync=sync)
+
+
 def build_shard(wl, dev):
     """A workload's device state and one bf16 gradient buffer per micro-batch
     (seeded masters and step-0 gradients, m = v = 0), and its optimizer handle.
@@ -291,7 +304,7 @@ def extra_workload(wl_id, steps, warmup, dev, world, peak, no_clocks):
         def one():
             for k in range(G):
                 opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=pat[k], stream=stream)
-            opt.grad_norm(stream=stream)
+            global_norm(opt, world, stream)
             opt.step(stream=stream)
         for _ in range(warmup):
             one()
@@ -405,7 +418,7 @@ def run_ours(args):
             opt.accumulate(grads[k], first=k == 0, last=k == G - 1, defer=pat[k], stream=stream)
             if ev is not None:
                 ev[1 + k].record(stream)
-        opt.grad_norm(stream=stream)
+        global_norm(opt, world, stream)
         if ev is not None:
             ev[G + 1].record(stream)
         opt.step(stream=stream)
@@ -448,7 +461,7 @@ def run_ours(args):
 
     # variant: the same step captured once as a CUDA graph and replayed (the
     # step scalars live on the device, so replays are later steps)
-    if not args.no_variant:
+    if not args.no_variant and world == 1:   # a multi-rank step waits for the ranks' norms on the host
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             cs = torch.cuda.current_stream(dev)
@@ -503,7 +516,7 @@ def run_ours(args):
                     + "; same FP32 adds in the same order"}}
     if graph_variant is not None:
         variant = dict(variant or {}, cuda_graph_replay=graph_variant)
-    if not args.no_variant and not args.no_offload:
+    if not args.no_variant and not args.no_offload and world == 1:   # host cores are shared by the ranks
         off = offload_variant(wl, dev, 5)
         if off is not None:
             variant = dict(variant or {}, zero_offload=off)
@@ -576,7 +589,8 @@ def run_ours(args):
         "config": {"workload": wl.name, "elements": n, "tensors": len(wl.tensors), "groups": groups_used(wl), "gas": G,
                    "mode": f"{wl.mode}; " + ("last micro-batch deferred into the fused step" if defer else "norm fused into last accumulate"),
                    "bytes_per_elem_per_step": sum(bpe.values()), "hbm_gbs_per_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
-                   "l2": l2_note, "parallelism": f"replicas x{world}"},
+                   "l2": l2_note,
+                   "parallelism": f"ZeRO partitions x{world}, global-norm all-gather per step" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "kernel": "k_step (fused clip+AdamW+master+bf16)", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes_per_launch": bpe["step"] * n},
@@ -645,7 +659,7 @@ def run_e2e(args, opt, grads, G, defer, dev, world, n):
             if not (defer and k == G - 1):
                 free[k] = torch.cuda.Event()
                 free[k].record(comp)
-        norm = opt.grad_norm(stream=comp, sync=True)
+        norm = global_norm(opt, world, comp, sync=True)
         opt.step(stream=comp)
         if defer:
             free[G - 1] = torch.cuda.Event()
