@@ -271,8 +271,8 @@ int bf16opt_set_global_sumsq(bf16opt_t *h, double global_sumsq, void *stream);
  * once on a stream, replays as later steps (same gradient buffers; lr_override
  * values are frozen into the capture).  Calls that synchronise (grad_norm with
  * host_norm, grad_norm_local, get/set_step, set_lr_schedule,
- * set_skip_nonfinite, debug_faults, create, destroy) must stay outside a
- * capture. */
+ * set_skip_nonfinite, debug_faults, create, create_offload, destroy, and step
+ * on an offload handle) must stay outside a capture. */
 
 /* One fused pass: clip, AdamW (t = t + 1, bias-corrected, decoupled
  * weight decay), FP32 master/moment update and bf16 parameter write

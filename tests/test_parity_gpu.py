@@ -124,8 +124,13 @@ def test_small_ragged_variants(case, mode, defer):
 
 
 @needs_cuda
-def test_list_more_tensors_than_one_launch():
-    """1100 tensors (> 1024 gradient pointers per launch): two launches per pass."""
+@pytest.mark.parametrize("sched", ["auto", "claim"])
+def test_list_more_tensors_than_one_launch(sched, monkeypatch):
+    """1100 tensors (> 1024 gradient pointers per launch): two launches per pass
+    (three with two pointers per tensor) -- with claiming forced on, the
+    launches of one pass share the chunk counter one after another."""
+    if sched == "claim":
+        monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
     rng = np.random.default_rng(5)
     sizes = rng.integers(1, 700, 1100).tolist()
     wl = workloads.custom(150, sizes, decay=[i % 2 == 0 for i in range(1100)], gas=2, steps=2,
