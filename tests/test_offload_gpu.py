@@ -140,3 +140,55 @@ def test_offload_skips_a_nonfinite_step_and_rejects_wrong_memory():
                                                        "param_bf16")), wl.groups)
     assert C.bf16opt_create_offload(desc)[0] == C.BF16OPT_ERR_INVALID_ARG
     assert "current device" in C.bf16opt_last_error(None)
+
+
+@needs_cuda
+def test_offload_checkpoint_resume():
+    """state_dict / load_state_dict of an offload optimizer (host master and
+    moments, device bf16 parameters): dump after one step, restore into fresh
+    buffers, continue -- the same bits as an uninterrupted run."""
+    wl = workloads.custom(973, [30_001, 999], decay=[True, False], gas=2, steps=3, grad_sigma=0.2)
+    pattern = [False, True]
+    full = OffloadShard(wl, pattern)
+    full.run(wl.steps)
+    want = full.states()
+    full.opt.close()
+
+    a = OffloadShard(wl, pattern)
+    a.run(1)
+    sd = a.opt.state_dict()
+    a.opt.close()
+    b = OffloadShard(wl, pattern)
+    b.opt.load_state_dict(sd)
+    for s in range(1, wl.steps):
+        for k in range(wl.gas):
+            buf = b.gbufs[k % len(b.gbufs)]
+            sgpu.fill_grad(wl, s, k, buf)
+            b.opt.accumulate(buf, first=k == 0, last=k == wl.gas - 1, defer=pattern[k])
+        b.opt.grad_norm()
+        b.opt.step()
+    torch.cuda.synchronize()
+    assert b.opt.t == wl.steps
+    _same_bits(b.states(), want)
+    b.opt.close()
+
+
+@needs_cuda
+def test_reduce_scatter_without_a_process_group():
+    """accumulate_reduce_scatter with no process group initialised: one rank,
+    the whole buffer is its partition, the same as plain accumulate calls."""
+    wl = workloads.custom(974, [20_000, 77], decay=[True, False], gas=3, steps=2, grad_sigma=0.1)
+    dev = GpuShard(wl, defer=[False, False, True])
+    dev.run(wl.steps)
+    want = dev.states()
+    dev.close()
+    sh = GpuShard(wl, defer=False)
+    for s in range(wl.steps):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, sh.gbuf)
+            sh.opt.accumulate_reduce_scatter(sh.gbuf, first=k == 0, last=k == wl.gas - 1)
+        sh.opt.grad_norm_distributed()
+        sh.opt.step()
+    torch.cuda.synchronize()
+    _same_bits(sh.states(), want)
+    sh.close()

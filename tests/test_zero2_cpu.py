@@ -97,3 +97,33 @@ def test_zero2_exchange_and_rank_ordered_fold_gloo():
         for S, S_ref in zip(r[2], ref["sumsq"]):
             assert abs(S - S_ref) <= 1e-14 * S_ref
     compare(got, ref, scales, wl)    # accumulator bit for bit, states within the tolerance
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 7, 8, 9, 16, 17])
+@pytest.mark.parametrize("last", [False, True])
+def test_fold_pattern_keeps_the_library_limits(world, last):
+    """The received slices ride on DEFER: never more than 8 pending (the
+    library's limit), a non-last micro-batch folds all of its slices by its
+    final one (so the receive buffer can be reused), and the last micro-batch
+    leaves at most 8 deferred into the norm pass and the step."""
+    from mixed_precision_optimizer_bf16_gb300.optimizer import fold_pattern
+    flags = fold_pattern(world, last)
+    assert len(flags) == world
+    pending = 0
+    for f in flags:
+        pending = pending + 1 if f else 0
+        assert pending <= 8
+    if not last:
+        assert flags[-1] is False
+    else:
+        assert flags[-1] is True and pending == (world % 8 or 8) if world > 8 else all(flags)
+
+
+def test_partition_bounds():
+    from mixed_precision_optimizer_bf16_gb300.optimizer import partition_bounds
+    assert partition_bounds(10, 3) == [0, 4, 8, 10]
+    assert partition_bounds(12, 4) == [0, 3, 6, 9, 12]
+    assert partition_bounds(5, 8) == [0, 1, 2, 3, 4, 5, 5, 5, 5]
+    for n, w in ((1_722_408_960, 8), (7, 7), (1, 1)):
+        b = partition_bounds(n, w)
+        assert b[0] == 0 and b[-1] == n and all(x <= y for x, y in zip(b, b[1:]))
