@@ -334,7 +334,7 @@ def compare(gpu, ref, scales, wl, grad_scale=1.0, check_acc=True):
     """Element-wise parity; returns a stats dict, raises AssertionError on a breach.
 
     Elements whose FP32 bits equal the oracle's need no tolerance arithmetic;
-    the bounds are evaluated on the others only (same verdict, less work on
+    the bounds are evaluated on the others only (same outcome, less work on
     multi-GB shards)."""
     stats = {}
     if check_acc is not False:
