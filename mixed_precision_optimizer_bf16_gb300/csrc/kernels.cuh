@@ -9,17 +9,21 @@
 //                    micro-batches);
 //   k_norm_final     fixed-order FP64 sum of the chunk partials, norm and clip
 //                    coefficient ("企业官网建设流程全解析" (cf-1.com), section 4.3: global
-//                    norm clipped at 1.0);
+//                    norm clipped at 1.0), and the next step's per-group AdamW
+//                    scalars and skip decision;
 //   k_norm_from_sumsq the same from an all-rank sum handed in by the host (ZeRO);
-//   k_step_scalars   t <- t + 1 and the per-group AdamW scalars of step t;
+//   k_step_scalars   t <- t + 1 and the scalars of step t again, for a step with a
+//                    learning-rate override or settings changed since the norm;
 //   k_step           clip x AdamW x FP32 master/moment update x bf16 cast in one pass
-//                    ("企业官网建设流程全解析", sections 1 and 3.3).
+//                    ("企业官网建设流程全解析", sections 1 and 3.3); advances the step
+//                    counter when the norm kernel prepared the scalars.
 //
 // Work decomposition.  A segment is one run of elements with one parameter
 // group and one set of base pointers (a flat range or a list tensor).  The
 // host cuts each segment into chunks of at most kChunk elements (the first one
 // shortened so that later chunks start on a 128-byte line of the master
-// buffer); a persistent grid strides over the chunk table.  Inside a chunk,
+// buffer); a persistent grid takes the chunks by a fixed stride or claims them
+// from a counter (see the chunk schedule below).  Inside a chunk,
 // thread t handles 4-element quads t, t+T, ... so that every warp-wide access
 // is contiguous: FP32 as 16-byte and bf16 as 8-byte vectors.  Leading elements
 // up to the lead pointer's next kHeadAlign-element boundary, and the ragged
@@ -29,7 +33,8 @@
 //
 // Determinism.  The norm's partial of chunk c depends only on the chunk's
 // data and on the fixed thread->element map, so the result does not depend
-// on the grid size or on scheduling; the final sum runs in chunk order.
+// on the grid size, on scheduling or on which CTA takes which chunk; the final
+// sum runs in chunk order.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -116,7 +121,8 @@ struct NormState {
     int32_t pad;
 };
 
-// Per-group scalars of one step, FP32, computed in FP64 by k_step_scalars.
+// Per-group scalars of one step, FP32, computed in FP64 on the device
+// (group_scalars: by the norm kernel, or by k_step_scalars).
 struct GroupK {
     float b1, omb1, b2, omb2;
     float eps;
