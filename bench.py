@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--extra", default="3,4", help="other workloads timed after the headline one ('' = none)")
     ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--no-offload", action="store_true", help="skip the ZeRO-Offload variant")
+    ap.add_argument("--no-probe", action="store_true", help="skip the HBM bandwidth probe")
     return ap.parse_args()
 
 
@@ -570,6 +571,17 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
 
+    # the bandwidth each traffic mix reaches on this GPU, measured in this run:
+    # the ceiling the kernels are set against (the roofline's peak stays the
+    # measured copy in MEASURED_PEAKS.json)
+    probe = None
+    if not args.no_probe and not args.elements:
+        from mixed_precision_optimizer_bf16_gb300 import hbm_probe
+        probe = hbm_probe.measure(device=dev)
+        probe["step_kernel_of_step_mix"] = round(achieved / probe["step_mix_gbs"], 4)
+        probe["note"] = ("16-byte-vector streaming kernels, chunks claimed: copy 1:1, write-only, read-only, "
+                         "and the fused step's 18:14 read:write mix with no arithmetic")
+
     # the other single-GPU target shards, timed by the same run (config freed first)
     extra = None
     if args.extra and not args.elements:
@@ -615,6 +627,7 @@ def run_ours(args):
         "norm_and_step": norm_and_step,
         "variants": variant,
         "workloads": extra,
+        "hbm_probe": probe,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,

@@ -11,6 +11,10 @@ DEPS = SOURCES + [os.path.join(HERE, "csrc", "kernels.cuh"), os.path.join(HERE, 
 
 # -ffp-contract=off: host code rounds every product on its own (the offloaded
 # step's host update repeats the device kernel's operations exactly)
+PROBE_LIB_PATH = os.path.join(HERE, "libhbmprobe.so")
+PROBE_SOURCES = [os.path.join(HERE, "csrc", "hbm_probe.cu")]
+PROBE_DEPS = PROBE_SOURCES + [os.path.join(ROOT, "include", "hbm_probe.h")]
+
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off", "-shared"]
 
@@ -29,6 +33,17 @@ def _stale(out, deps):
 
 def build_cmd(extra=(), out=None):
     return [nvcc()] + NVCC_FLAGS + list(extra) + ["-I", os.path.join(ROOT, "include"), "-o", out or LIB_PATH] + SOURCES
+
+
+def build_probe_cmd():
+    return [nvcc()] + NVCC_FLAGS + ["-I", os.path.join(ROOT, "include"), "-o", PROBE_LIB_PATH] + PROBE_SOURCES
+
+
+def build_probe(force=False):
+    """Compile libhbmprobe.so (the HBM bandwidth probe) if missing or stale."""
+    if force or _stale(PROBE_LIB_PATH, PROBE_DEPS):
+        subprocess.run(build_probe_cmd(), check=True)
+    return PROBE_LIB_PATH
 
 
 def build_checked(out):
