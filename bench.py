@@ -579,8 +579,21 @@ def run_ours(args):
         from mixed_precision_optimizer_bf16_gb300 import hbm_probe
         probe = hbm_probe.measure(device=dev)
         probe["step_kernel_of_step_mix"] = round(achieved / probe["step_mix_gbs"], 4)
-        probe["note"] = ("16-byte-vector streaming kernels, chunks claimed: copy 1:1, write-only, read-only, "
-                         "and the fused step's 18:14 read:write mix with no arithmetic")
+        # every pass against the ceiling of its own read:write mix
+        mix = {"step": probe["step_mix_gbs"]}
+        for k, c in enumerate(calls):
+            if c == 6 and k == 0 and not pattern[0]:
+                mix[f"accumulate_{k}"] = probe["first_mix_gbs"]      # FIRST: read 2, write 4
+            elif c == 10:
+                mix[f"accumulate_{k}"] = probe["acc_mix_gbs"]        # read 6, write 4
+            elif c == 6 and pattern[k]:
+                mix[f"accumulate_{k}"] = probe["read_gbs"]           # deferred LAST: read only
+        for nm, ceil in mix.items():
+            if kern.get(nm, {}).get("gbs"):
+                kern[nm]["of_mix_ceiling"] = round(kern[nm]["gbs"] / ceil, 4)
+        probe["note"] = ("16-byte-vector streaming kernels, chunks claimed: copy 1:1, write-only, read-only, the "
+                         "fused step's 18:14 read:write mix and the accumulate passes' 2:4 and 6:4, no arithmetic; "
+                         "kernels.*.of_mix_ceiling = a pass's GB/s over its own mix's")
 
     # the other single-GPU target shards, timed by the same run (config freed first)
     extra = None

@@ -10,9 +10,14 @@
  *   HBM_PROBE_READ      read n 16-byte vectors (one word per CTA written);
  *   HBM_PROBE_STEP_MIX  the fused optimizer step's mix: per 4 elements read
  *                       16 + 8 + 16 + 16 + 16 bytes from five buffers and write
- *                       16 + 16 + 16 + 8 bytes to four (18 : 14 bytes per element).
+ *                       16 + 16 + 16 + 8 bytes to four (18 : 14 bytes per element);
+ *   HBM_PROBE_FIRST_MIX the first accumulate pass's: per 4 elements read 8 bytes,
+ *                       write 16 (2 : 4 bytes per element);
+ *   HBM_PROBE_ACC_MIX   a later accumulate pass's: per 4 elements read 16 + 8
+ *                       bytes, write 16 (6 : 4 bytes per element).
  * Every kernel takes its 64 KiB chunks from a counter the way the optimizer's
- * passes do; the counter is reset before each launch.
+ * passes do; the counter returns to zero by itself at the end of each launch
+ * (the CTA holding the last claim past the end resets it).
  *
  * Buffers (device memory of the current device, 16-byte aligned, not
  * overlapping; the caller allocates them):
@@ -22,7 +27,10 @@
  *             (hbm_probe_sink_bytes gives the size);
  *   STEP_MIX: n counts 4-element quads: buf[0] accumulator (16 B per quad),
  *             buf[1] gradient (8), buf[2..4] master, m, v (16 each), buf[5]
- *             bf16 parameters (8).
+ *             bf16 parameters (8);
+ *   FIRST_MIX: n quads: buf[0] gradient (8 B per quad), buf[1] accumulator (16);
+ *   ACC_MIX:   n quads: buf[0] gradient (8 B per quad), buf[1] accumulator (16,
+ *             read and written).
  * n must be a multiple of 4096 (64 KiB chunks of 16-byte vectors).
  *
  * hbm_probe_run times `reps` launches after `warmup` untimed ones with CUDA
@@ -47,6 +55,8 @@ extern "C" {
 #define HBM_PROBE_WRITE 1
 #define HBM_PROBE_READ 2
 #define HBM_PROBE_STEP_MIX 3
+#define HBM_PROBE_FIRST_MIX 4
+#define HBM_PROBE_ACC_MIX 5
 
 int hbm_probe_run(int kind, void *const *buf, uint64_t n, int warmup, int reps, void *stream, float *ms,
                   double *bytes);

@@ -127,6 +127,36 @@ __global__ void __launch_bounds__(kT) k_mix(const float4 *__restrict__ a, const 
     cl.done(c);
 }
 
+// The accumulate passes' traffic: bf16 quads read (8 B), FP32 quads written
+// (16 B), and with HAS_ACC the FP32 quads read first (16 B).
+template <bool HAS_ACC, int U>
+__global__ void __launch_bounds__(kT) k_acc_mix(const uint2 *__restrict__ g, float4 *__restrict__ a, uint32_t nch,
+                                               unsigned *ctr) {
+    __shared__ uint32_t sh;
+    Claim cl{ctr, nch, &sh};
+    uint32_t c = cl.next();
+    for (; c < nch; c = cl.next()) {
+        const uint64_t q0 = (uint64_t)c * kVecPerChunk;
+        for (uint32_t b = threadIdx.x; b < kVecPerChunk; b += kT * U) {
+            uint2 gv[U];
+            float4 av[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                gv[u] = __ldcs(g + q0 + b + u * kT);
+                if (HAS_ACC) av[u] = __ldcs(a + q0 + b + u * kT);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float4 x = make_float4(__uint_as_float(gv[u].x << 16), __uint_as_float(gv[u].x & 0xffff0000u),
+                                             __uint_as_float(gv[u].y << 16), __uint_as_float(gv[u].y & 0xffff0000u));
+                __stcs(a + q0 + b + u * kT,
+                       HAS_ACC ? make_float4(av[u].x + x.x, av[u].y + x.y, av[u].z + x.z, av[u].w + x.w) : x);
+            }
+        }
+    }
+    cl.done(c);
+}
+
 std::mutex g_mu;
 unsigned *g_ctr[64] = {};
 
@@ -174,7 +204,7 @@ extern "C" int hbm_probe_run(int kind, void *const *buf, uint64_t n, int warmup,
                              double *bytes) {
     if (!buf || !ms || !bytes || n == 0 || n % kVecPerChunk != 0 || reps < 1 || warmup < 0) return -1;
     const int nbuf = kind == HBM_PROBE_COPY ? 2 : kind == HBM_PROBE_WRITE ? 1 : kind == HBM_PROBE_READ ? 2
-                                                : kind == HBM_PROBE_STEP_MIX ? 6 : 0;
+                   : kind == HBM_PROBE_STEP_MIX ? 6 : (kind == HBM_PROBE_FIRST_MIX || kind == HBM_PROBE_ACC_MIX) ? 2 : 0;
     if (nbuf == 0) return -1;
     for (int i = 0; i < nbuf; ++i)
         if (!buf[i] || mis16(buf[i])) return -1;
@@ -196,6 +226,8 @@ extern "C" int hbm_probe_run(int kind, void *const *buf, uint64_t n, int warmup,
         case HBM_PROBE_COPY: k_copy<8><<<grid, kT, 0, st>>>((const float4 *)buf[0], (float4 *)buf[1], nch, ctr); break;
         case HBM_PROBE_WRITE: k_write<8><<<grid, kT, 0, st>>>((float4 *)buf[0], nch, ctr); break;
         case HBM_PROBE_READ: k_read<8><<<grid, kT, 0, st>>>((const uint4 *)buf[0], (uint32_t *)buf[1], nch, ctr); break;
+        case HBM_PROBE_FIRST_MIX: k_acc_mix<false, 8><<<grid, kT, 0, st>>>((const uint2 *)buf[0], (float4 *)buf[1], nch, ctr); break;
+        case HBM_PROBE_ACC_MIX: k_acc_mix<true, 8><<<grid, kT, 0, st>>>((const uint2 *)buf[0], (float4 *)buf[1], nch, ctr); break;
         default:
             k_mix<4><<<grid, kT, 0, st>>>((const float4 *)buf[0], (const uint2 *)buf[1], (float4 *)buf[2],
                                          (float4 *)buf[3], (float4 *)buf[4], (uint2 *)buf[5], nch, ctr);
@@ -205,6 +237,8 @@ extern "C" int hbm_probe_run(int kind, void *const *buf, uint64_t n, int warmup,
     case HBM_PROBE_COPY: rc = grid_of(k_copy<8>, &grid); b = 32.0 * (double)n; break;
     case HBM_PROBE_WRITE: rc = grid_of(k_write<8>, &grid); b = 16.0 * (double)n; break;
     case HBM_PROBE_READ: rc = grid_of(k_read<8>, &grid); b = 16.0 * (double)n; break;
+    case HBM_PROBE_FIRST_MIX: rc = grid_of(k_acc_mix<false, 8>, &grid); b = 24.0 * (double)n; break;   // 6 B x 4
+    case HBM_PROBE_ACC_MIX: rc = grid_of(k_acc_mix<true, 8>, &grid); b = 40.0 * (double)n; break;      // 10 B x 4
     default: rc = grid_of(k_mix<4>, &grid); b = 128.0 * (double)n; break;   // 4 elements x 32 B per quad
     }
     if (rc) return rc;
