@@ -351,8 +351,8 @@ int bf16opt_set_step(bf16opt_t *h, int64_t t);
  * Computes, without a handle and without allocating anything, the global L2
  * norm of a flat FP32 gradient accumulator `grad_accum` of n elements (each
  * element times grad_scale, rounded to FP32), with the same deterministic
- * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard (whose
- * master buffer has the accumulator's offset modulo 128 bytes), and the
+ * chunked reduction as bf16opt_grad_norm on a one-range FLAT shard over an
+ * accumulator with the same offset modulo 128 bytes, and the
  * clip coefficient c = max_grad_norm / norm if norm > max_grad_norm (> 0),
  * else 1.  `out` is owned by the caller; the result is written there on
  * `stream` (nothing is synchronised).  `out` and `grad_accum` must be memory

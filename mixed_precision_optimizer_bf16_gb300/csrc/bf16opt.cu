@@ -595,17 +595,21 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     if (overlaps(iv)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "state buffers overlap");
 
     // Chunk table: every segment cut into chunks of at most `chunk` elements, in
-    // segment order.  The first chunk of a segment is shortened by the master
-    // buffer's element offset from a kHeadAlign boundary, so that every later
-    // chunk starts on such a boundary: those chunks need no scalar head, and no
-    // 128-byte line of the (equally offset) buffers is split between two chunks.
+    // segment order.  The first chunk of a segment is shortened by the
+    // accumulator's element offset from a kHeadAlign boundary, so that every
+    // later chunk starts on such a boundary: those chunks need no scalar head,
+    // and no 128-byte line of the (equally offset) buffers is split between two
+    // chunks.  The accumulator is the buffer every norm pass streams, so the
+    // norm's chunking -- and its bits -- depend on it alone: an offload handle
+    // (master in host memory) and a device handle over accumulators with the
+    // same offset reduce the same chunks, as does bf16opt_grad_norm_static.
     uint64_t total = 0;
     for (const Seg &s : segs) total += s.numel;
     const uint32_t chunk = chunk_elems(total);
     std::vector<Chunk> chunks;
     for (uint32_t si = 0; si < segs.size(); ++si) {
         const Seg &s = segs[si];
-        const uint64_t first = chunk - first_chunk_cut(s.p);
+        const uint64_t first = chunk - first_chunk_cut(s.acc);
         for (uint64_t off = 0; off < s.numel;) {
             if (chunks.size() >= 0xffffffffull) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many chunks");
             const uint64_t len = std::min<uint64_t>(off == 0 ? first : chunk, s.numel - off);

@@ -21,10 +21,10 @@
 // Work decomposition.  A segment is one run of elements with one parameter
 // group and one set of base pointers (a flat range or a list tensor).  The
 // host cuts each segment into chunks of at most kChunk elements (the first one
-// shortened so that later chunks start on a 128-byte line of the master
-// buffer); a persistent grid takes the chunks by a fixed stride or claims them
-// from a counter (see the chunk schedule below).  Inside a chunk,
-// thread t handles 4-element quads t, t+T, ... so that every warp-wide access
+// shortened so that later chunks start on a 128-byte line of the
+// accumulator); a persistent grid takes the chunks by a fixed stride or claims
+// them from a counter (see the chunk schedule below).  Inside a chunk, thread
+// t handles 4-element quads t, t+T, ... so that every warp-wide access
 // is contiguous: FP32 as 16-byte and bf16 as 8-byte vectors.  Leading elements
 // up to the lead pointer's next kHeadAlign-element boundary, and the ragged
 // tail, are done one element at a time by a warp chosen per chunk.  If the
