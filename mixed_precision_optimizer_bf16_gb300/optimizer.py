@@ -108,7 +108,7 @@ def partition_bounds(n, world):
     return [min(int(n), r * part) for r in range(int(world) + 1)]
 
 
-def exchange_gradient_slices(full_grad, bounds, group=None):
+def exchange_gradient_slices(full_grad, bounds, group=None, phase=0):
     """The exchange half of a ZeRO-2 gradient reduce-scatter.
 
     full_grad: this rank's bf16 gradient (bf16 or int16 tensor) of the whole
@@ -118,8 +118,10 @@ def exchange_gradient_slices(full_grad, bounds, group=None):
     device: row q is rank q's gradient over this rank's partition, so the rows
     are in rank order.  Point-to-point sends of byte views (gloo has no
     all-to-all and no 16-bit types); with gloo a CUDA gradient is staged
-    through host memory.  Without an initialised process group the only row is
-    the gradient itself."""
+    through host memory.  phase: element offset (0-31) of every row within a
+    128-byte line -- give the accumulator's, so that the library streams rows
+    and accumulator as aligned vectors.  Without an initialised process group
+    the only row is the gradient itself."""
     import torch.distributed as dist
     if not (dist.is_available() and dist.is_initialized()):
         return full_grad.reshape(1, -1)
@@ -130,27 +132,28 @@ def exchange_gradient_slices(full_grad, bounds, group=None):
     src = full_grad.detach().cpu() if stage else full_grad.detach()
     src = src.contiguous().view(torch.uint8)
     lo, hi = bounds[rank], bounds[rank + 1]
-    # rows padded to whole 128-byte lines, so that every row starts where the
-    # state buffers do (vector-aligned) whatever the partition size
-    stride = -(-(hi - lo) // 64) * 64
+    # rows of whole 128-byte lines (the allocation starts on one), each row's
+    # elements starting `phase` elements into its first line
+    ph = int(phase) % 32
+    stride = -(-(hi - lo + ph) // 64) * 64
     out = torch.empty((world, max(stride, 1)), dtype=full_grad.dtype, device=full_grad.device)
     recv = torch.empty_like(out, device="cpu") if stage else out
     ops = []
     for q in range(world):
         peer = dist.get_global_rank(group, q) if group is not None else q
         if q == rank:
-            recv[q, :hi - lo].view(torch.uint8).copy_(src[2 * lo:2 * hi])
+            recv[q, ph:ph + hi - lo].view(torch.uint8).copy_(src[2 * lo:2 * hi])
             continue
         if bounds[q + 1] > bounds[q]:
             ops.append(dist.P2POp(dist.isend, src[2 * bounds[q]:2 * bounds[q + 1]], peer, group))
         if hi > lo:
-            ops.append(dist.P2POp(dist.irecv, recv[q, :hi - lo].view(torch.uint8), peer, group))
+            ops.append(dist.P2POp(dist.irecv, recv[q, ph:ph + hi - lo].view(torch.uint8), peer, group))
     if ops:
         for w in dist.batch_isend_irecv(ops):
             w.wait()
     if stage:
         out.copy_(recv)
-    return out[:, :hi - lo]
+    return out[:, ph:ph + hi - lo]
 
 
 def fold_pattern(slices, last):
@@ -321,8 +324,10 @@ class BF16Optimizer:
         if bounds[rank + 1] - bounds[rank] != self.n:
             raise ValueError(f"partition of rank {rank} has {bounds[rank + 1] - bounds[rank]} elements, "
                              f"this optimizer {self.n}")
+        # rows at the accumulator's element offset within a 128-byte line
+        phase = (self._state[0]["grad_accum"].data_ptr() // 4) % 32 if self.n else 0
         with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
-            recv = exchange_gradient_slices(full_grad, bounds, group)
+            recv = exchange_gradient_slices(full_grad, bounds, group, phase)
         flags = fold_pattern(world, last)
         for q in range(world):
             self.accumulate(recv[q], first=first and q == 0, last=last and q == world - 1, defer=flags[q],

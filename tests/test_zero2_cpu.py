@@ -55,8 +55,10 @@ def _worker(rank, port, q):
         for s in range(wl.steps):
             for k in range(GAS):
                 full = synth.fill_grad(wl, s, k * WORLD + rank, np.empty(wl.n, np.uint16))
-                recv = exchange_gradient_slices(torch.from_numpy(full.view(np.int16)), b)
+                ph = (7 * s + 3 * k + rank) % 32          # any row phase gives the same rows
+                recv = exchange_gradient_slices(torch.from_numpy(full.view(np.int16)), b, phase=ph)
                 assert tuple(recv.shape) == (WORLD, hi - lo)
+                assert all((recv[q].data_ptr() // 2) % 32 == ph for q in range(WORLD))
                 for src in range(WORLD):
                     want = synth.fill_grad(wl, s, k * WORLD + src, np.empty(hi - lo, np.uint16), lo)
                     got = recv[src].numpy().view(np.uint16)
