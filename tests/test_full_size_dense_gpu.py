@@ -1,10 +1,12 @@
-"""Every element of the full-size flat shards against the oracle.
+"""Every element of the full-size shards against the oracle.
 
 The benchmark's own shard (1,722,408,960 elements, 293 tensors, GAS 4, two
 steps) in the benchmark's launch configuration (last micro-batch deferred into
 the fused step), with every micro-batch deferred, and with every micro-batch
-stored; and the 1.83e9-element GAS-32 partition with the last micro-batch
-deferred and with all 32 gradients resident.  The GPU runs all variants first
+stored; the 1.83e9-element GAS-32 partition with the last micro-batch
+deferred and with all 32 gradients resident; and the 3,700,064,256-element
+ragged list of 72 separately allocated tensors (GAS 8, two steps) with the
+last micro-batch deferred.  The GPU runs all variants first
 and keeps their states resident; the oracle then runs the shard one host
 slice at a time (inputs regenerated from the counters, the global clip
 coefficient of every step streamed beforehand) and each slice is compared
@@ -59,3 +61,9 @@ def test_scaled_bloom_full_size_dense():
 def test_large_partition_full_size_dense():
     wl = workloads.workload(3)
     _run_dense(wl, {"last_deferred": True, "resident_in_eights": resident_pattern(wl.gas)})
+
+
+@needs_cuda
+def test_tp4_slice_full_size_dense():
+    wl = workloads.workload(4)
+    _run_dense(wl, {"last_deferred": True})

@@ -149,35 +149,8 @@ def test_grad_scale():
 
 # ----------------------------------------------------------- full-size sampled
 
-@needs_cuda
-@pytest.mark.parametrize("defer", [True, False, "all"])
-def test_scaled_bloom_full_size_sampled(defer):
-    """1,722,408,960 elements, 293 tensors in one flat buffer, decay/no-decay
-    ranges, GAS 4, 2 steps; the benchmark's launch configuration is defer=True,
-    its all-deferred variant defer="all"."""
-    wl = workloads.workload(2)
-    st = sampled_parity(wl, defer=[True] * wl.gas if defer == "all" else defer)
-    print("scaled BLOOM", defer, st)
-
-
-@needs_cuda
-@pytest.mark.parametrize("pattern", ["last", "eights"])
-def test_large_partition_full_size_sampled(pattern):
-    """1.83e9 flat elements, GAS 32, 1 step: the last micro-batch deferred, or
-    every gradient resident with each run of 8 folded by its 8th and the last
-    8 deferred into the norm pass and the step (32 gradient buffers, ~150 GB
-    on the device; the 8-gradient fold kernels at full size)."""
-    from mixed_precision_optimizer_bf16_gb300.optimizer import resident_pattern
-    wl = workloads.workload(3)
-    st = sampled_parity(wl, defer=True if pattern == "last" else resident_pattern(wl.gas))
-    print("large partition", pattern, st)
-
-
-@needs_cuda
-def test_tp4_slice_full_size_sampled():
-    """72 separate tensors, 3,700,064,256 elements, GAS 8, 2 steps."""
-    st = sampled_parity(workloads.workload(4), defer=True)
-    print("TP4 slice", st)
+# (The full-size shards are compared on every element in
+# test_full_size_dense_gpu.py.)
 
 
 @needs_cuda
