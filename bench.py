@@ -437,6 +437,9 @@ def run_ours(args):
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize(dev)
+    rc_path, path = C.bf16opt_step_path(opt.h)
+    step_kernel = {C.BF16OPT_PATH_PIPELINE: "k_step_pipe (fused clip+AdamW+master+bf16, bulk-copy pipeline)",
+                   C.BF16OPT_PATH_VECTOR: "k_step (fused clip+AdamW+master+bf16, vector loads)"}.get(path, "none")
 
     K = args.steps
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
@@ -633,7 +636,7 @@ def run_ours(args):
                    "bytes_per_elem_per_step": sum(bpe.values()), "hbm_gbs_per_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                    "l2": l2_note,
                    "parallelism": f"ZeRO partitions x{world}, global-norm all-gather per step" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": "k_step (fused clip+AdamW+master+bf16)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": step_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes_per_launch": bpe["step"] * n},
         "kernels": kern,

@@ -390,6 +390,34 @@ typedef struct {
 int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, float grad_scale, float max_grad_norm,
                              bf16opt_norm_result_t *out, void *stream);
 
+/* ---- data path of the step -------------------------------------------------
+ * No counterpart in the paper.  Which kernel the handle's most recent
+ * bf16opt_step ran (enqueued): NONE (no step yet, or the shard is empty),
+ * VECTOR (per-thread 16-byte vector loads and stores), PIPELINE (bulk
+ * asynchronous copies through shared memory; see below), HOST (an offload
+ * handle: the host cores update the master and moments).  Errors: INVALID_ARG
+ * (not a live handle, path NULL). */
+#define BF16OPT_PATH_NONE 0
+#define BF16OPT_PATH_VECTOR 1
+#define BF16OPT_PATH_PIPELINE 2
+#define BF16OPT_PATH_HOST 3
+int bf16opt_step_path(const bf16opt_t *h, int *path);
+
+/* ---- pipeline health ----------------------------------------------------
+ * No counterpart in the paper: a health check of the fused step's copy
+ * pipeline.  On shards of 2^25 elements and more whose buffers are aligned
+ * alike (per segment: the FP32 streams at one element index modulo 4, the
+ * bf16 streams at one modulo 8, agreeing modulo 4) bf16opt_step moves its
+ * traffic with bulk asynchronous copies through a ring of shared-memory
+ * stages (the environment variable BF16OPT_STEP_PIPE=1 / 0, read when a handle
+ * is created, forces it on / off), and every wait on a stage is bounded (2 s; a
+ * stage normally turns over in microseconds).  A wait that gives up is
+ * counted in a device word and its CTA stops, leaving the rest of its chunks
+ * of that step not updated.  This call waits for the device, stores the count
+ * into *count (0 = every step completed) and clears it.
+ * Errors: INVALID_ARG (count NULL), UNSUPPORTED (no device), CUDA. */
+int bf16opt_pipeline_timeouts(uint32_t *count);
+
 /* ---- checked build -------------------------------------------------------
  * No counterpart in the paper: a debugging aid standing in for a memory
  * checker.  In a build compiled with -DBF16K_CHECKS the kernels test, before

@@ -27,6 +27,10 @@ BF16OPT_DEFER = 4
 BF16OPT_MAX_GROUPS = 16
 BF16OPT_MAX_DEFERRED = 8
 BF16OPT_STATIC_NORM_MAX_ELEMS = 1 << 30
+BF16OPT_PATH_NONE = 0
+BF16OPT_PATH_VECTOR = 1
+BF16OPT_PATH_PIPELINE = 2
+BF16OPT_PATH_HOST = 3
 
 c_u64, c_u32, c_i32, c_f32, c_vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
 
@@ -67,7 +71,7 @@ EXPORTS = ("bf16opt_create", "bf16opt_create_offload", "bf16opt_accumulate", "bf
            "bf16opt_grad_norm_static", "bf16opt_lr_factor", "bf16opt_set_lr_schedule",
            "bf16opt_grad_norm_local", "bf16opt_set_global_sumsq", "bf16opt_set_rank_sumsqs",
            "bf16opt_sum_rank_sumsqs", "bf16opt_set_skip_nonfinite", "bf16opt_debug_faults",
-           "bf16opt_abi_version")
+           "bf16opt_pipeline_timeouts", "bf16opt_step_path", "bf16opt_abi_version")
 
 ABI_VERSION = 2   # BF16OPT_ABI_VERSION of the header these declarations mirror
 
@@ -128,6 +132,10 @@ def load(path=None):
     L.bf16opt_set_skip_nonfinite.argtypes = [hp, ctypes.c_int]
     L.bf16opt_debug_faults.restype = ctypes.c_int
     L.bf16opt_debug_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.bf16opt_pipeline_timeouts.restype = ctypes.c_int
+    L.bf16opt_step_path.restype = ctypes.c_int
+    L.bf16opt_step_path.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    L.bf16opt_pipeline_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.bf16opt_lr_factor.restype = ctypes.c_int
     L.bf16opt_lr_factor.argtypes = [ctypes.POINTER(bf16opt_lr_schedule_t), ctypes.c_int64,
                                     ctypes.POINTER(ctypes.c_double)]
@@ -253,6 +261,20 @@ def bf16opt_debug_faults():
     bits = ctypes.c_uint32(0)
     rc = load().bf16opt_debug_faults(ctypes.byref(bits))
     return rc, bits.value
+
+
+def bf16opt_pipeline_timeouts():
+    """(status, waits of the step's copy pipeline that gave up since the last call)."""
+    n = ctypes.c_uint32(0)
+    rc = load().bf16opt_pipeline_timeouts(ctypes.byref(n))
+    return rc, n.value
+
+
+def bf16opt_step_path(h):
+    """(status, BF16OPT_PATH_* of the handle's last step)."""
+    path = ctypes.c_int(0)
+    rc = load().bf16opt_step_path(h, ctypes.byref(path))
+    return rc, path.value
 
 
 def bf16opt_last_error(h=None):

@@ -48,6 +48,8 @@ struct bf16opt {
     uint32_t n_chunks = 0;
     Seg *segs_d = nullptr;
     Chunk *chunks_d = nullptr;
+    PipeUnit *units_d = nullptr;         // units of the pipelined step, in chunk order
+    std::vector<uint32_t> chunk_unit0;   // first unit of chunk c (n_chunks + 1 entries)
     double *partials_d = nullptr;
     NormState *norm_d = nullptr;
     unsigned *queue_d = nullptr;         // chunk counter of the pass in flight (0 between passes)
@@ -71,6 +73,8 @@ struct bf16opt {
     bool skip_nonfinite = false;
     bool pdl = true;                     // launch with programmatic stream serialization (BF16OPT_PDL=0: off)
     bool claim = true;                   // CTAs claim chunks from queue_d (BF16OPT_SCHEDULE=static: fixed stride)
+    bool pipe = true;                    // fused step through the bulk-copy pipeline (BF16OPT_STEP_PIPE=0: vector loads)
+    int step_path = BF16OPT_PATH_NONE;   // data path of the last step (bf16opt_step_path)
     bool scalars_ready = false;          // the norm kernel prepared this step's scalars (groups' own lr)
     bf16opt_lr_schedule_t sched{};
     std::string last_error;
@@ -186,6 +190,30 @@ uint32_t first_chunk_cut(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) 
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 
+// A function attribute set once per kernel and device (kernels of one
+// template share a function type, so the kernel's address is the key).
+template <class K>
+cudaError_t kernel_attr_once(K kernel, int dev, cudaFuncAttribute attr, int value) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void *, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const void *key = reinterpret_cast<const void *>(kernel);
+    for (const auto &e : done)
+        if (e.first == key && e.second == dev) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, attr, value);
+    if (e == cudaSuccess) done.emplace_back(key, dev);
+    return e;
+}
+
+// Shared-memory carveout of the streaming kernels: the least shared memory,
+// the most L1.  Without the preference a kernel that fits the shared-memory
+// configuration the step's copy pipeline left behind runs in it, with a small
+// L1 -- where its loads in flight are staged -- and the accumulate passes ran
+// 1.4 % slower.
+#ifndef BF16K_STREAM_CARVEOUT
+#define BF16K_STREAM_CARVEOUT 0
+#endif
+
 template <class K>
 int grid_for(bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
     int per_sm = 0;
@@ -210,12 +238,12 @@ int grid_for(bf16opt_t *h, K kernel, uint32_t nchunks, int threads = kThreads) {
 // predecessor drains, and waits on the device (griddepcontrol.wait) before
 // its first memory access -- see pdl_enter in kernels.cuh.
 template <class... KArgs, class... Args>
-cudaError_t launch(const bf16opt_t *h, void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
-                   Args &&...args) {
+cudaError_t launch_smem(const bf16opt_t *h, void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                        cudaStream_t st, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -223,6 +251,11 @@ cudaError_t launch(const bf16opt_t *h, void (*kernel)(KArgs...), unsigned grid, 
     cfg.attrs = attr;
     cfg.numAttrs = h->pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <class... KArgs, class... Args>
+cudaError_t launch(const bf16opt_t *h, void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                   Args &&...args) {
+    return launch_smem(h, kernel, grid, block, 0, st, std::forward<Args>(args)...);
 }
 
 // Gradients a pass folds: K micro-batches (FLAT: one pointer each; LIST: one
@@ -275,6 +308,11 @@ int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
+#if BF16K_STREAM_CARVEOUT >= 0
+        if (kernel_attr_once(k, h->device, cudaFuncAttributePreferredSharedMemoryCarveout, BF16K_STREAM_CARVEOUT) !=
+            cudaSuccess)
+            cudaGetLastError();   // a hint: the pass runs without it
+#endif
         const cudaError_t e1 = launch(h, k, grid_for(h, k, c1 - c0), kThreads, st, (const Seg *)h->segs_d,
                                       (const Chunk *)h->chunks_d, c0, c1, gt, h->partials_d, h->gscale,
                                       h->claim ? h->queue_d : nullptr);
@@ -298,6 +336,29 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
 
 constexpr uint64_t kStepClaimChunksPerCta = 64;
 
+// The bulk-copy step needs every stream of a chunk's body 16-byte aligned at
+// one element: per segment, the FP32 pointers (master, m, v, the accumulator
+// if read) share their element index modulo 4, the bf16 ones (parameters,
+// folded gradients) share theirs modulo 8, and the two agree modulo 4.
+bool pipe_aligned(const bf16opt_t *h, const FoldSet &fs, bool has_acc) {
+    const size_t K = fs.count();
+    for (const Seg &s : h->segs) {
+        if (s.numel == 0) continue;
+        const uint32_t f = (uint32_t)(((uintptr_t)s.p >> 2) & 3u);
+        const uint32_t b = (uint32_t)(((uintptr_t)s.bf >> 1) & 7u);
+        if ((b & 3u) != f) return false;
+        for (const float *x : {s.m, s.v})
+            if ((uint32_t)(((uintptr_t)x >> 2) & 3u) != f) return false;
+        if (has_acc && (uint32_t)(((uintptr_t)s.acc >> 2) & 3u) != f) return false;
+        for (size_t j = 0; j < K; ++j) {
+            const uint16_t *g = (h->mode == BF16OPT_FLAT ? fs.flat[j] : (*fs.list[j])[s.grad_slot]) + s.grad_off;
+            if ((uint32_t)(((uintptr_t)g >> 1) & 7u) != b) return false;
+        }
+    }
+    return true;
+}
+
+
 // commit_t: the first launch advances the device step counter (the step's
 // scalars were prepared by the norm kernel; otherwise k_step_scalars did both).
 template <bool HAS_ACC, int KMAX>
@@ -305,8 +366,29 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
     constexpr int U = KMAX <= 1 ? BF16K_STEP_U : (KMAX <= 4 ? BF16K_FOLD4_STEP_U : BF16K_FOLD8_STEP_U);
     cudaError_t e = cudaSuccess;
     bool first = true;
+    const bool pipe = h->pipe && pipe_aligned(h, fs, HAS_ACC);
+    const int K = (int)fs.count();
+    h->step_path = pipe ? BF16OPT_PATH_PIPELINE : BF16OPT_PATH_VECTOR;
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
+        if (pipe) {
+            auto kp = k_step_pipe<HAS_ACC, KMAX, GT>;
+            const size_t smem = (size_t)pipe_stages(HAS_ACC, K) * pipe_quad_bytes(HAS_ACC, K) *
+                                pipe_tile_quads(HAS_ACC, K);
+            cudaError_t e1 = kernel_attr_once(kp, h->device, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kPipeSmem);   // the most any K of the variant takes
+            const uint32_t u0 = h->chunk_unit0[c0], u1 = h->chunk_unit0[c1];
+            uint64_t grid = std::min<uint64_t>((uint64_t)h->sm_count, u1 - u0);
+            if (h->max_grid > 0 && grid > (uint64_t)h->max_grid) grid = (uint64_t)h->max_grid;
+            if (e1 == cudaSuccess)
+                e1 = launch_smem(h, kp, (unsigned)std::max<uint64_t>(1, grid), kPipeThreads, smem, st,
+                                 (const Seg *)h->segs_d, (const Chunk *)h->chunks_d, (const PipeUnit *)h->units_d,
+                                 u0, u1, gt, h->step_d, (const NormState *)h->norm_d, h->gscale,
+                                 (commit_t && first) ? 1 : 0, h->claim ? h->queue_d : nullptr);
+            first = false;
+            if (e == cudaSuccess) e = e1;
+            return;
+        }
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
         const int grid = grid_for(h, k, c1 - c0, kStepThreads);
         // one CTA per SM: claiming pays once every CTA has many chunks to go
@@ -362,6 +444,8 @@ void free_scratch(bf16opt_t *h) {
     free_offload(h);
     if (h->segs_d) cudaFree(h->segs_d);
     if (h->chunks_d) cudaFree(h->chunks_d);
+    if (h->units_d) cudaFree(h->units_d);
+    h->units_d = nullptr;
     if (h->partials_d) cudaFree(h->partials_d);
     if (h->norm_d) cudaFree(h->norm_d);
     if (h->queue_d) cudaFree(h->queue_d);
@@ -626,6 +710,28 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
             if (slot_chunk0[s] > slot_chunk0[s + 1]) slot_chunk0[s] = slot_chunk0[s + 1];
     }
 
+    // Units of the pipelined step: each chunk's body -- from its first element
+    // at which the bf16 parameters are 16-byte aligned, a multiple of 8
+    // elements -- cut into runs of kPipeUnitQuads quads, in chunk order.
+    std::vector<PipeUnit> units;
+    std::vector<uint32_t> chunk_unit0(chunks.size() + 1, 0);
+    for (uint32_t c = 0; c < chunks.size(); ++c) {
+        if (units.size() >= 0xffffffffull) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "too many step units");
+        chunk_unit0[c] = (uint32_t)units.size();
+        const Chunk &ch = chunks[c];
+        const Seg &sg = segs[ch.seg];
+        const uint32_t hb = pipe_head(sg.bf + ch.start, ch.len);
+        const uint32_t nqb = ((ch.len - hb) >> 3) << 1;
+        const uint32_t scal = (hb != 0 || hb + 4u * nqb != ch.len) ? 1u : 0u;
+        uint32_t q = 0;
+        do {
+            const uint32_t nq = std::min(kPipeUnitQuads, nqb - q);
+            units.push_back({ch.start + hb + 4ull * q, ch.seg, c, nq, q == 0 ? scal : 0u});
+            q += kPipeUnitQuads;
+        } while (q < nqb);
+    }
+    chunk_unit0[chunks.size()] = (uint32_t)units.size();
+
     // Device and scratch.
     int dev = 0, ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
@@ -642,6 +748,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     h->n_tensors = d->mode == BF16OPT_LIST ? d->n_tensors : 0;
     h->segs = segs;
     h->slot_chunk0 = slot_chunk0;
+    h->chunk_unit0 = chunk_unit0;
     h->n_chunks = (uint32_t)chunks.size();
     h->groups.assign(d->groups, d->groups + d->n_groups);
     h->max_norm = d->max_grad_norm;
@@ -660,11 +767,19 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     // BF16OPT_SCHEDULE=static / claim overrides (to compare).
     h->claim = total >= (uint64_t(1) << 25);
     if (const char *sc = std::getenv("BF16OPT_SCHEDULE")) h->claim = std::strcmp(sc, "static") != 0;
+    // The fused step moves its traffic with bulk copies on shards of 2^25
+    // elements and more (it also needs buffers aligned alike, see
+    // pipe_aligned); on a 1M-element shard the pipeline's fill cost more than
+    // it gained (12.4 vs 10.4 us).  BF16OPT_STEP_PIPE=1 / 0 overrides (to test
+    // and compare).
+    h->pipe = total >= (uint64_t(1) << 25);
+    if (const char *sp = std::getenv("BF16OPT_STEP_PIPE")) h->pipe = std::atoi(sp) != 0;
 
     cudaError_t e = cudaSuccess;
     const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());
     if ((e = cudaMalloc(&h->segs_d, nseg * sizeof(Seg))) != cudaSuccess ||
         (e = cudaMalloc(&h->chunks_d, nch * sizeof(Chunk))) != cudaSuccess ||
+        (e = cudaMalloc(&h->units_d, std::max<size_t>(1, units.size()) * sizeof(PipeUnit))) != cudaSuccess ||
         (e = cudaMalloc(&h->partials_d, nch * sizeof(double))) != cudaSuccess ||
         (e = cudaMalloc(&h->norm_d, sizeof(NormState))) != cudaSuccess ||
         (e = cudaMalloc(&h->queue_d, sizeof(unsigned))) != cudaSuccess ||
@@ -678,6 +793,7 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     }
     if ((!segs.empty() && (e = cudaMemcpy(h->segs_d, segs.data(), segs.size() * sizeof(Seg), cudaMemcpyHostToDevice)) != cudaSuccess) ||
         (!chunks.empty() && (e = cudaMemcpy(h->chunks_d, chunks.data(), chunks.size() * sizeof(Chunk), cudaMemcpyHostToDevice)) != cudaSuccess) ||
+        (!units.empty() && (e = cudaMemcpy(h->units_d, units.data(), units.size() * sizeof(PipeUnit), cudaMemcpyHostToDevice)) != cudaSuccess) ||
         (e = cudaMemset(h->norm_d, 0, sizeof(NormState))) != cudaSuccess ||
         (e = cudaMemset(h->queue_d, 0, sizeof(unsigned))) != cudaSuccess ||
         (e = cudaMemset(h->step_d, 0, sizeof(StepState))) != cudaSuccess ||
@@ -1289,6 +1405,34 @@ extern "C" int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, flo
     k_static_final<<<1, kFinalThreads, 0, st>>>(partials, nchunks, max_grad_norm, out_d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "grad_norm_static kernel launch");
+    return BF16OPT_OK;
+}
+
+int bf16opt_step_path(const bf16opt_t *h, int *path) {
+    if (path) *path = BF16OPT_PATH_NONE;
+    if (!live(h)) return fail(nullptr, BF16OPT_ERR_INVALID_ARG, "not a live handle");
+    if (!path) return fail(const_cast<bf16opt_t *>(h), BF16OPT_ERR_INVALID_ARG, "path must be non-NULL");
+    *path = h->offload ? BF16OPT_PATH_HOST : h->step_path;
+    return BF16OPT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Waits of the fused step's copy pipeline that gave up (see kernels.cuh).
+// ---------------------------------------------------------------------------
+extern "C" int bf16opt_pipeline_timeouts(uint32_t *count) {
+    if (!count) return BF16OPT_ERR_INVALID_ARG;
+    *count = 0;
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return fail(nullptr, BF16OPT_ERR_UNSUPPORTED, "no CUDA device");
+    }
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_pipe_timeouts, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pipe_timeouts, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "reading the pipeline's timeout count");
+    *count = v;
     return BF16OPT_OK;
 }
 

@@ -821,4 +821,398 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
     sch.release(c);
 }
 
+
+// ------------------------------------------------------ bulk-copy pipeline
+// The fused step's traffic moved by the SM's bulk asynchronous copy unit
+// instead of per-thread vector loads and stores: cp.async.bulk copies whole
+// runs of a stream between global and shared memory, loads completing on an
+// mbarrier by transaction count, stores retired through bulk groups.  One
+// thread of the CTA issues every copy; the other warps compute in shared
+// memory.  Measured on the step's 18:14 read:write mix over 2^30 elements:
+// 7.20 TB/s against 7.00 TB/s for the best shape of 16-byte vector loads.
+
+// Waits that gave up (see mbar_wait); read and cleared by
+// bf16opt_pipeline_timeouts.
+__device__ uint32_t g_pipe_timeouts;
+
+constexpr uint64_t kPipeWaitNs = 2000000000ull;   // a stage wait normally takes microseconds
+constexpr uint64_t kPipeDrainNs = 200000000ull;   // copies still in flight after a timeout
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+// Makes the initialised barriers visible to the asynchronous proxy.
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// One arrival that also expects `bytes` of bulk-copy transactions this phase.
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase of parity `parity` of *b to complete, for at most
+// limit_ns; a wait that gives up is counted in g_pipe_timeouts and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(b, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) {
+            atomicAdd(&g_pipe_timeouts, 1u);
+            return false;
+        }
+    }
+}
+// L2 policy of the bulk copies: evict first, like the streaming loads and
+// stores (ld/st .cs) of every other pass.  Without it the copies leave their
+// lines at normal priority; the L2 then evicts the other passes' evict-first
+// lines ahead of them, and every pass after the step ran 1.4 % slower (the
+// step kernel of another handle too) until a kernel touched those lines again.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global -> shared, `bytes` (a multiple of 16, both addresses 16-byte aligned),
+// completing as transactions on *bar.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+// Shared -> global, in the current bulk group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until at most N of this thread's most recent bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's shared-memory writes before later asynchronous-proxy
+// (bulk copy) reads of them.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+#ifndef BF16K_PIPE_WARPS
+#define BF16K_PIPE_WARPS 8
+#endif
+#ifndef BF16K_PIPE_SMEM
+#define BF16K_PIPE_SMEM (200u * 1024u)
+#endif
+constexpr int kPipeWarps = BF16K_PIPE_WARPS;            // compute warps (one more warp issues the copies)
+constexpr int kPipeThreads = 32 * (kPipeWarps + 1);
+constexpr int kPipeCompute = 32 * kPipeWarps;
+constexpr uint32_t kPipeSmem = BF16K_PIPE_SMEM;         // stage buffers per CTA (one CTA per SM)
+constexpr int kPipeMaxStages = 8;
+constexpr int kPipeLag = 1;                             // stores still reading a stage when the next load is issued
+static_assert(kPipeWarps >= 2, "the head and tail scalars go to compute warps 0 and 1");
+
+// Bytes of one stage per 4-element quad: the accumulator, K gradient slots
+// (one when K = 0: the bf16 output; otherwise slot 0 takes the bf16 output
+// after the gradients are read), master, m, v.
+__host__ __device__ constexpr uint32_t pipe_quad_bytes(bool has_acc, int K) {
+    return (has_acc ? 16u : 0u) + 8u * (uint32_t)(K > 0 ? K : 1) + 48u;
+}
+// Quads per tile (a stage holds one tile): even, so that every bf16 run is a
+// multiple of 16 bytes.
+__host__ __device__ constexpr uint32_t pipe_tile_quads(bool has_acc, int K) {
+    return pipe_quad_bytes(has_acc, K) <= 80u ? 512u : 256u;
+}
+__host__ __device__ constexpr int pipe_stages(bool has_acc, int K) {
+    return (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * pipe_tile_quads(has_acc, K))) < kPipeMaxStages
+               ? (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * pipe_tile_quads(has_acc, K)))
+               : kPipeMaxStages;
+}
+static_assert(pipe_stages(true, kMaxFold) > kPipeLag && pipe_stages(false, 1) <= kPipeMaxStages, "pipeline depth");
+
+// Leading scalar elements of a chunk before its bulk body: up to the first
+// element at which the bf16 parameter pointer is 16-byte aligned.  The host
+// runs the pipeline only on segments whose FP32 pointers share their element
+// index modulo 4 and whose bf16 pointers share it modulo 8 (the two agreeing
+// modulo 4), so every stream is 16-byte aligned there.
+__host__ __device__ __forceinline__ uint32_t pipe_head(const uint16_t *bf, uint32_t len) {
+    const uint32_t h = (8u - (uint32_t)(((uintptr_t)bf >> 1) & 7u)) & 7u;
+    return h < len ? h : len;
+}
+
+// The pipelined step's unit of work, claimed one at a time: up to
+// kPipeUnitQuads quads of one chunk's body (a chunk without body, only scalar
+// elements, is one unit with nq = 0).  The host lists the units of every
+// chunk in chunk order.  Measured on the 1.72B-element shard (step kernel):
+// units of 2,048 / 8,192 / 16,384 / 32,768 elements took 8.19 / 7.74 / 7.78 /
+// 7.82 ms (vector loads, chunk claims: 7.93).  Smaller claims keep the SMs
+// streaming from nearby addresses, but one claim per stage tile cost more
+// than that gained.
+#ifndef BF16K_PIPE_UNIT_QUADS
+#define BF16K_PIPE_UNIT_QUADS 2048
+#endif
+constexpr uint32_t kPipeUnitQuads = BF16K_PIPE_UNIT_QUADS;
+static_assert(kPipeUnitQuads % 512 == 0, "a unit is whole tiles of every variant");
+struct PipeUnit {
+    uint64_t el;        // first body element, relative to the segment
+    uint32_t seg;
+    uint32_t chunk;
+    uint32_t nq;        // body quads (even; at most kPipeUnitQuads)
+    uint32_t scalars;   // the chunk's first unit, and the chunk has scalar head or tail elements
+};
+
+// What the copy thread tells the compute warps about the tile in a stage.
+struct TileDesc {
+    float *p, *m, *v;   // the tile's first body element in each output stream
+    uint16_t *bf;
+    uint32_t group;
+    uint32_t nq;        // body quads in the tile (even; 0 for a chunk without body)
+    uint32_t chunk;     // its chunk; kTileEnd: no more tiles for this CTA
+    uint32_t scalars;   // this tile also does the chunk's scalar head and tail
+};
+constexpr uint32_t kTileEnd = 0xffffffffu;
+
+// Fused clip + AdamW + master update + bf16 cast over chunks [c0, c1), the
+// same arithmetic per element as k_step (bit-identical results), with the
+// traffic moved by bulk copies.  One CTA per SM.  Warp 0, lane 0, walks the
+// CTA's chunks (claimed from `queue`, or the fixed stride when it is null),
+// cuts each chunk's aligned body into tiles and streams each tile through a
+// ring of shared-memory stages: acc, the deferred gradients, master, m and v
+// in; master, m, v and the bf16 parameters out, in place.  The compute warps
+// take the stages in order, update them and release them to the copy thread.
+template <bool HAS_ACC, int KMAX, class GT>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, const PipeUnit *__restrict__ units,
+            uint32_t u0, uint32_t u1, GT gt, StepState *st, const NormState *__restrict__ ns, float gscale,
+            int commit_t, unsigned *queue) {
+    extern __shared__ __align__(128) unsigned char pipe_smem[];
+    __shared__ uint64_t full[kPipeMaxStages], done[kPipeMaxStages];
+    __shared__ TileDesc desc[kPipeMaxStages];
+    __shared__ GroupK sh_g[kMaxGroups];
+    constexpr int KA = KMAX > 0 ? KMAX : 1;
+    const int K = KMAX <= 1 ? KMAX : (int)gt.k;
+    pdl_enter();
+    if (st->skip) return;                   // non-finite norm, skipping enabled (no CTA claims a chunk)
+    if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
+    const uint32_t tq = pipe_tile_quads(HAS_ACC, K);
+    const int nst = pipe_stages(HAS_ACC, K);
+    for (int i = threadIdx.x; i < kMaxGroups; i += kPipeThreads) sh_g[i] = st->gtab.g[i];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&done[i], kPipeCompute);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    // stage layout
+    const uint32_t off_g = HAS_ACC ? 16u * tq : 0u;
+    const uint32_t off_p = off_g + 8u * tq * (uint32_t)(K > 0 ? K : 1);
+    const uint32_t off_m = off_p + 16u * tq, off_v = off_m + 16u * tq;
+    const uint32_t stage_bytes = off_v + 16u * tq;
+    const uint32_t load_bytes = stage_bytes - (K == 0 ? 8u * tq : 0u);   // per full tile
+
+    if (threadIdx.x < 32) {
+        if (threadIdx.x != 0) return;
+        // ---------------------------------------------------- copy thread
+        constexpr int L = kPipeLag;
+        const int D = nst - L;              // tiles loaded ahead of the oldest one not yet stored
+        const uint64_t pol = l2_evict_first();
+        int issued = 0, stored = 0;
+        bool ok = true;
+        // The oldest computed tile's results go out: p, m, v, bf16.
+        auto retire = [&]() -> bool {
+            const int s = stored % nst;
+            if (!mbar_wait(&done[s], (uint32_t)(stored / nst) & 1u, kPipeWaitNs)) return false;
+            const TileDesc d = desc[s];
+            if (d.nq) {
+                unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
+                bulk_store(d.p, stg + off_p, 16u * d.nq, pol);
+                bulk_store(d.m, stg + off_m, 16u * d.nq, pol);
+                bulk_store(d.v, stg + off_v, 16u * d.nq, pol);
+                bulk_store(d.bf, stg + off_g, 8u * d.nq, pol);
+            }
+            bulk_commit();
+            ++stored;
+            return true;
+        };
+        // Stage for tile `issued`: free once the tile that used it was stored
+        // and its stores have read it.
+        auto acquire = [&]() -> int {
+            while (stored <= issued - D) {
+                if (!retire()) return -1;
+                bulk_wait_read<L>();
+            }
+            return issued % nst;
+        };
+        // Units u0 + claim: the next unit is claimed, and its table entry
+        // loaded, one unit ahead, so neither round trip stalls the copies.
+        const bool claims = queue != nullptr;
+        uint32_t u = claims ? u0 + atomicAdd(queue, 1u) : u0 + blockIdx.x;
+        uint32_t last = u;                  // the most recent claim
+        uint32_t un = u;
+        if (u < u1) last = un = claims ? u0 + atomicAdd(queue, 1u) : u + gridDim.x;
+        PipeUnit rec{};
+        if (u < u1) rec = units[u];
+        uint32_t cur_seg = 0xffffffffu;
+        Seg sg{};
+        const uint16_t *gb[KA];
+        while (ok && u < u1) {
+            const bool more = un < u1;
+            PipeUnit recn{};
+            if (more) recn = units[un];
+            const uint32_t unn = more ? (claims ? u0 + atomicAdd(queue, 1u) : un + gridDim.x) : un;
+            if (more) last = unn;
+            if (rec.seg != cur_seg) {
+                cur_seg = rec.seg;
+                sg = segs[cur_seg];
+#pragma unroll
+                for (int j = 0; j < KA; ++j) gb[j] = (j < K) ? gt.get(sg.grad_slot, j) + sg.grad_off : nullptr;
+            }
+            const uint64_t e0 = rec.el;
+            bool bad = check_fails(e0 + 4ull * rec.nq > sg.numel, kFaultChunkRange);
+            if (rec.nq) {
+                bool mis = mis16(sg.p + e0) || mis16(sg.m + e0) || mis16(sg.v + e0) || mis16(sg.bf + e0) ||
+                           (HAS_ACC && mis16(sg.acc + e0));
+#pragma unroll
+                for (int j = 0; j < KA; ++j)
+                    if (j < K) mis = mis || mis16(gb[j] + e0);
+                bad = bad || check_fails(mis, kFaultAlign);
+            }
+            if (!bad) {
+                for (uint32_t q = 0; q < rec.nq || q == 0; q += tq) {
+                    const uint32_t nq = rec.nq - q < tq ? rec.nq - q : tq;
+                    const int s = acquire();
+                    if (s < 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t e = e0 + 4ull * q;
+                    desc[s] = TileDesc{sg.p + e, sg.m + e, sg.v + e, sg.bf + e, sg.group, nq, rec.chunk,
+                                       q == 0 ? rec.scalars : 0u};
+                    if (nq) {
+                        unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
+                        mbar_arrive_tx(&full[s], nq == tq ? load_bytes : (load_bytes / tq) * nq);
+                        if (HAS_ACC) bulk_load(stg, sg.acc + e, 16u * nq, &full[s], pol);
+#pragma unroll
+                        for (int j = 0; j < KA; ++j)
+                            if (j < K) bulk_load(stg + off_g + 8u * tq * j, gb[j] + e, 8u * nq, &full[s], pol);
+                        bulk_load(stg + off_p, sg.p + e, 16u * nq, &full[s], pol);
+                        bulk_load(stg + off_m, sg.m + e, 16u * nq, &full[s], pol);
+                        bulk_load(stg + off_v, sg.v + e, 16u * nq, &full[s], pol);
+                    } else {
+                        mbar_arrive(&full[s]);
+                    }
+                    ++issued;
+                }
+            }
+            u = un;
+            un = unn;
+            rec = recn;
+        }
+        if (ok) {
+            const int s = acquire();
+            if (s >= 0) {
+                desc[s].chunk = kTileEnd;
+                mbar_arrive(&full[s]);
+                while (stored < issued)
+                    if (!retire()) break;
+            }
+        }
+        if (stored < issued) {
+            // gave up: let the loads still in flight land before leaving
+            for (int i = stored; i < issued; ++i)
+                mbar_wait(&full[i % nst], (uint32_t)(i / nst) & 1u, kPipeDrainNs);
+            // and keep the counter's reset rule: claim (without work) up to the first claim past the end
+            if (claims)
+                while (last < u1) last = u0 + atomicAdd(queue, 1u);
+        }
+        bulk_wait_all();
+        // every CTA's claims ended on exactly one past the end; the last such claim resets the counter
+        if (claims && last - u0 == (u1 - u0) + gridDim.x - 1) atomicExch(queue, 0u);
+        return;
+    }
+
+    // -------------------------------------------------------- compute warps
+    const float c_hi = ns->c_hi, c_lo = ns->c_lo;
+    const uint32_t ct = threadIdx.x - 32;
+    for (int i = 0;; ++i) {
+        const int s = i % nst;
+        if (!mbar_wait(&full[s], (uint32_t)(i / nst) & 1u, kPipeWaitNs)) return;
+        const TileDesc d = desc[s];
+        if (d.chunk == kTileEnd) return;
+        const GroupK G = sh_g[d.group];
+        unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
+        const float4 *a4 = reinterpret_cast<const float4 *>(stg);
+        uint2 *g4 = reinterpret_cast<uint2 *>(stg + off_g);
+        float4 *p4 = reinterpret_cast<float4 *>(stg + off_p);
+        float4 *m4 = reinterpret_cast<float4 *>(stg + off_m);
+        float4 *v4 = reinterpret_cast<float4 *>(stg + off_v);
+        for (uint32_t q = ct; q < d.nq; q += kPipeCompute) {
+            float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
+            uint2 gv[KA];
+            if (HAS_ACC) av = a4[q];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < K) gv[j] = g4[(size_t)tq * j + q];
+            const float4 pv = p4[q], mv = m4[q], vv = v4[q];
+            const float4 e = fold_quad<HAS_ACC, KMAX>(av, gv, K);
+            const AdamOut o0 = adam_elem(__fmul_rn(e.x, gscale), pv.x, mv.x, vv.x, c_hi, c_lo, G);
+            const AdamOut o1 = adam_elem(__fmul_rn(e.y, gscale), pv.y, mv.y, vv.y, c_hi, c_lo, G);
+            const AdamOut o2 = adam_elem(__fmul_rn(e.z, gscale), pv.z, mv.z, vv.z, c_hi, c_lo, G);
+            const AdamOut o3 = adam_elem(__fmul_rn(e.w, gscale), pv.w, mv.w, vv.w, c_hi, c_lo, G);
+            p4[q] = make_float4(o0.p, o1.p, o2.p, o3.p);
+            m4[q] = make_float4(o0.m, o1.m, o2.m, o3.m);
+            v4[q] = make_float4(o0.v, o1.v, o2.v, o3.v);
+            g4[q] = make_uint2(pack_bf16x2(o0.p, o1.p), pack_bf16x2(o2.p, o3.p));
+        }
+        if (d.scalars) {
+            // the chunk's head (warp 0) and tail (warp 1) elements, straight from global memory
+            const Chunk ch = chunks[d.chunk];
+            const Seg sg = segs[ch.seg];
+            const uint32_t len = ch.len;
+            const uint32_t hb = pipe_head(sg.bf + ch.start, len);
+            const uint32_t tail0 = hb + ((((len - hb) >> 3) << 1) << 2);
+            const uint32_t w = ct >> 5, lane = ct & 31u;
+            const uint32_t i0 = w == 0 ? lane : (w == 1 ? tail0 + lane : len);
+            if (i0 < (w == 0 ? hb : len) && !check_fails(ch.start + len > sg.numel, kFaultChunkRange)) {
+                const float *a = sg.acc + ch.start;
+                const uint16_t *g[KA];
+#pragma unroll
+                for (int j = 0; j < KA; ++j)
+                    g[j] = (j < K) ? gt.get(sg.grad_slot, j) + sg.grad_off + ch.start : nullptr;
+                float *p = sg.p + ch.start;
+                float *m = sg.m + ch.start;
+                float *v = sg.v + ch.start;
+                const float ev = __fmul_rn(fold_scalar<HAS_ACC, KMAX>(a, g, K, i0), gscale);
+                const AdamOut o = adam_elem(ev, p[i0], m[i0], v[i0], c_hi, c_lo, G);
+                p[i0] = o.p;
+                m[i0] = o.m;
+                v[i0] = o.v;
+                sg.bf[ch.start + i0] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
+            }
+        }
+        fence_async_smem();
+        mbar_arrive(&done[s]);
+    }
+}
+
 }  // namespace bf16k

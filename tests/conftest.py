@@ -22,12 +22,19 @@ def pytest_collection_modifyitems(config, items):
 
 
 def pytest_sessionfinish(session, exitstatus):
+    # Every bounded wait of the fused step's copy pipeline completed: a wait that
+    # gave up during the session fails it (checked only where a GPU ran the tests).
+    from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
+    if C._lib is not None and "torch" in sys.modules and sys.modules["torch"].cuda.is_available():
+        rc, n = C.bf16opt_pipeline_timeouts()
+        print(f"\nstep pipeline: status {rc}, timed-out waits {n}")
+        if rc != 0 or n != 0:
+            session.exitstatus = 1
     # Under a checked build of the library (BF16OPT_CHECK_FAULTS set, the build
     # named by BF16OPT_LIBRARY), any bounds or alignment violation the kernels
     # recorded during the session fails it.
     if not os.environ.get("BF16OPT_CHECK_FAULTS"):
         return
-    from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
     rc, bits = C.bf16opt_debug_faults()
     print(f"\nchecked build: status {rc}, fault bits {bits:#x}")
     if rc != 0 or bits != 0:

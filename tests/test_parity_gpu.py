@@ -81,10 +81,15 @@ def test_device_generator_matches_host():
 # ------------------------------------------------------------- dense parity
 
 @needs_cuda
+@pytest.mark.parametrize("step", ["auto", "pipe"])
 @pytest.mark.parametrize("defer", [False, True])
-def test_tiny_workload_dense(defer):
+def test_tiny_workload_dense(defer, step, monkeypatch):
+    """The 1M-element shard, 3 steps; "pipe": the fused step forced through the
+    bulk-copy pipeline (a shard this small takes vector loads by default)."""
+    if step == "pipe":
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     st = dense_parity(workloads.workload(1), defer=defer)
-    print("tiny", defer, st)
+    print("tiny", defer, step, st)
 
 
 @needs_cuda
@@ -112,10 +117,13 @@ SMALL = [
 
 
 @needs_cuda
+@pytest.mark.parametrize("step", ["auto", "pipe"])
 @pytest.mark.parametrize("case", range(len(SMALL)))
 @pytest.mark.parametrize("mode", ["flat", "list"])
 @pytest.mark.parametrize("defer", [False, True])
-def test_small_ragged_variants(case, mode, defer):
+def test_small_ragged_variants(case, mode, defer, step, monkeypatch):
+    if step == "pipe":
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     sizes, mis, gas, steps, sigma = SMALL[case]
     decay = [(i % 3) != 1 for i in range(len(sizes))]
     wl = workloads.custom(100 + case, sizes, decay=decay, gas=gas, steps=steps, grad_sigma=sigma, misalign=mis,
@@ -124,13 +132,17 @@ def test_small_ragged_variants(case, mode, defer):
 
 
 @needs_cuda
-@pytest.mark.parametrize("sched", ["auto", "claim"])
+@pytest.mark.parametrize("sched", ["auto", "claim", "pipe"])
 def test_list_more_tensors_than_one_launch(sched, monkeypatch):
     """1100 tensors (> 1024 gradient pointers per launch): two launches per pass
     (three with two pointers per tensor) -- with claiming forced on, the
-    launches of one pass share the chunk counter one after another."""
-    if sched == "claim":
+    launches of one pass share the chunk counter one after another; "pipe"
+    also forces the fused step through the bulk-copy pipeline, whose launches
+    share the counter the same way."""
+    if sched in ("claim", "pipe"):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
+    if sched == "pipe":
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     rng = np.random.default_rng(5)
     sizes = rng.integers(1, 700, 1100).tolist()
     wl = workloads.custom(150, sizes, decay=[i % 2 == 0 for i in range(1100)], gas=2, steps=2,
@@ -301,6 +313,61 @@ def test_lr_override_and_resume():
 
 
 @needs_cuda
+@pytest.mark.parametrize("pipe", ["0", "1"])
+def test_step_kernel_follows_the_switch(pipe, monkeypatch):
+    """BF16OPT_STEP_PIPE=1 runs the fused step as the bulk-copy pipeline
+    kernel, =0 as the vector-load kernel -- so the tests that force either one
+    exercise the kernel they name."""
+    monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
+    wl = workloads.custom(196, [20_001, 77], decay=[True, False], gas=2, steps=1, grad_sigma=0.1, misalign=3)
+    sh = GpuShard(wl, defer=True)
+    assert C.bf16opt_step_path(sh.opt.h) == (0, C.BF16OPT_PATH_NONE)
+    sh.run(1)
+    want = C.BF16OPT_PATH_PIPELINE if pipe == "1" else C.BF16OPT_PATH_VECTOR
+    assert C.bf16opt_step_path(sh.opt.h) == (0, want)
+    sh.close()
+
+
+@needs_cuda
+def test_pipe_needs_bf16_offsets_alike():
+    """Gradients 4 elements (8 bytes) off the parameters' offset modulo 16 bytes:
+    vector loads still apply (same offset modulo 8 bytes) but no element puts
+    every bf16 stream on a 16-byte boundary, so the step takes the vector-load
+    kernel even when the pipeline is asked for -- and equals the oracle."""
+    import os
+    wl = workloads.custom(197, [10_007, 64], decay=[True, False], gas=2, steps=2, grad_sigma=0.1)
+    n = wl.n
+    os.environ["BF16OPT_STEP_PIPE"] = "1"
+    try:
+        flat = {k: torch.zeros(n, dtype=dt, device="cuda") for k, dt in
+                (("master", torch.float32), ("exp_avg", torch.float32), ("exp_avg_sq", torch.float32),
+                 ("grad_accum", torch.float32), ("param_bf16", torch.int16))}
+        sgpu.fill_master(wl, flat["master"])
+        opt = BF16Optimizer(wl.groups, flat=flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
+    finally:
+        os.environ.pop("BF16OPT_STEP_PIPE", None)
+    gb = torch.empty(n + 64, dtype=torch.int16, device="cuda")[4:4 + n]
+    norms = []
+
+    def one(s):
+        for k in range(wl.gas):
+            sgpu.fill_grad(wl, s, k, gb)
+            opt.accumulate(gb, first=k == 0, last=k == wl.gas - 1, defer=k == wl.gas - 1)
+        norms.append(opt.grad_norm(sync=True))
+        opt.step()
+
+    one(0)
+    assert C.bf16opt_step_path(opt.h) == (0, C.BF16OPT_PATH_VECTOR)
+    one(1)
+    got = dict(p=flat["master"].cpu().numpy(), m=flat["exp_avg"].cpu().numpy(), v=flat["exp_avg_sq"].cpu().numpy(),
+               acc=flat["grad_accum"].cpu().numpy(), p_bf16=flat["param_bf16"].cpu().numpy().view(np.uint16))
+    opt.close()
+    ref, scales = oracle_dense(wl, wl.steps)
+    check_norms(norms, ref["sumsq"])
+    compare(got, ref, scales, wl, check_acc=False)
+
+
+@needs_cuda
 def test_inconsistent_alignment_falls_back_correctly():
     """Buffers with different offsets modulo 16 B take the element-wise path."""
     wl = workloads.custom(195, [10007], gas=2, steps=2, grad_sigma=0.1)
@@ -467,10 +534,14 @@ DEFER_PATTERNS = [
 
 
 @needs_cuda
+@pytest.mark.parametrize("step", ["auto", "pipe"])
 @pytest.mark.parametrize("pat", range(len(DEFER_PATTERNS)))
 @pytest.mark.parametrize("mode", ["flat", "list"])
-def test_deferred_patterns(pat, mode):
-    """Deferring any micro-batches folds the same FP32 adds in the same order."""
+def test_deferred_patterns(pat, mode, step, monkeypatch):
+    """Deferring any micro-batches folds the same FP32 adds in the same order
+    (with "pipe", in the bulk-copy step too: up to 8 gradient slots per stage)."""
+    if step == "pipe":
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     pattern = DEFER_PATTERNS[pat]
     sizes = [50_001, 3, 16_384, 777] if mode == "flat" else [20_000, 5, 16_385, 1200]
     wl = workloads.custom(240 + pat, sizes, decay=[True, False, True, False], gas=len(pattern), steps=2,
@@ -503,9 +574,11 @@ def test_results_do_not_depend_on_the_grid(monkeypatch):
     wl = workloads.custom(250, [300_001, 4097, 77], decay=[True, False, True], gas=3, steps=2, grad_sigma=0.1,
                           misalign=1)
     outs = []
-    for cap, sched in ((None, "static"), ("1", "static"), ("7", "static"), (None, "claim"), ("1", "claim"),
-                       ("7", "claim")):
+    for cap, sched, pipe in ((None, "static", "0"), ("1", "static", "0"), ("7", "static", "0"), (None, "claim", "0"),
+                             ("1", "claim", "0"), ("7", "claim", "0"), (None, "static", "1"), ("1", "static", "1"),
+                             ("7", "claim", "1"), (None, "claim", "1")):
         monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
         if cap is None:
             monkeypatch.delenv("BF16OPT_MAX_GRID", raising=False)
         else:
@@ -523,7 +596,7 @@ def test_results_do_not_depend_on_the_grid(monkeypatch):
 # ------------------------------------------------------------ CUDA graphs
 
 @needs_cuda
-@pytest.mark.parametrize("sched", ["auto", "claim"])
+@pytest.mark.parametrize("sched", ["auto", "claim", "pipe"])
 @pytest.mark.parametrize("mode", ["flat", "list"])
 def test_cuda_graph_replay_matches_eager(mode, sched, monkeypatch):
     """One step captured into a CUDA graph and replayed for the later steps
@@ -532,8 +605,10 @@ def test_cuda_graph_replay_matches_eager(mode, sched, monkeypatch):
     per-step scalars live on the device.  With chunk claiming forced on, the
     replays also show that the claim counter is back at zero after every pass
     (it resets itself; no memset node sits in the graph)."""
-    if sched == "claim":
+    if sched in ("claim", "pipe"):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
+    if sched == "pipe":
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     wl = workloads.custom(260, [40_000, 3, 16_385, 999], decay=[True, False, True, False], gas=3, steps=4,
                           grad_sigma=0.1, misalign=2, mode=mode)
     eager = GpuShard(wl, defer=[False, True, True])
@@ -827,9 +902,12 @@ def test_random_sequences_match_oracle(seed, monkeypatch):
     """Random shapes, layouts, GAS and deferral patterns: every one equals the
     oracle (norms, m, v, master, bf16) over two steps.  Half of the seeds
     force chunk claiming on (these shards are small enough to take the fixed
-    stride by default)."""
+    stride by default), half force the fused step through the bulk-copy
+    pipeline."""
     if seed % 4 in (1, 2):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
+    if seed % 4 in (2, 3):
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
     wl, pattern, gscale = _random_case(seed)
     dense_parity(wl, defer=pattern, grad_scale=gscale)
 
@@ -907,7 +985,9 @@ def test_small_sizes_every_misalignment(mode):
     """Every buffer offset 0..7 elements for sizes around the quad, warp and
     128-byte boundaries (1 ... 4097 elements; LIST adds a second, 5-element
     tensor), GAS cycling 1, 2, 3 and the last micro-batch deferred on every
-    other case: 152 dense runs, each equal to the oracle over two steps."""
+    other case, the fused step through vector loads and through the bulk-copy
+    pipeline: 304 dense runs, each equal to the oracle over two steps."""
+    import os
     case = 0
     for n in SWEEP_SIZES:
         for mis in range(8):
@@ -915,10 +995,15 @@ def test_small_sizes_every_misalignment(mode):
             sizes = [n] if mode == "flat" else [n, 5]
             wl = workloads.custom(600 + case, sizes, decay=[True, False][:len(sizes)], gas=gas, steps=2,
                                   grad_sigma=0.3, misalign=mis, mode=mode)
-            try:
-                dense_parity(wl, defer=bool(case % 2))
-            except AssertionError as e:
-                raise AssertionError(f"n={n} misalign={mis} gas={gas} defer={bool(case % 2)}: {e}") from None
+            for pipe in ("0", "1"):
+                os.environ["BF16OPT_STEP_PIPE"] = pipe
+                try:
+                    dense_parity(wl, defer=bool(case % 2))
+                except AssertionError as e:
+                    raise AssertionError(f"n={n} misalign={mis} gas={gas} defer={bool(case % 2)} "
+                                         f"pipe={pipe}: {e}") from None
+                finally:
+                    os.environ.pop("BF16OPT_STEP_PIPE", None)
             case += 1
 
 
@@ -1065,14 +1150,16 @@ def test_fast_pinned_buffers():
 @needs_cuda
 def test_claimed_chunks_on_a_full_chunk_shard(monkeypatch):
     """A shard of 2^25 + 4099 elements (full 32,768-element chunks, so its CTAs
-    claim chunks by default) over many passes -- every deferral pattern the
-    bench uses, two steps each -- equals the fixed-stride schedule bit for bit
-    and the oracle within the tolerance."""
+    claim chunks, and its fused step runs the bulk-copy pipeline, by default)
+    over many passes -- every deferral pattern the bench uses, two steps each --
+    equals the fixed-stride schedule and the vector-load step bit for bit and
+    the oracle within the tolerance."""
     wl = workloads.custom(280, [(1 << 25) - 1000, 5099], decay=[True, False], gas=4, steps=2, grad_sigma=0.01,
                           misalign=3)
     outs = []
-    for sched in ("claim", "static"):
+    for sched, pipe in (("claim", "1"), ("static", "1"), ("claim", "0"), ("static", "0")):
         monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
+        monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
         for pat in ([False, False, False, True], [True] * 4, [True, False, True, True]):
             sh = GpuShard(wl, defer=pat)
             sh.run(wl.steps)
