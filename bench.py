@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "optimizer-step elements/s and achieved HBM GB/s (% of peak) on 1 GB300"
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_step_scaled_bloom_prefix_134m.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_step_pipe_scaled_bloom_prefix_134m.md")
 # the kernels and their launch shape: the recorded ncu traffic holds while this file is unchanged
 KERNEL_SOURCES = [os.path.join(ROOT, "mixed_precision_optimizer_bf16_gb300", "csrc", "kernels.cuh")]
 

@@ -366,15 +366,15 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
     constexpr int U = KMAX <= 1 ? BF16K_STEP_U : (KMAX <= 4 ? BF16K_FOLD4_STEP_U : BF16K_FOLD8_STEP_U);
     cudaError_t e = cudaSuccess;
     bool first = true;
-    const bool pipe = h->pipe && pipe_aligned(h, fs, HAS_ACC);
     const int K = (int)fs.count();
+    const bool pipe = KMAX <= 4 && h->pipe && pipe_fits(HAS_ACC, K) && pipe_aligned(h, fs, HAS_ACC);
     h->step_path = pipe ? BF16OPT_PATH_PIPELINE : BF16OPT_PATH_VECTOR;
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
-        if (pipe) {
+        if constexpr (KMAX <= 4) {
+          if (pipe) {
             auto kp = k_step_pipe<HAS_ACC, KMAX, GT>;
-            const size_t smem = (size_t)pipe_stages(HAS_ACC, K) * pipe_quad_bytes(HAS_ACC, K) *
-                                pipe_tile_quads(HAS_ACC, K);
+            const size_t smem = (size_t)pipe_stages(HAS_ACC, K) * pipe_quad_bytes(HAS_ACC, K) * kPipeTileQuads;
             cudaError_t e1 = kernel_attr_once(kp, h->device, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)kPipeSmem);   // the most any K of the variant takes
             const uint32_t u0 = h->chunk_unit0[c0], u1 = h->chunk_unit0[c1];
@@ -388,6 +388,7 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
             first = false;
             if (e == cudaSuccess) e = e1;
             return;
+          }
         }
         auto k = k_step<HAS_ACC, KMAX, GT, U>;
         const int grid = grid_for(h, k, c1 - c0, kStepThreads);

@@ -938,15 +938,22 @@ __host__ __device__ constexpr uint32_t pipe_quad_bytes(bool has_acc, int K) {
 }
 // Quads per tile (a stage holds one tile): even, so that every bf16 run is a
 // multiple of 16 bytes.
-__host__ __device__ constexpr uint32_t pipe_tile_quads(bool has_acc, int K) {
-    return pipe_quad_bytes(has_acc, K) <= 80u ? 512u : 256u;
+constexpr uint32_t kPipeTileQuads = 512;
+// The pipeline takes passes whose stage is at most 80 bytes per quad (the
+// accumulator with up to 2 deferred gradients, or up to 4 without it): five
+// 40 KB stages.  Folding more gradients, a stage holds one 4 KB run per
+// gradient; folding 8 of them through the pipeline made the whole step 7-13 %
+// slower than with vector loads (the GAS-32 and 72-tensor shards).
+constexpr uint32_t kPipeMaxQuadBytes = 80;
+__host__ __device__ constexpr bool pipe_fits(bool has_acc, int K) {
+    return pipe_quad_bytes(has_acc, K) <= kPipeMaxQuadBytes;
 }
 __host__ __device__ constexpr int pipe_stages(bool has_acc, int K) {
-    return (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * pipe_tile_quads(has_acc, K))) < kPipeMaxStages
-               ? (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * pipe_tile_quads(has_acc, K)))
+    return (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * kPipeTileQuads)) < kPipeMaxStages
+               ? (int)(kPipeSmem / (pipe_quad_bytes(has_acc, K) * kPipeTileQuads))
                : kPipeMaxStages;
 }
-static_assert(pipe_stages(true, kMaxFold) > kPipeLag && pipe_stages(false, 1) <= kPipeMaxStages, "pipeline depth");
+static_assert(pipe_stages(false, 4) > kPipeLag && pipe_stages(false, 4) >= 4, "pipeline depth");
 
 // Leading scalar elements of a chunk before its bulk body: up to the first
 // element at which the bf16 parameter pointer is 16-byte aligned.  The host
@@ -970,7 +977,7 @@ __host__ __device__ __forceinline__ uint32_t pipe_head(const uint16_t *bf, uint3
 #define BF16K_PIPE_UNIT_QUADS 2048
 #endif
 constexpr uint32_t kPipeUnitQuads = BF16K_PIPE_UNIT_QUADS;
-static_assert(kPipeUnitQuads % 512 == 0, "a unit is whole tiles of every variant");
+static_assert(kPipeUnitQuads % kPipeTileQuads == 0, "a unit is whole tiles");
 struct PipeUnit {
     uint64_t el;        // first body element, relative to the segment
     uint32_t seg;
@@ -998,6 +1005,7 @@ constexpr uint32_t kTileEnd = 0xffffffffu;
 // ring of shared-memory stages: acc, the deferred gradients, master, m and v
 // in; master, m, v and the bf16 parameters out, in place.  The compute warps
 // take the stages in order, update them and release them to the copy thread.
+// The host launches it only when pipe_fits(HAS_ACC, K).
 template <bool HAS_ACC, int KMAX, class GT>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, const PipeUnit *__restrict__ units,
@@ -1012,7 +1020,7 @@ k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, cons
     pdl_enter();
     if (st->skip) return;                   // non-finite norm, skipping enabled (no CTA claims a chunk)
     if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
-    const uint32_t tq = pipe_tile_quads(HAS_ACC, K);
+    constexpr uint32_t tq = kPipeTileQuads;
     const int nst = pipe_stages(HAS_ACC, K);
     for (int i = threadIdx.x; i < kMaxGroups; i += kPipeThreads) sh_g[i] = st->gtab.g[i];
     if (threadIdx.x == 0) {
