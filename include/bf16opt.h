@@ -404,16 +404,17 @@ int bf16opt_grad_norm_static(const float *grad_accum, uint64_t n, float grad_sca
 int bf16opt_step_path(const bf16opt_t *h, int *path);
 
 /* ---- pipeline health ----------------------------------------------------
- * No counterpart in the paper: a health check of the fused step's copy
- * pipeline.  On shards of 2^25 elements and more whose buffers are aligned
- * alike (per segment: the FP32 streams at one element index modulo 4, the
- * bf16 streams at one modulo 8, agreeing modulo 4) bf16opt_step moves its
- * traffic with bulk asynchronous copies through a ring of shared-memory
- * stages (the environment variable BF16OPT_STEP_PIPE=1 / 0, read when a handle
- * is created, forces it on / off), and every wait on a stage is bounded (2 s; a
- * stage normally turns over in microseconds).  A wait that gives up is
- * counted in a device word and its CTA stops, leaving the rest of its chunks
- * of that step not updated.  This call waits for the device, stores the count
+ * No counterpart in the paper: a health check of the copy pipeline.  On
+ * shards of 2^25 elements and more whose buffers are aligned alike (per
+ * segment: the FP32 streams at one element index modulo 4, the bf16 streams
+ * at one modulo 8, agreeing modulo 4), bf16opt_step and the accumulate passes
+ * after FIRST that store the accumulator move their traffic with bulk
+ * asynchronous copies through a ring of shared-memory stages.  The
+ * environment variable BF16OPT_PIPE=1 / 0, read when a handle is created,
+ * forces this on / off.  Every wait on a stage is bounded (2 s; a stage
+ * normally turns over in microseconds).  A wait that gives up is counted in
+ * a device word and its CTA stops, leaving the rest of its units of that
+ * pass not updated.  This call waits for the device, stores the count
  * into *count (0 = every step completed) and clears it.
  * Errors: INVALID_ARG (count NULL), UNSUPPORTED (no device), CUDA. */
 int bf16opt_pipeline_timeouts(uint32_t *count);

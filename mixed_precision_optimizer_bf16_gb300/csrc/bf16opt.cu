@@ -73,7 +73,7 @@ struct bf16opt {
     bool skip_nonfinite = false;
     bool pdl = true;                     // launch with programmatic stream serialization (BF16OPT_PDL=0: off)
     bool claim = true;                   // CTAs claim chunks from queue_d (BF16OPT_SCHEDULE=static: fixed stride)
-    bool pipe = true;                    // fused step through the bulk-copy pipeline (BF16OPT_STEP_PIPE=0: vector loads)
+    bool pipe = true;                    // step and later accumulates through the bulk-copy pipeline (BF16OPT_PIPE)
     int step_path = BF16OPT_PATH_NONE;   // data path of the last step (bf16opt_step_path)
     bool scalars_ready = false;          // the norm kernel prepared this step's scalars (groups' own lr)
     bf16opt_lr_schedule_t sched{};
@@ -301,12 +301,59 @@ int for_each_launch(bf16opt_t *h, const FoldSet &fs, F &&launch) {
     return 0;
 }
 
+// The bulk-copy passes need every stream of a chunk's body 16-byte aligned at
+// one element: per segment, the FP32 pointers (master, m, v, the accumulator
+// if used) share their element index modulo 4, the bf16 ones (parameters,
+// folded gradients) share theirs modulo 8, and the two agree modulo 4.  (The
+// units' bodies start where the bf16 parameters are 16-byte aligned.)
+bool pipe_aligned(const bf16opt_t *h, const FoldSet &fs, bool has_acc) {
+    const size_t K = fs.count();
+    for (const Seg &s : h->segs) {
+        if (s.numel == 0) continue;
+        const uint32_t f = (uint32_t)(((uintptr_t)s.p >> 2) & 3u);
+        const uint32_t b = (uint32_t)(((uintptr_t)s.bf >> 1) & 7u);
+        if ((b & 3u) != f) return false;
+        for (const float *x : {s.m, s.v})
+            if ((uint32_t)(((uintptr_t)x >> 2) & 3u) != f) return false;
+        if (has_acc && (uint32_t)(((uintptr_t)s.acc >> 2) & 3u) != f) return false;
+        for (size_t j = 0; j < K; ++j) {
+            const uint16_t *g = (h->mode == BF16OPT_FLAT ? fs.flat[j] : (*fs.list[j])[s.grad_slot]) + s.grad_off;
+            if ((uint32_t)(((uintptr_t)g >> 1) & 7u) != b) return false;
+        }
+    }
+    return true;
+}
+
 template <bool HAS_ACC, int KMAX, bool WRITE, bool NORM>
 int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
     constexpr int U = KMAX <= 1 ? BF16K_ACC_U : (KMAX <= 4 ? BF16K_FOLD4_ACC_U : BF16K_FOLD8_ACC_U);
     cudaError_t e = cudaSuccess;
+    // A pass that adds one gradient to the stored accumulator and stores it
+    // takes the bulk-copy pipeline where the fused step does (the pipeline's
+    // size rule, buffers aligned alike): on the 1.72B shard 2.398 against
+    // 2.443 ms.  The FIRST pass (no accumulator read) was slower through it
+    // (1.560 against 1.499 ms); passes with the norm or several gradients keep
+    // vector loads too.
+    const bool pipe = HAS_ACC && KMAX == 1 && WRITE && !NORM && h->pipe && pipe_aligned(h, fs, true);
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
+        if constexpr (HAS_ACC && KMAX == 1 && WRITE && !NORM) {
+            if (pipe) {
+                auto kp = k_accum_pipe<GT>;
+                constexpr size_t smem = (size_t)kAccStages * kAccQuadBytes * kAccTileQuads;
+                cudaError_t e1 = kernel_attr_once(kp, h->device, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)smem);
+                const uint32_t u0 = h->chunk_unit0[c0], u1 = h->chunk_unit0[c1];
+                uint64_t grid = std::min<uint64_t>((uint64_t)h->sm_count, u1 - u0);
+                if (h->max_grid > 0 && grid > (uint64_t)h->max_grid) grid = (uint64_t)h->max_grid;
+                if (e1 == cudaSuccess)
+                    e1 = launch_smem(h, kp, (unsigned)std::max<uint64_t>(1, grid), kPipeThreads, smem, st,
+                                     (const Seg *)h->segs_d, (const Chunk *)h->chunks_d,
+                                     (const PipeUnit *)h->units_d, u0, u1, gt, h->claim ? h->queue_d : nullptr);
+                if (e == cudaSuccess) e = e1;
+                return;
+            }
+        }
         auto k = k_accum<HAS_ACC, KMAX, WRITE, NORM, GT, U>;
 #if BF16K_STREAM_CARVEOUT >= 0
         if (kernel_attr_once(k, h->device, cudaFuncAttributePreferredSharedMemoryCarveout, BF16K_STREAM_CARVEOUT) !=
@@ -336,27 +383,6 @@ int launch_accum(bf16opt_t *h, bool has_acc, const FoldSet &fs, cudaStream_t st)
 
 constexpr uint64_t kStepClaimChunksPerCta = 64;
 
-// The bulk-copy step needs every stream of a chunk's body 16-byte aligned at
-// one element: per segment, the FP32 pointers (master, m, v, the accumulator
-// if read) share their element index modulo 4, the bf16 ones (parameters,
-// folded gradients) share theirs modulo 8, and the two agree modulo 4.
-bool pipe_aligned(const bf16opt_t *h, const FoldSet &fs, bool has_acc) {
-    const size_t K = fs.count();
-    for (const Seg &s : h->segs) {
-        if (s.numel == 0) continue;
-        const uint32_t f = (uint32_t)(((uintptr_t)s.p >> 2) & 3u);
-        const uint32_t b = (uint32_t)(((uintptr_t)s.bf >> 1) & 7u);
-        if ((b & 3u) != f) return false;
-        for (const float *x : {s.m, s.v})
-            if ((uint32_t)(((uintptr_t)x >> 2) & 3u) != f) return false;
-        if (has_acc && (uint32_t)(((uintptr_t)s.acc >> 2) & 3u) != f) return false;
-        for (size_t j = 0; j < K; ++j) {
-            const uint16_t *g = (h->mode == BF16OPT_FLAT ? fs.flat[j] : (*fs.list[j])[s.grad_slot]) + s.grad_off;
-            if ((uint32_t)(((uintptr_t)g >> 1) & 7u) != b) return false;
-        }
-    }
-    return true;
-}
 
 
 // commit_t: the first launch advances the device step counter (the step's
@@ -768,13 +794,13 @@ int bf16opt_create(const bf16opt_desc_t *d, bf16opt_t **out) {
     // BF16OPT_SCHEDULE=static / claim overrides (to compare).
     h->claim = total >= (uint64_t(1) << 25);
     if (const char *sc = std::getenv("BF16OPT_SCHEDULE")) h->claim = std::strcmp(sc, "static") != 0;
-    // The fused step moves its traffic with bulk copies on shards of 2^25
-    // elements and more (it also needs buffers aligned alike, see
-    // pipe_aligned); on a 1M-element shard the pipeline's fill cost more than
-    // it gained (12.4 vs 10.4 us).  BF16OPT_STEP_PIPE=1 / 0 overrides (to test
-    // and compare).
+    // The fused step and the accumulate passes after FIRST move their traffic
+    // with bulk copies on shards of 2^25 elements and more (they also need
+    // buffers aligned alike, see pipe_aligned); on a 1M-element shard the
+    // pipeline's fill cost more than it gained (step 12.4 vs 10.4 us).
+    // BF16OPT_PIPE=1 / 0 overrides (to test and compare).
     h->pipe = total >= (uint64_t(1) << 25);
-    if (const char *sp = std::getenv("BF16OPT_STEP_PIPE")) h->pipe = std::atoi(sp) != 0;
+    if (const char *sp = std::getenv("BF16OPT_PIPE")) h->pipe = std::atoi(sp) != 0;
 
     cudaError_t e = cudaSuccess;
     const size_t nseg = std::max<size_t>(1, segs.size()), nch = std::max<size_t>(1, chunks.size());

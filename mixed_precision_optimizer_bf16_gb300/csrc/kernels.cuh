@@ -930,16 +930,16 @@ constexpr int kPipeMaxStages = 8;
 constexpr int kPipeLag = 1;                             // stores still reading a stage when the next load is issued
 static_assert(kPipeWarps >= 2, "the head and tail scalars go to compute warps 0 and 1");
 
-// Bytes of one stage per 4-element quad: the accumulator, K gradient slots
-// (one when K = 0: the bf16 output; otherwise slot 0 takes the bf16 output
-// after the gradients are read), master, m, v.
+// Bytes of one fused-step stage per 4-element quad: the accumulator, K
+// gradient slots (one when K = 0: the bf16 output; otherwise slot 0 takes the
+// bf16 output after the gradients are read), master, m, v.
 __host__ __device__ constexpr uint32_t pipe_quad_bytes(bool has_acc, int K) {
     return (has_acc ? 16u : 0u) + 8u * (uint32_t)(K > 0 ? K : 1) + 48u;
 }
-// Quads per tile (a stage holds one tile): even, so that every bf16 run is a
-// multiple of 16 bytes.
+// Quads per fused-step tile (a stage holds one tile): even, so that every
+// bf16 run is a multiple of 16 bytes.
 constexpr uint32_t kPipeTileQuads = 512;
-// The pipeline takes passes whose stage is at most 80 bytes per quad (the
+// The pipeline takes fused steps whose stage is at most 80 bytes per quad (the
 // accumulator with up to 2 deferred gradients, or up to 4 without it): five
 // 40 KB stages.  Folding more gradients, a stage holds one 4 KB run per
 // gradient; folding 8 of them through the pipeline made the whole step 7-13 %
@@ -955,6 +955,18 @@ __host__ __device__ constexpr int pipe_stages(bool has_acc, int K) {
 }
 static_assert(pipe_stages(false, 4) > kPipeLag && pipe_stages(false, 4) >= 4, "pipeline depth");
 
+// An accumulate pass's stage: one tile of 2,048 quads (8,192 elements, one
+// claimed unit), accumulator 32 KB + gradient 16 KB; four stages.  Probe on
+// a later pass's traffic (6:4 bytes read:written) over 1.8e9 elements: 7.22
+// TB/s against 7.15 with 16-byte vector loads; with 4,096-element tiles it
+// was slower than vector loads (the copy thread's work per tile dominated).
+constexpr uint32_t kAccTileQuads = 2048;
+constexpr uint32_t kAccQuadBytes = 24;
+constexpr int kAccStages = (int)(kPipeSmem / (kAccQuadBytes * kAccTileQuads)) < kPipeMaxStages
+                               ? (int)(kPipeSmem / (kAccQuadBytes * kAccTileQuads))
+                               : kPipeMaxStages;
+static_assert(kAccStages > kPipeLag && kAccStages >= 4, "accumulate pipeline depth");
+
 // Leading scalar elements of a chunk before its bulk body: up to the first
 // element at which the bf16 parameter pointer is 16-byte aligned.  The host
 // runs the pipeline only on segments whose FP32 pointers share their element
@@ -965,7 +977,7 @@ __host__ __device__ __forceinline__ uint32_t pipe_head(const uint16_t *bf, uint3
     return h < len ? h : len;
 }
 
-// The pipelined step's unit of work, claimed one at a time: up to
+// The pipelined passes' unit of work, claimed one at a time: up to
 // kPipeUnitQuads quads of one chunk's body (a chunk without body, only scalar
 // elements, is one unit with nq = 0).  The host lists the units of every
 // chunk in chunk order.  Measured on the 1.72B-element shard (step kernel):
@@ -977,7 +989,7 @@ __host__ __device__ __forceinline__ uint32_t pipe_head(const uint16_t *bf, uint3
 #define BF16K_PIPE_UNIT_QUADS 2048
 #endif
 constexpr uint32_t kPipeUnitQuads = BF16K_PIPE_UNIT_QUADS;
-static_assert(kPipeUnitQuads % kPipeTileQuads == 0, "a unit is whole tiles");
+static_assert(kPipeUnitQuads % kPipeTileQuads == 0 && kPipeUnitQuads % kAccTileQuads == 0, "a unit is whole tiles");
 struct PipeUnit {
     uint64_t el;        // first body element, relative to the segment
     uint32_t seg;
@@ -988,8 +1000,7 @@ struct PipeUnit {
 
 // What the copy thread tells the compute warps about the tile in a stage.
 struct TileDesc {
-    float *p, *m, *v;   // the tile's first body element in each output stream
-    uint16_t *bf;
+    void *out[4];       // the tile's first body element in each stream the pass stores
     uint32_t group;
     uint32_t nq;        // body quads in the tile (even; 0 for a chunk without body)
     uint32_t chunk;     // its chunk; kTileEnd: no more tiles for this CTA
@@ -997,178 +1008,252 @@ struct TileDesc {
 };
 constexpr uint32_t kTileEnd = 0xffffffffu;
 
-// Fused clip + AdamW + master update + bf16 cast over chunks [c0, c1), the
-// same arithmetic per element as k_step (bit-identical results), with the
-// traffic moved by bulk copies.  One CTA per SM.  Warp 0, lane 0, walks the
-// CTA's chunks (claimed from `queue`, or the fixed stride when it is null),
-// cuts each chunk's aligned body into tiles and streams each tile through a
-// ring of shared-memory stages: acc, the deferred gradients, master, m and v
-// in; master, m, v and the bf16 parameters out, in place.  The compute warps
-// take the stages in order, update them and release them to the copy thread.
-// The host launches it only when pipe_fits(HAS_ACC, K).
-template <bool HAS_ACC, int KMAX, class GT>
-__global__ void __launch_bounds__(kPipeThreads, 1)
-k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, const PipeUnit *__restrict__ units,
-            uint32_t u0, uint32_t u1, GT gt, StepState *st, const NormState *__restrict__ ns, float gscale,
-            int commit_t, unsigned *queue) {
-    extern __shared__ __align__(128) unsigned char pipe_smem[];
-    __shared__ uint64_t full[kPipeMaxStages], done[kPipeMaxStages];
-    __shared__ TileDesc desc[kPipeMaxStages];
-    __shared__ GroupK sh_g[kMaxGroups];
-    constexpr int KA = KMAX > 0 ? KMAX : 1;
-    const int K = KMAX <= 1 ? KMAX : (int)gt.k;
-    pdl_enter();
-    if (st->skip) return;                   // non-finite norm, skipping enabled (no CTA claims a chunk)
-    if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
-    constexpr uint32_t tq = kPipeTileQuads;
-    const int nst = pipe_stages(HAS_ACC, K);
-    for (int i = threadIdx.x; i < kMaxGroups; i += kPipeThreads) sh_g[i] = st->gtab.g[i];
+// The barriers and descriptors of a pipelined pass (static shared memory).
+struct PipeShared {
+    uint64_t full[kPipeMaxStages];   // a stage's loads landed (or a tile without body, or the end)
+    uint64_t done[kPipeMaxStages];   // the compute warps finished a stage
+    TileDesc desc[kPipeMaxStages];
+};
+
+// A pipelined pass over units [u0, u1): the same ring of shared-memory stages
+// for every pass, and an `Ops` type for what a pass moves and computes:
+//   kTileQuads                 quads per tile (even; divides kPipeUnitQuads)
+//   stages, stage_bytes        ring depth, bytes of one stage
+//   tile_bytes(nq)             bytes the loads of a tile of nq quads bring in
+//   set_seg(sg)                the copy thread's per-segment set-up
+//   misaligned(sg, e)          a stream not 16-byte aligned at element e (checked build)
+//   load(sg, e, nq, stage, bar, pol)   the tile's bulk loads, completing on bar
+//   outputs(sg, e, out)        where the tile's results go
+//   store(d, stage, pol)       the tile's bulk stores
+//   compute(d, stage, ct)      compute thread ct's quads of a stage, in place
+//   scalar(ch, sg, i, group)   element i of a chunk, from and to global memory
+//
+// Warp 0, lane 0, is the copy thread.  It claims units (from `queue`, or the
+// fixed stride when it is null), the next unit and its table entry one unit
+// ahead.  It cuts each unit into tiles and streams each tile through the
+// ring.  A stage is refilled once the tile that used it was stored and its
+// stores have read it; D = stages - kPipeLag tiles stay loaded ahead of the
+// oldest one not yet stored.  The compute warps take the stages in order,
+// update them in place, and release them to the copy thread; warps 0 and 1
+// also do a chunk's scalar head and tail elements with its first tile.
+//
+// Every wait is bounded (kPipeWaitNs).  A copy thread that gives up lets its
+// loads in flight land, keeps the counter's reset rule and returns; compute
+// warps that give up return.  g_pipe_timeouts counts every wait that gave up.
+template <class Ops>
+__device__ __forceinline__ void pipe_copy_thread(Ops &ops, const Seg *__restrict__ segs,
+                                                 const PipeUnit *__restrict__ units, uint32_t u0, uint32_t u1,
+                                                 unsigned *queue, unsigned char *smem, PipeShared &sh) {
+    constexpr int L = kPipeLag;
+    constexpr uint32_t tq = Ops::kTileQuads;
+    const int nst = ops.stages;
+    const int D = nst - L;
+    const uint64_t pol = l2_evict_first();
+    int issued = 0, stored = 0;
+    bool ok = true;
+    // The oldest computed tile's results go out.
+    auto retire = [&]() -> bool {
+        const int s = stored % nst;
+        if (!mbar_wait(&sh.done[s], (uint32_t)(stored / nst) & 1u, kPipeWaitNs)) return false;
+        if (sh.desc[s].nq) ops.store(sh.desc[s], smem + (size_t)s * ops.stage_bytes, pol);
+        bulk_commit();
+        ++stored;
+        return true;
+    };
+    // Stage for tile `issued`: free once the tile that used it was stored
+    // and its stores have read it.
+    auto acquire = [&]() -> int {
+        while (stored <= issued - D) {
+            if (!retire()) return -1;
+            bulk_wait_read<L>();
+        }
+        return issued % nst;
+    };
+    const bool claims = queue != nullptr;
+    uint32_t u = claims ? u0 + atomicAdd(queue, 1u) : u0 + blockIdx.x;
+    uint32_t last = u;                  // the most recent claim
+    uint32_t un = u;
+    if (u < u1) last = un = claims ? u0 + atomicAdd(queue, 1u) : u + gridDim.x;
+    PipeUnit rec{};
+    if (u < u1) rec = units[u];
+    uint32_t cur_seg = 0xffffffffu;
+    Seg sg{};
+    while (ok && u < u1) {
+        const bool more = un < u1;
+        PipeUnit recn{};
+        if (more) recn = units[un];
+        const uint32_t unn = more ? (claims ? u0 + atomicAdd(queue, 1u) : un + gridDim.x) : un;
+        if (more) last = unn;
+        if (rec.seg != cur_seg) {
+            cur_seg = rec.seg;
+            sg = segs[cur_seg];
+            ops.set_seg(sg);
+        }
+        const uint64_t e0 = rec.el;
+        bool bad = check_fails(e0 + 4ull * rec.nq > sg.numel, kFaultChunkRange);
+        if (rec.nq) bad = bad || check_fails(ops.misaligned(sg, e0), kFaultAlign);
+        if (!bad) {
+            for (uint32_t q = 0; q < rec.nq || q == 0; q += tq) {
+                const uint32_t nq = rec.nq - q < tq ? rec.nq - q : tq;
+                const int s = acquire();
+                if (s < 0) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t e = e0 + 4ull * q;
+                TileDesc &d = sh.desc[s];
+                ops.outputs(sg, e, d.out);
+                d.group = sg.group;
+                d.nq = nq;
+                d.chunk = rec.chunk;
+                d.scalars = q == 0 ? rec.scalars : 0u;
+                if (nq) {
+                    mbar_arrive_tx(&sh.full[s], ops.tile_bytes(nq));
+                    ops.load(sg, e, nq, smem + (size_t)s * ops.stage_bytes, &sh.full[s], pol);
+                } else {
+                    mbar_arrive(&sh.full[s]);
+                }
+                ++issued;
+            }
+        }
+        u = un;
+        un = unn;
+        rec = recn;
+    }
+    if (ok) {
+        const int s = acquire();
+        if (s >= 0) {
+            sh.desc[s].chunk = kTileEnd;
+            mbar_arrive(&sh.full[s]);
+            while (stored < issued)
+                if (!retire()) break;
+        }
+    }
+    if (stored < issued) {
+        // gave up: let the loads still in flight land before leaving
+        for (int i = stored; i < issued; ++i)
+            mbar_wait(&sh.full[i % nst], (uint32_t)(i / nst) & 1u, kPipeDrainNs);
+        // and keep the counter's reset rule: claim (without work) up to the first claim past the end
+        if (claims)
+            while (last < u1) last = u0 + atomicAdd(queue, 1u);
+    }
+    bulk_wait_all();
+    // every CTA's claims ended on exactly one past the end; the last such claim resets the counter
+    if (claims && last - u0 == (u1 - u0) + gridDim.x - 1) atomicExch(queue, 0u);
+}
+
+template <class Ops>
+__device__ __forceinline__ void pipe_compute_warps(const Ops &ops, const Seg *__restrict__ segs,
+                                                   const Chunk *__restrict__ chunks, unsigned char *smem,
+                                                   PipeShared &sh) {
+    const uint32_t ct = threadIdx.x - 32;
+    const int nst = ops.stages;
+    for (int i = 0;; ++i) {
+        const int s = i % nst;
+        if (!mbar_wait(&sh.full[s], (uint32_t)(i / nst) & 1u, kPipeWaitNs)) return;
+        const TileDesc d = sh.desc[s];
+        if (d.chunk == kTileEnd) return;
+        unsigned char *stg = smem + (size_t)s * ops.stage_bytes;
+        ops.compute(d, stg, ct);
+        if (d.scalars) {
+            // the chunk's head (warp 0) and tail (warp 1) elements, straight from global memory
+            const Chunk ch = chunks[d.chunk];
+            const Seg sg = segs[ch.seg];
+            const uint32_t len = ch.len;
+            const uint32_t hb = pipe_head(sg.bf + ch.start, len);
+            const uint32_t tail0 = hb + ((((len - hb) >> 3) << 1) << 2);
+            const uint32_t w = ct >> 5, lane = ct & 31u;
+            const uint32_t i0 = w == 0 ? lane : (w == 1 ? tail0 + lane : len);
+            if (i0 < (w == 0 ? hb : len) && !check_fails(ch.start + len > sg.numel, kFaultChunkRange))
+                ops.scalar(ch, sg, i0, d.group);
+        }
+        fence_async_smem();
+        mbar_arrive(&sh.done[s]);
+    }
+}
+
+// Sets up the barriers (thread 0), then runs the copy thread (warp 0, lane 0;
+// the rest of warp 0 leaves) or the compute warps.
+template <class Ops>
+__device__ __forceinline__ void pipe_run(Ops &ops, const Seg *__restrict__ segs, const Chunk *__restrict__ chunks,
+                                         const PipeUnit *__restrict__ units, uint32_t u0, uint32_t u1,
+                                         unsigned *queue, unsigned char *smem, PipeShared &sh) {
     if (threadIdx.x == 0) {
-        for (int i = 0; i < nst; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&done[i], kPipeCompute);
+        for (int i = 0; i < ops.stages; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.done[i], kPipeCompute);
         }
         mbar_init_fence();
     }
     __syncthreads();
-    // stage layout
-    const uint32_t off_g = HAS_ACC ? 16u * tq : 0u;
-    const uint32_t off_p = off_g + 8u * tq * (uint32_t)(K > 0 ? K : 1);
-    const uint32_t off_m = off_p + 16u * tq, off_v = off_m + 16u * tq;
-    const uint32_t stage_bytes = off_v + 16u * tq;
-    const uint32_t load_bytes = stage_bytes - (K == 0 ? 8u * tq : 0u);   // per full tile
-
     if (threadIdx.x < 32) {
-        if (threadIdx.x != 0) return;
-        // ---------------------------------------------------- copy thread
-        constexpr int L = kPipeLag;
-        const int D = nst - L;              // tiles loaded ahead of the oldest one not yet stored
-        const uint64_t pol = l2_evict_first();
-        int issued = 0, stored = 0;
-        bool ok = true;
-        // The oldest computed tile's results go out: p, m, v, bf16.
-        auto retire = [&]() -> bool {
-            const int s = stored % nst;
-            if (!mbar_wait(&done[s], (uint32_t)(stored / nst) & 1u, kPipeWaitNs)) return false;
-            const TileDesc d = desc[s];
-            if (d.nq) {
-                unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
-                bulk_store(d.p, stg + off_p, 16u * d.nq, pol);
-                bulk_store(d.m, stg + off_m, 16u * d.nq, pol);
-                bulk_store(d.v, stg + off_v, 16u * d.nq, pol);
-                bulk_store(d.bf, stg + off_g, 8u * d.nq, pol);
-            }
-            bulk_commit();
-            ++stored;
-            return true;
-        };
-        // Stage for tile `issued`: free once the tile that used it was stored
-        // and its stores have read it.
-        auto acquire = [&]() -> int {
-            while (stored <= issued - D) {
-                if (!retire()) return -1;
-                bulk_wait_read<L>();
-            }
-            return issued % nst;
-        };
-        // Units u0 + claim: the next unit is claimed, and its table entry
-        // loaded, one unit ahead, so neither round trip stalls the copies.
-        const bool claims = queue != nullptr;
-        uint32_t u = claims ? u0 + atomicAdd(queue, 1u) : u0 + blockIdx.x;
-        uint32_t last = u;                  // the most recent claim
-        uint32_t un = u;
-        if (u < u1) last = un = claims ? u0 + atomicAdd(queue, 1u) : u + gridDim.x;
-        PipeUnit rec{};
-        if (u < u1) rec = units[u];
-        uint32_t cur_seg = 0xffffffffu;
-        Seg sg{};
-        const uint16_t *gb[KA];
-        while (ok && u < u1) {
-            const bool more = un < u1;
-            PipeUnit recn{};
-            if (more) recn = units[un];
-            const uint32_t unn = more ? (claims ? u0 + atomicAdd(queue, 1u) : un + gridDim.x) : un;
-            if (more) last = unn;
-            if (rec.seg != cur_seg) {
-                cur_seg = rec.seg;
-                sg = segs[cur_seg];
-#pragma unroll
-                for (int j = 0; j < KA; ++j) gb[j] = (j < K) ? gt.get(sg.grad_slot, j) + sg.grad_off : nullptr;
-            }
-            const uint64_t e0 = rec.el;
-            bool bad = check_fails(e0 + 4ull * rec.nq > sg.numel, kFaultChunkRange);
-            if (rec.nq) {
-                bool mis = mis16(sg.p + e0) || mis16(sg.m + e0) || mis16(sg.v + e0) || mis16(sg.bf + e0) ||
-                           (HAS_ACC && mis16(sg.acc + e0));
-#pragma unroll
-                for (int j = 0; j < KA; ++j)
-                    if (j < K) mis = mis || mis16(gb[j] + e0);
-                bad = bad || check_fails(mis, kFaultAlign);
-            }
-            if (!bad) {
-                for (uint32_t q = 0; q < rec.nq || q == 0; q += tq) {
-                    const uint32_t nq = rec.nq - q < tq ? rec.nq - q : tq;
-                    const int s = acquire();
-                    if (s < 0) {
-                        ok = false;
-                        break;
-                    }
-                    const uint64_t e = e0 + 4ull * q;
-                    desc[s] = TileDesc{sg.p + e, sg.m + e, sg.v + e, sg.bf + e, sg.group, nq, rec.chunk,
-                                       q == 0 ? rec.scalars : 0u};
-                    if (nq) {
-                        unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
-                        mbar_arrive_tx(&full[s], nq == tq ? load_bytes : (load_bytes / tq) * nq);
-                        if (HAS_ACC) bulk_load(stg, sg.acc + e, 16u * nq, &full[s], pol);
-#pragma unroll
-                        for (int j = 0; j < KA; ++j)
-                            if (j < K) bulk_load(stg + off_g + 8u * tq * j, gb[j] + e, 8u * nq, &full[s], pol);
-                        bulk_load(stg + off_p, sg.p + e, 16u * nq, &full[s], pol);
-                        bulk_load(stg + off_m, sg.m + e, 16u * nq, &full[s], pol);
-                        bulk_load(stg + off_v, sg.v + e, 16u * nq, &full[s], pol);
-                    } else {
-                        mbar_arrive(&full[s]);
-                    }
-                    ++issued;
-                }
-            }
-            u = un;
-            un = unn;
-            rec = recn;
-        }
-        if (ok) {
-            const int s = acquire();
-            if (s >= 0) {
-                desc[s].chunk = kTileEnd;
-                mbar_arrive(&full[s]);
-                while (stored < issued)
-                    if (!retire()) break;
-            }
-        }
-        if (stored < issued) {
-            // gave up: let the loads still in flight land before leaving
-            for (int i = stored; i < issued; ++i)
-                mbar_wait(&full[i % nst], (uint32_t)(i / nst) & 1u, kPipeDrainNs);
-            // and keep the counter's reset rule: claim (without work) up to the first claim past the end
-            if (claims)
-                while (last < u1) last = u0 + atomicAdd(queue, 1u);
-        }
-        bulk_wait_all();
-        // every CTA's claims ended on exactly one past the end; the last such claim resets the counter
-        if (claims && last - u0 == (u1 - u0) + gridDim.x - 1) atomicExch(queue, 0u);
+        if (threadIdx.x == 0) pipe_copy_thread(ops, segs, units, u0, u1, queue, smem, sh);
         return;
     }
+    pipe_compute_warps(ops, segs, chunks, smem, sh);
+}
 
-    // -------------------------------------------------------- compute warps
-    const float c_hi = ns->c_hi, c_lo = ns->c_lo;
-    const uint32_t ct = threadIdx.x - 32;
-    for (int i = 0;; ++i) {
-        const int s = i % nst;
-        if (!mbar_wait(&full[s], (uint32_t)(i / nst) & 1u, kPipeWaitNs)) return;
-        const TileDesc d = desc[s];
-        if (d.chunk == kTileEnd) return;
-        const GroupK G = sh_g[d.group];
-        unsigned char *stg = pipe_smem + (size_t)s * stage_bytes;
+// The fused step's traffic and arithmetic per tile (see k_step_pipe).
+template <bool HAS_ACC, int KMAX, class GT>
+struct StepOps {
+    static constexpr uint32_t kTileQuads = kPipeTileQuads;
+    static constexpr int KA = KMAX > 0 ? KMAX : 1;
+    const GT *gt;
+    const GroupK *gtab;                 // the groups' scalars (shared memory)
+    int K;
+    float gscale, c_hi, c_lo;
+    int stages;
+    uint32_t stage_bytes, off_g, off_p, off_m, off_v;
+    const uint16_t *gb[KA];             // copy thread: the current segment's gradient bases
+
+    __device__ StepOps(const GT *g, const GroupK *tab, int k, float gs, float hi, float lo)
+        : gt(g), gtab(tab), K(k), gscale(gs), c_hi(hi), c_lo(lo) {
+        stages = pipe_stages(HAS_ACC, K);
+        off_g = HAS_ACC ? 16u * kTileQuads : 0u;
+        off_p = off_g + 8u * kTileQuads * (uint32_t)(K > 0 ? K : 1);
+        off_m = off_p + 16u * kTileQuads;
+        off_v = off_m + 16u * kTileQuads;
+        stage_bytes = off_v + 16u * kTileQuads;
+    }
+    __device__ uint32_t tile_bytes(uint32_t nq) const {
+        return nq * (pipe_quad_bytes(HAS_ACC, K) - (K == 0 ? 8u : 0u));   // no gradient slot is loaded when K = 0
+    }
+    __device__ void set_seg(const Seg &sg) {
+#pragma unroll
+        for (int j = 0; j < KA; ++j) gb[j] = (j < K) ? gt->get(sg.grad_slot, j) + sg.grad_off : nullptr;
+    }
+    __device__ bool misaligned(const Seg &sg, uint64_t e) const {
+        bool mis = mis16(sg.p + e) || mis16(sg.m + e) || mis16(sg.v + e) || mis16(sg.bf + e) ||
+                   (HAS_ACC && mis16(sg.acc + e));
+#pragma unroll
+        for (int j = 0; j < KA; ++j)
+            if (j < K) mis = mis || mis16(gb[j] + e);
+        return mis;
+    }
+    __device__ void load(const Seg &sg, uint64_t e, uint32_t nq, unsigned char *stg, uint64_t *bar,
+                         uint64_t pol) const {
+        if (HAS_ACC) bulk_load(stg, sg.acc + e, 16u * nq, bar, pol);
+#pragma unroll
+        for (int j = 0; j < KA; ++j)
+            if (j < K) bulk_load(stg + off_g + 8u * kTileQuads * j, gb[j] + e, 8u * nq, bar, pol);
+        bulk_load(stg + off_p, sg.p + e, 16u * nq, bar, pol);
+        bulk_load(stg + off_m, sg.m + e, 16u * nq, bar, pol);
+        bulk_load(stg + off_v, sg.v + e, 16u * nq, bar, pol);
+    }
+    __device__ void outputs(const Seg &sg, uint64_t e, void **out) const {
+        out[0] = sg.p + e;
+        out[1] = sg.m + e;
+        out[2] = sg.v + e;
+        out[3] = sg.bf + e;
+    }
+    __device__ void store(const TileDesc &d, unsigned char *stg, uint64_t pol) const {
+        bulk_store(d.out[0], stg + off_p, 16u * d.nq, pol);
+        bulk_store(d.out[1], stg + off_m, 16u * d.nq, pol);
+        bulk_store(d.out[2], stg + off_v, 16u * d.nq, pol);
+        bulk_store(d.out[3], stg + off_g, 8u * d.nq, pol);
+    }
+    __device__ void compute(const TileDesc &d, unsigned char *stg, uint32_t ct) const {
+        const GroupK G = gtab[d.group];
         const float4 *a4 = reinterpret_cast<const float4 *>(stg);
         uint2 *g4 = reinterpret_cast<uint2 *>(stg + off_g);
         float4 *p4 = reinterpret_cast<float4 *>(stg + off_p);
@@ -1180,7 +1265,7 @@ k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, cons
             if (HAS_ACC) av = a4[q];
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (j < K) gv[j] = g4[(size_t)tq * j + q];
+                if (j < K) gv[j] = g4[(size_t)kTileQuads * j + q];
             const float4 pv = p4[q], mv = m4[q], vv = v4[q];
             const float4 e = fold_quad<HAS_ACC, KMAX>(av, gv, K);
             const AdamOut o0 = adam_elem(__fmul_rn(e.x, gscale), pv.x, mv.x, vv.x, c_hi, c_lo, G);
@@ -1192,35 +1277,99 @@ k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, cons
             v4[q] = make_float4(o0.v, o1.v, o2.v, o3.v);
             g4[q] = make_uint2(pack_bf16x2(o0.p, o1.p), pack_bf16x2(o2.p, o3.p));
         }
-        if (d.scalars) {
-            // the chunk's head (warp 0) and tail (warp 1) elements, straight from global memory
-            const Chunk ch = chunks[d.chunk];
-            const Seg sg = segs[ch.seg];
-            const uint32_t len = ch.len;
-            const uint32_t hb = pipe_head(sg.bf + ch.start, len);
-            const uint32_t tail0 = hb + ((((len - hb) >> 3) << 1) << 2);
-            const uint32_t w = ct >> 5, lane = ct & 31u;
-            const uint32_t i0 = w == 0 ? lane : (w == 1 ? tail0 + lane : len);
-            if (i0 < (w == 0 ? hb : len) && !check_fails(ch.start + len > sg.numel, kFaultChunkRange)) {
-                const float *a = sg.acc + ch.start;
-                const uint16_t *g[KA];
-#pragma unroll
-                for (int j = 0; j < KA; ++j)
-                    g[j] = (j < K) ? gt.get(sg.grad_slot, j) + sg.grad_off + ch.start : nullptr;
-                float *p = sg.p + ch.start;
-                float *m = sg.m + ch.start;
-                float *v = sg.v + ch.start;
-                const float ev = __fmul_rn(fold_scalar<HAS_ACC, KMAX>(a, g, K, i0), gscale);
-                const AdamOut o = adam_elem(ev, p[i0], m[i0], v[i0], c_hi, c_lo, G);
-                p[i0] = o.p;
-                m[i0] = o.m;
-                v[i0] = o.v;
-                sg.bf[ch.start + i0] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
-            }
-        }
-        fence_async_smem();
-        mbar_arrive(&done[s]);
     }
+    __device__ void scalar(const Chunk &ch, const Seg &sg, uint32_t i, uint32_t group) const {
+        const uint16_t *g[KA];
+#pragma unroll
+        for (int j = 0; j < KA; ++j) g[j] = (j < K) ? gt->get(sg.grad_slot, j) + sg.grad_off + ch.start : nullptr;
+        float *p = sg.p + ch.start;
+        float *m = sg.m + ch.start;
+        float *v = sg.v + ch.start;
+        const float ev = __fmul_rn(fold_scalar<HAS_ACC, KMAX>(sg.acc + ch.start, g, K, i), gscale);
+        const AdamOut o = adam_elem(ev, p[i], m[i], v[i], c_hi, c_lo, gtab[group]);
+        p[i] = o.p;
+        m[i] = o.m;
+        v[i] = o.v;
+        sg.bf[ch.start + i] = __bfloat16_as_ushort(__float2bfloat16_rn(o.p));
+    }
+};
+
+// Fused clip + AdamW + master update + bf16 cast over units [u0, u1), the
+// same arithmetic per element as k_step (bit-identical results), with the
+// traffic moved by bulk copies (pipe_run): acc, the deferred gradients,
+// master, m and v in; master, m, v and the bf16 parameters out, in place.
+// One CTA per SM.  The host launches it only when pipe_fits(HAS_ACC, K).
+template <bool HAS_ACC, int KMAX, class GT>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+k_step_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, const PipeUnit *__restrict__ units,
+            uint32_t u0, uint32_t u1, const __grid_constant__ GT gt, StepState *st,
+            const NormState *__restrict__ ns, float gscale, int commit_t, unsigned *queue) {
+    extern __shared__ __align__(128) unsigned char pipe_smem[];
+    __shared__ PipeShared sh;
+    __shared__ GroupK sh_g[kMaxGroups];
+    pdl_enter();
+    if (st->skip) return;                   // non-finite norm, skipping enabled (no CTA claims a unit)
+    if (commit_t && blockIdx.x == 0 && threadIdx.x == 0) st->t += 1;
+    for (int i = threadIdx.x; i < kMaxGroups; i += kPipeThreads) sh_g[i] = st->gtab.g[i];
+    StepOps<HAS_ACC, KMAX, GT> ops(&gt, sh_g, KMAX <= 1 ? KMAX : (int)gt.k, gscale, ns->c_hi, ns->c_lo);
+    pipe_run(ops, segs, chunks, units, u0, u1, queue, pipe_smem, sh);
+}
+
+// One gradient added to the accumulator per tile (acc = acc + g), stored back
+// (see k_accum_pipe).
+template <class GT>
+struct AccumOps {
+    static constexpr uint32_t kTileQuads = kAccTileQuads;
+    static constexpr int stages = kAccStages;
+    static constexpr uint32_t stage_bytes = kAccQuadBytes * kAccTileQuads;
+    static constexpr uint32_t off_g = 16u * kAccTileQuads;
+    const GT *gt;
+    const uint16_t *gb;                 // copy thread: the current segment's gradient base
+
+    __device__ explicit AccumOps(const GT *g) : gt(g), gb(nullptr) {}
+    __device__ uint32_t tile_bytes(uint32_t nq) const { return nq * kAccQuadBytes; }
+    __device__ void set_seg(const Seg &sg) { gb = gt->get(sg.grad_slot, 0) + sg.grad_off; }
+    __device__ bool misaligned(const Seg &sg, uint64_t e) const { return mis16(sg.acc + e) || mis16(gb + e); }
+    __device__ void load(const Seg &sg, uint64_t e, uint32_t nq, unsigned char *stg, uint64_t *bar,
+                         uint64_t pol) const {
+        bulk_load(stg, sg.acc + e, 16u * nq, bar, pol);
+        bulk_load(stg + off_g, gb + e, 8u * nq, bar, pol);
+    }
+    __device__ void outputs(const Seg &sg, uint64_t e, void **out) const {
+        out[0] = sg.acc + e;
+        out[1] = out[2] = out[3] = nullptr;
+    }
+    __device__ void store(const TileDesc &d, unsigned char *stg, uint64_t pol) const {
+        bulk_store(d.out[0], stg, 16u * d.nq, pol);
+    }
+    __device__ void compute(const TileDesc &d, unsigned char *stg, uint32_t ct) const {
+        float4 *a4 = reinterpret_cast<float4 *>(stg);
+        const uint2 *g4 = reinterpret_cast<const uint2 *>(stg + off_g);
+        for (uint32_t q = ct; q < d.nq; q += kPipeCompute) {
+            const uint2 gv = g4[q];
+            a4[q] = fold_quad<true, 1>(a4[q], &gv, 1);
+        }
+    }
+    __device__ void scalar(const Chunk &ch, const Seg &sg, uint32_t i, uint32_t) const {
+        const uint16_t *g = gt->get(sg.grad_slot, 0) + sg.grad_off + ch.start;
+        float *a = sg.acc + ch.start;
+        a[i] = fold_scalar<true, 1>(a, &g, 1, i);
+    }
+};
+
+// An accumulate pass after FIRST that adds one gradient to the accumulator
+// and stores it (no norm): the same FP32 add per element as k_accum
+// (bit-identical), with the traffic moved by bulk copies (pipe_run).  One CTA
+// per SM.
+template <class GT>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+k_accum_pipe(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, const PipeUnit *__restrict__ units,
+             uint32_t u0, uint32_t u1, const __grid_constant__ GT gt, unsigned *queue) {
+    extern __shared__ __align__(128) unsigned char pipe_smem[];
+    __shared__ PipeShared sh;
+    pdl_enter();
+    AccumOps<GT> ops(&gt);
+    pipe_run(ops, segs, chunks, units, u0, u1, queue, pipe_smem, sh);
 }
 
 }  // namespace bf16k

@@ -87,7 +87,7 @@ def test_tiny_workload_dense(defer, step, monkeypatch):
     """The 1M-element shard, 3 steps; "pipe": the fused step forced through the
     bulk-copy pipeline (a shard this small takes vector loads by default)."""
     if step == "pipe":
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     st = dense_parity(workloads.workload(1), defer=defer)
     print("tiny", defer, step, st)
 
@@ -123,7 +123,7 @@ SMALL = [
 @pytest.mark.parametrize("defer", [False, True])
 def test_small_ragged_variants(case, mode, defer, step, monkeypatch):
     if step == "pipe":
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     sizes, mis, gas, steps, sigma = SMALL[case]
     decay = [(i % 3) != 1 for i in range(len(sizes))]
     wl = workloads.custom(100 + case, sizes, decay=decay, gas=gas, steps=steps, grad_sigma=sigma, misalign=mis,
@@ -142,7 +142,7 @@ def test_list_more_tensors_than_one_launch(sched, monkeypatch):
     if sched in ("claim", "pipe"):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
     if sched == "pipe":
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     rng = np.random.default_rng(5)
     sizes = rng.integers(1, 700, 1100).tolist()
     wl = workloads.custom(150, sizes, decay=[i % 2 == 0 for i in range(1100)], gas=2, steps=2,
@@ -315,10 +315,10 @@ def test_lr_override_and_resume():
 @needs_cuda
 @pytest.mark.parametrize("pipe", ["0", "1"])
 def test_step_kernel_follows_the_switch(pipe, monkeypatch):
-    """BF16OPT_STEP_PIPE=1 runs the fused step as the bulk-copy pipeline
+    """BF16OPT_PIPE=1 runs the fused step as the bulk-copy pipeline
     kernel, =0 as the vector-load kernel -- so the tests that force either one
     exercise the kernel they name."""
-    monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
+    monkeypatch.setenv("BF16OPT_PIPE", pipe)
     wl = workloads.custom(196, [20_001, 77], decay=[True, False], gas=2, steps=1, grad_sigma=0.1, misalign=3)
     sh = GpuShard(wl, defer=True)
     assert C.bf16opt_step_path(sh.opt.h) == (0, C.BF16OPT_PATH_NONE)
@@ -337,7 +337,7 @@ def test_pipe_needs_bf16_offsets_alike():
     import os
     wl = workloads.custom(197, [10_007, 64], decay=[True, False], gas=2, steps=2, grad_sigma=0.1)
     n = wl.n
-    os.environ["BF16OPT_STEP_PIPE"] = "1"
+    os.environ["BF16OPT_PIPE"] = "1"
     try:
         flat = {k: torch.zeros(n, dtype=dt, device="cuda") for k, dt in
                 (("master", torch.float32), ("exp_avg", torch.float32), ("exp_avg_sq", torch.float32),
@@ -345,7 +345,7 @@ def test_pipe_needs_bf16_offsets_alike():
         sgpu.fill_master(wl, flat["master"])
         opt = BF16Optimizer(wl.groups, flat=flat, ranges=wl.ranges(), max_grad_norm=wl.max_norm)
     finally:
-        os.environ.pop("BF16OPT_STEP_PIPE", None)
+        os.environ.pop("BF16OPT_PIPE", None)
     gb = torch.empty(n + 64, dtype=torch.int16, device="cuda")[4:4 + n]
     norms = []
 
@@ -541,7 +541,7 @@ def test_deferred_patterns(pat, mode, step, monkeypatch):
     """Deferring any micro-batches folds the same FP32 adds in the same order
     (with "pipe", in the bulk-copy step too: up to 8 gradient slots per stage)."""
     if step == "pipe":
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     pattern = DEFER_PATTERNS[pat]
     sizes = [50_001, 3, 16_384, 777] if mode == "flat" else [20_000, 5, 16_385, 1200]
     wl = workloads.custom(240 + pat, sizes, decay=[True, False, True, False], gas=len(pattern), steps=2,
@@ -578,7 +578,7 @@ def test_results_do_not_depend_on_the_grid(monkeypatch):
                              ("1", "claim", "0"), ("7", "claim", "0"), (None, "static", "1"), ("1", "static", "1"),
                              ("7", "claim", "1"), (None, "claim", "1")):
         monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
+        monkeypatch.setenv("BF16OPT_PIPE", pipe)
         if cap is None:
             monkeypatch.delenv("BF16OPT_MAX_GRID", raising=False)
         else:
@@ -608,7 +608,7 @@ def test_cuda_graph_replay_matches_eager(mode, sched, monkeypatch):
     if sched in ("claim", "pipe"):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
     if sched == "pipe":
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     wl = workloads.custom(260, [40_000, 3, 16_385, 999], decay=[True, False, True, False], gas=3, steps=4,
                           grad_sigma=0.1, misalign=2, mode=mode)
     eager = GpuShard(wl, defer=[False, True, True])
@@ -907,7 +907,7 @@ def test_random_sequences_match_oracle(seed, monkeypatch):
     if seed % 4 in (1, 2):
         monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
     if seed % 4 in (2, 3):
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", "1")
+        monkeypatch.setenv("BF16OPT_PIPE", "1")
     wl, pattern, gscale = _random_case(seed)
     dense_parity(wl, defer=pattern, grad_scale=gscale)
 
@@ -996,14 +996,14 @@ def test_small_sizes_every_misalignment(mode):
             wl = workloads.custom(600 + case, sizes, decay=[True, False][:len(sizes)], gas=gas, steps=2,
                                   grad_sigma=0.3, misalign=mis, mode=mode)
             for pipe in ("0", "1"):
-                os.environ["BF16OPT_STEP_PIPE"] = pipe
+                os.environ["BF16OPT_PIPE"] = pipe
                 try:
                     dense_parity(wl, defer=bool(case % 2))
                 except AssertionError as e:
                     raise AssertionError(f"n={n} misalign={mis} gas={gas} defer={bool(case % 2)} "
                                          f"pipe={pipe}: {e}") from None
                 finally:
-                    os.environ.pop("BF16OPT_STEP_PIPE", None)
+                    os.environ.pop("BF16OPT_PIPE", None)
             case += 1
 
 
@@ -1159,7 +1159,7 @@ def test_claimed_chunks_on_a_full_chunk_shard(monkeypatch):
     outs = []
     for sched, pipe in (("claim", "1"), ("static", "1"), ("claim", "0"), ("static", "0")):
         monkeypatch.setenv("BF16OPT_SCHEDULE", sched)
-        monkeypatch.setenv("BF16OPT_STEP_PIPE", pipe)
+        monkeypatch.setenv("BF16OPT_PIPE", pipe)
         for pat in ([False, False, False, True], [True] * 4, [True, False, True, True]):
             sh = GpuShard(wl, defer=pat)
             sh.run(wl.steps)
