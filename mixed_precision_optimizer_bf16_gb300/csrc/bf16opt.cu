@@ -394,7 +394,7 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
     bool first = true;
     const int K = (int)fs.count();
     const bool pipe = KMAX <= 4 && h->pipe && pipe_fits(HAS_ACC, K) && pipe_aligned(h, fs, HAS_ACC);
-    h->step_path = pipe ? BF16OPT_PATH_PIPELINE : BF16OPT_PATH_VECTOR;
+    h->step_path = h->n_chunks == 0 ? BF16OPT_PATH_NONE : (pipe ? BF16OPT_PATH_PIPELINE : BF16OPT_PATH_VECTOR);
     int rc = for_each_launch(h, fs, [&](const auto &gt, uint32_t c0, uint32_t c1) {
         using GT = std::decay_t<decltype(gt)>;
         if constexpr (KMAX <= 4) {

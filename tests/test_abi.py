@@ -218,8 +218,19 @@ def test_unknown_handles_are_rejected_without_dereference(lib):
     assert C.bf16opt_set_step(fake, 3) == E
     assert C.bf16opt_set_skip_nonfinite(fake, True) == E
     assert C.bf16opt_set_lr_schedule(fake, C.lr_schedule(10, 100, 0.1)) == E
+    assert C.bf16opt_step_path(fake) == (E, C.BF16OPT_PATH_NONE)
     assert C.bf16opt_destroy(fake) == E
     assert "not a live" in C.bf16opt_last_error(fake)
+
+
+def test_pipeline_timeouts_without_device(lib):
+    """The pipeline's timeout count needs a device: without one the call says
+    so instead of touching CUDA state; a NULL output is an argument error."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    assert C.bf16opt_pipeline_timeouts() == (C.BF16OPT_ERR_UNSUPPORTED, 0)
+    assert lib.bf16opt_pipeline_timeouts(None) == C.BF16OPT_ERR_INVALID_ARG
 
 
 def test_abi_version_matches_header_and_binding(lib):

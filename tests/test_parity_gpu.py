@@ -256,6 +256,7 @@ def test_empty_shard():
     assert C.bf16opt_grad_norm(h, 0, True) == (0, 0.0)
     assert C.bf16opt_step(h) == 0
     assert C.bf16opt_get_step(h) == (0, 1)
+    assert C.bf16opt_step_path(h) == (0, C.BF16OPT_PATH_NONE)   # nothing to launch
     C.bf16opt_destroy(h)
 
 
