@@ -414,8 +414,8 @@ int bf16opt_step_path(const bf16opt_t *h, int *path);
  * forces this on / off.  Every wait on a stage is bounded (2 s; a stage
  * normally turns over in microseconds).  A wait that gives up is counted in
  * a device word and its CTA stops, leaving the rest of its units of that
- * pass not updated.  This call waits for the device, stores the count
- * into *count (0 = every step completed) and clears it.
+ * pass not updated.  This call waits for the current device, stores that
+ * device's count into *count (0 = every pass completed) and clears it.
  * Errors: INVALID_ARG (count NULL), UNSUPPORTED (no device), CUDA. */
 int bf16opt_pipeline_timeouts(uint32_t *count);
 
