@@ -594,9 +594,21 @@ def run_ours(args):
         for nm, ceil in mix.items():
             if kern.get(nm, {}).get("gbs"):
                 kern[nm]["of_mix_ceiling"] = round(kern[nm]["gbs"] / ceil, 4)
-        probe["note"] = ("16-byte-vector streaming kernels, chunks claimed: copy 1:1, write-only, read-only, the "
-                         "fused step's 18:14 read:write mix and the accumulate passes' 2:4 and 6:4, no arithmetic; "
-                         "kernels.*.of_mix_ceiling = a pass's GB/s over its own mix's")
+        # the passes that moved their traffic with bulk copies, also against the
+        # bulk-copy ceiling of their mix
+        if path == C.BF16OPT_PATH_PIPELINE:
+            probe["step_kernel_of_bulk_step_mix"] = round(achieved / probe["step_mix_bulk_gbs"], 4)
+            bulk = {"step": probe["step_mix_bulk_gbs"]}
+            bulk.update({nm: probe["acc_mix_bulk_gbs"] for nm, c in mix.items() if c == probe["acc_mix_gbs"]})
+            for nm, ceil in bulk.items():
+                if kern.get(nm, {}).get("gbs"):
+                    kern[nm]["of_bulk_mix_ceiling"] = round(kern[nm]["gbs"] / ceil, 4)
+        probe["note"] = ("streaming kernels with no arithmetic beyond a few adds, work claimed from a counter: "
+                         "16-byte vector loads for copy 1:1, write-only, read-only, the fused step's 18:14 "
+                         "read:write mix and the accumulate passes' 2:4 and 6:4; bulk copies through shared "
+                         "memory (*_bulk_gbs) for the step's and a later accumulate's mixes; "
+                         "kernels.*.of_mix_ceiling = a pass's GB/s over its own mix's vector-load ceiling, "
+                         "of_bulk_mix_ceiling over its bulk-copy ceiling (pipelined passes)")
 
     # the other single-GPU target shards, timed by the same run (config freed first)
     extra = None

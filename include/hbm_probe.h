@@ -14,10 +14,20 @@
  *   HBM_PROBE_FIRST_MIX the first accumulate pass's: per 4 elements read 8 bytes,
  *                       write 16 (2 : 4 bytes per element);
  *   HBM_PROBE_ACC_MIX   a later accumulate pass's: per 4 elements read 16 + 8
- *                       bytes, write 16 (6 : 4 bytes per element).
- * Every kernel takes its 64 KiB chunks from a counter the way the optimizer's
- * passes do; the counter returns to zero by itself at the end of each launch
- * (the CTA holding the last claim past the end resets it).
+ *                       bytes, write 16 (6 : 4 bytes per element);
+ *   HBM_PROBE_BULK_STEP_MIX  the fused step's mix moved by bulk asynchronous
+ *                       copies through shared memory, as the pipelined step
+ *                       moves it (512-quad tiles, five stages, one copy
+ *                       thread and eight compute warps per SM, 2,048 quads
+ *                       per claim);
+ *   HBM_PROBE_BULK_ACC_MIX   a later accumulate pass's mix the same way
+ *                       (2,048-quad tiles, four stages, one tile per claim).
+ * The first six kinds use 16-byte vector loads and stores.  Every kernel
+ * takes its work from a counter the way the optimizer's passes do; the
+ * counter returns to zero by itself at the end of each launch (the CTA
+ * holding the last claim past the end resets it).  The bulk kinds bound every
+ * wait on a shared-memory barrier (2 s); a wait that gives up makes the run
+ * return -5.
  *
  * Buffers (device memory of the current device, 16-byte aligned, not
  * overlapping; the caller allocates them):
@@ -25,12 +35,12 @@
  *   WRITE:    buf[0], n x 16 bytes;
  *   READ:     buf[0], n x 16 bytes; buf[1] >= 4 bytes per CTA of the launch
  *             (hbm_probe_sink_bytes gives the size);
- *   STEP_MIX: n counts 4-element quads: buf[0] accumulator (16 B per quad),
- *             buf[1] gradient (8), buf[2..4] master, m, v (16 each), buf[5]
- *             bf16 parameters (8);
+ *   STEP_MIX, BULK_STEP_MIX: n counts 4-element quads: buf[0] accumulator
+ *             (16 B per quad), buf[1] gradient (8), buf[2..4] master, m, v (16
+ *             each), buf[5] bf16 parameters (8);
  *   FIRST_MIX: n quads: buf[0] gradient (8 B per quad), buf[1] accumulator (16);
- *   ACC_MIX:   n quads: buf[0] gradient (8 B per quad), buf[1] accumulator (16,
- *             read and written).
+ *   ACC_MIX, BULK_ACC_MIX: n quads: buf[0] gradient (8 B per quad), buf[1]
+ *             accumulator (16, read and written).
  * n must be a multiple of 4096 (64 KiB chunks of 16-byte vectors).
  *
  * hbm_probe_run times `reps` launches after `warmup` untimed ones with CUDA
@@ -57,6 +67,8 @@ extern "C" {
 #define HBM_PROBE_STEP_MIX 3
 #define HBM_PROBE_FIRST_MIX 4
 #define HBM_PROBE_ACC_MIX 5
+#define HBM_PROBE_BULK_STEP_MIX 6
+#define HBM_PROBE_BULK_ACC_MIX 7
 
 int hbm_probe_run(int kind, void *const *buf, uint64_t n, int warmup, int reps, void *stream, float *ms,
                   double *bytes);

@@ -8,6 +8,7 @@ from . import build as _build
 
 HBM_PROBE_COPY, HBM_PROBE_WRITE, HBM_PROBE_READ, HBM_PROBE_STEP_MIX = 0, 1, 2, 3
 HBM_PROBE_FIRST_MIX, HBM_PROBE_ACC_MIX = 4, 5
+HBM_PROBE_BULK_STEP_MIX, HBM_PROBE_BULK_ACC_MIX = 6, 7
 EXPORTS = ("hbm_probe_run", "hbm_probe_sink_bytes")
 
 _lib = None
@@ -48,7 +49,9 @@ def measure(vectors=1 << 28, quads=1 << 28, device="cuda", reps=10):
     """GB/s of each traffic mix on `device`: copy (1:1) and write-only and
     read-only over buffers of `vectors` 16-byte vectors; the fused step's
     18:14 mix and the accumulate passes' 2:4 (first) and 6:4 (later) mixes over
-    `quads` 4-element quads.  Allocates and frees the buffers."""
+    `quads` 4-element quads, with vector loads, and the step's and a later
+    accumulate's mixes through bulk copies (`*_bulk_gbs`).  Allocates and frees
+    the buffers."""
     import torch
     out = {}
     stream = torch.cuda.current_stream(device).cuda_stream
@@ -70,11 +73,13 @@ def measure(vectors=1 << 28, quads=1 << 28, device="cuda", reps=10):
     bufs = [torch.zeros(quads * k, dtype=dt, device=device) for k, dt in
             ((4, torch.float32), (4, torch.int16), (4, torch.float32), (4, torch.float32), (4, torch.float32),
              (4, torch.int16))]
-    rc, ms, nbytes = hbm_probe_run(HBM_PROBE_STEP_MIX, [t.data_ptr() for t in bufs], quads, 3, reps, stream)
-    if rc:
-        raise RuntimeError(f"hbm_probe_run(step_mix) failed ({rc})")
-    out["step_mix_gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
-    for name, kind in (("first_mix_gbs", HBM_PROBE_FIRST_MIX), ("acc_mix_gbs", HBM_PROBE_ACC_MIX)):
+    for name, kind in (("step_mix_gbs", HBM_PROBE_STEP_MIX), ("step_mix_bulk_gbs", HBM_PROBE_BULK_STEP_MIX)):
+        rc, ms, nbytes = hbm_probe_run(kind, [t.data_ptr() for t in bufs], quads, 3, reps, stream)
+        if rc:
+            raise RuntimeError(f"hbm_probe_run({name}) failed ({rc})")
+        out[name] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    for name, kind in (("first_mix_gbs", HBM_PROBE_FIRST_MIX), ("acc_mix_gbs", HBM_PROBE_ACC_MIX),
+                       ("acc_mix_bulk_gbs", HBM_PROBE_BULK_ACC_MIX)):
         rc, ms, nbytes = hbm_probe_run(kind, [bufs[1].data_ptr(), bufs[0].data_ptr()], quads, 3, reps, stream)
         if rc:
             raise RuntimeError(f"hbm_probe_run({name}) failed ({rc})")

@@ -51,6 +51,26 @@ def test_probe_on_the_gpu(lib):
     torch.cuda.synchronize()
     assert rc == 0 and ms > 0 and nbytes == 32 * n
     assert torch.equal(a, b)                       # every chunk copied exactly once
+    # the bulk-copy kinds move every tile exactly once: one launch of the
+    # accumulate mix adds g to acc once per element, one launch of the step
+    # mix adds a to p once per element and writes p's high halves as bf16
+    q = 1 << 22
+    g = torch.randint(-2**14, 2**14, (q * 4,), dtype=torch.int16, device="cuda")   # finite bf16 values
+    acc = torch.randn(q * 4, device="cuda")
+    want = acc + (g.to(torch.int32) << 16).view(torch.float32)
+    rc, ms, nbytes = P.hbm_probe_run(P.HBM_PROBE_BULK_ACC_MIX, [g.data_ptr(), acc.data_ptr()], q, warmup=0, reps=1)
+    torch.cuda.synchronize()
+    assert rc == 0 and nbytes == 40 * q
+    assert torch.equal(acc.view(torch.int32), want.view(torch.int32))
+    bufs = [torch.randn(q * 4, device="cuda"), g, torch.randn(q * 4, device="cuda"), torch.randn(q * 4, device="cuda"),
+            torch.randn(q * 4, device="cuda"), torch.zeros(q * 4, dtype=torch.int16, device="cuda")]
+    p_want = bufs[2] + bufs[0]
+    rc, ms, nbytes = P.hbm_probe_run(P.HBM_PROBE_BULK_STEP_MIX, [t.data_ptr() for t in bufs], q, warmup=0, reps=1)
+    torch.cuda.synchronize()
+    assert rc == 0 and nbytes == 128 * q
+    assert torch.equal(bufs[2].view(torch.int32), p_want.view(torch.int32))
+    assert torch.equal(bufs[5], (p_want.view(torch.int32) >> 16).to(torch.int16))
     got = P.measure(vectors=n, quads=n // 2)
-    for k in ("copy_gbs", "write_gbs", "read_gbs", "step_mix_gbs"):
+    for k in ("copy_gbs", "write_gbs", "read_gbs", "step_mix_gbs", "first_mix_gbs", "acc_mix_gbs",
+              "step_mix_bulk_gbs", "acc_mix_bulk_gbs"):
         assert 500.0 < got[k] < 20000.0, (k, got)
