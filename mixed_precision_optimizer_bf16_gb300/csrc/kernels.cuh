@@ -1,7 +1,7 @@
 // kernels.cuh -- sm_103a kernels of the BF16 mixed-precision optimizer step.
 //
-// Three bandwidth-bound kernels (no tensor cores: nothing here is a
-// contraction) over a table of chunks, and three single-CTA kernels:
+// Bandwidth-bound kernels (no tensor cores: nothing here is a contraction)
+// over a table of chunks, and three single-CTA kernels:
 //   k_accum          folds bf16 micro-batch gradients into the FP32 accumulator,
 //                    optionally with the per-chunk partial sums of squares of the
 //                    global norm fused in ("BLOOM 176B 训练技术概览", section
@@ -16,7 +16,10 @@
 //                    learning-rate override or settings changed since the norm;
 //   k_step           clip x AdamW x FP32 master/moment update x bf16 cast in one pass
 //                    ("企业官网建设流程全解析", sections 1 and 3.3); advances the step
-//                    counter when the norm kernel prepared the scalars.
+//                    counter when the norm kernel prepared the scalars;
+//   k_step_pipe, k_accum_pipe  the fused step and the accumulate passes after
+//                    FIRST with the same arithmetic, their traffic moved by
+//                    bulk copies through shared memory (pipe_run, at the end).
 //
 // Work decomposition.  A segment is one run of elements with one parameter
 // group and one set of base pointers (a flat range or a list tensor).  The
@@ -823,13 +826,14 @@ k_step(const Seg *__restrict__ segs, const Chunk *__restrict__ chunks, uint32_t 
 
 
 // ------------------------------------------------------ bulk-copy pipeline
-// The fused step's traffic moved by the SM's bulk asynchronous copy unit
-// instead of per-thread vector loads and stores: cp.async.bulk copies whole
-// runs of a stream between global and shared memory, loads completing on an
-// mbarrier by transaction count, stores retired through bulk groups.  One
-// thread of the CTA issues every copy; the other warps compute in shared
-// memory.  Measured on the step's 18:14 read:write mix over 2^30 elements:
-// 7.20 TB/s against 7.00 TB/s for the best shape of 16-byte vector loads.
+// The traffic of the fused step and of the later accumulate passes moved by
+// the SM's bulk asynchronous copy unit instead of per-thread vector loads and
+// stores: cp.async.bulk copies whole runs of a stream between global and
+// shared memory, loads completing on an mbarrier by transaction count, stores
+// retired through bulk groups.  One thread of the CTA issues every copy; the
+// other warps compute in shared memory.  Measured on the step's 18:14
+// read:write mix over 2^30 elements: 7.20 TB/s against 7.00 TB/s for the best
+// shape of 16-byte vector loads.
 
 // Waits that gave up (see mbar_wait); read and cleared by
 // bf16opt_pipeline_timeouts.
