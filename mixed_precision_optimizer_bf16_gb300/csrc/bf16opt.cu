@@ -190,18 +190,30 @@ uint32_t first_chunk_cut(const void *p) { return (uint32_t)(((uintptr_t)p >> 2) 
 bool mis4(const void *p) { return ((uintptr_t)p & 3u) != 0; }
 bool mis2(const void *p) { return ((uintptr_t)p & 1u) != 0; }
 
-// A function attribute set once per kernel and device (kernels of one
-// template share a function type, so the kernel's address is the key).
+unsigned long long current_ctx_id();   // below, with the allocation-free norm
+
+// A function attribute set once per kernel, device and context (kernels of
+// one template share a function type, so the kernel's address is the key; a
+// context that replaced a reset one has the module loaded afresh, without
+// the attribute, and a new id).  Set on every call when the context's id
+// cannot be read.
 template <class K>
 cudaError_t kernel_attr_once(K kernel, int dev, cudaFuncAttribute attr, int value) {
+    struct Done {
+        const void *kernel;
+        int dev, attr;
+        unsigned long long ctx;
+    };
     static std::mutex mu;
-    static std::vector<std::pair<const void *, int>> done;
-    std::lock_guard<std::mutex> lock(mu);
+    static std::vector<Done> done;
     const void *key = reinterpret_cast<const void *>(kernel);
-    for (const auto &e : done)
-        if (e.first == key && e.second == dev) return cudaSuccess;
+    const unsigned long long ctx = current_ctx_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (ctx != 0)
+        for (const Done &d : done)
+            if (d.kernel == key && d.dev == dev && d.attr == (int)attr && d.ctx == ctx) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(kernel, attr, value);
-    if (e == cudaSuccess) done.emplace_back(key, dev);
+    if (e == cudaSuccess && ctx != 0) done.push_back({key, dev, (int)attr, ctx});
     return e;
 }
 

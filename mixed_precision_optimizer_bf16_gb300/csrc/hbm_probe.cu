@@ -376,22 +376,14 @@ int grid_of(K kernel, int *grid) {
     return 0;
 }
 
-// The bulk kernels' shared memory opt-in (once per device and kernel) and grid
-// (one CTA per SM).
+// The bulk kernels' shared memory opt-in (set on every run: a run is long,
+// and a context that replaced a reset one would not have it) and grid (one CTA
+// per SM).
 int bulk_setup(int dev, bool step, int *grid) {
-    static std::mutex mu;
-    static uint64_t done[2] = {0, 0};
-    std::lock_guard<std::mutex> lk(mu);
-    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
-    if (!bit) return -1;
-    cudaError_t e = cudaSuccess;
-    if (!(done[step ? 0 : 1] & bit)) {
-        e = step ? cudaFuncSetAttribute(k_bulk_mix<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(BulkMix<0>::stages * BulkMix<0>::stage_bytes))
-                 : cudaFuncSetAttribute(k_bulk_mix<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(BulkMix<1>::stages * BulkMix<1>::stage_bytes));
-        if (e == cudaSuccess) done[step ? 0 : 1] |= bit;
-    }
+    cudaError_t e = step ? cudaFuncSetAttribute(k_bulk_mix<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)(BulkMix<0>::stages * BulkMix<0>::stage_bytes))
+                         : cudaFuncSetAttribute(k_bulk_mix<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)(BulkMix<1>::stages * BulkMix<1>::stage_bytes));
     int sms = 0;
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess || sms < 1) {
