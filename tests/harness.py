@@ -29,6 +29,7 @@ Tolerances (the workload definitions' bar, plainest reading where silent):
                  scale it admits the few ulps their FP32 tolerance implies.
 """
 import math
+import os
 
 import numpy as np
 import torch
@@ -36,6 +37,7 @@ import torch
 import oracle
 import synth
 from synth import gpu as sgpu
+from mixed_precision_optimizer_bf16_gb300 import bf16opt as C
 from mixed_precision_optimizer_bf16_gb300.optimizer import BF16Optimizer, alloc_flat
 
 REL = 1e-6
@@ -71,6 +73,10 @@ class GpuShard:
             assert len(self.pattern) == G
         self.defer = self.pattern[-1]
         self.norms = []
+        # forced through the bulk-copy pipeline: the step must take it where its
+        # stage fits (the accumulator with up to 2 pending gradients, or up to 4
+        # without it) and the buffers are aligned alike (see expected_step_path)
+        self.forced_pipe = os.environ.get("BF16OPT_PIPE") == "1"
         if wl.mode == "flat":
             self.flat = alloc_flat(wl.n, "cuda", wl.misalign)
             sgpu.fill_master(wl, self.flat["master"])
@@ -116,10 +122,30 @@ class GpuShard:
         self.norms.append(norm)
         return norm
 
+    def expected_step_path(self):
+        """BF16OPT_PATH_* the fused step should have taken."""
+        if self.wl.n == 0:
+            return C.BF16OPT_PATH_NONE
+        if not self.forced_pipe:
+            return None
+        pending = len(self.pattern) - max([k + 1 for k, d in enumerate(self.pattern) if not d], default=0)
+        has_acc = not all(self.pattern)
+        quad_bytes = (16 if has_acc else 0) + 8 * max(pending, 1) + 48
+        # FLAT: every range's gradient starts at the range's own offset, as its
+        # state does.  LIST: tensor i's gradient is a slice at offsets[i] of one
+        # buffer while its state is allocated on its own, so the bf16 offsets
+        # agree modulo 16 bytes only where offsets[i] is a multiple of 8.
+        aligned = (self.wl.mode == "flat" or pending == 0 or
+                   all(off % 8 == 0 for t, off in zip(self.wl.tensors, self.wl.offsets) if t.numel))
+        return C.BF16OPT_PATH_PIPELINE if quad_bytes <= 80 and aligned else C.BF16OPT_PATH_VECTOR
+
     def run(self, steps):
         for s in range(steps):
             self.run_step(s)
         torch.cuda.synchronize()
+        want = self.expected_step_path()
+        if want is not None and steps:
+            assert C.bf16opt_step_path(self.opt.h) == (0, want), (C.bf16opt_step_path(self.opt.h), want)
 
     # ---- read back
     def full(self, name):
