@@ -59,9 +59,11 @@ def _alloc(n, dtype, misalign, device="cuda"):
 class GpuShard:
     """Device state of a workload + its bf16opt handle."""
 
-    def __init__(self, wl, grad_scale=1.0, defer=False):
+    def __init__(self, wl, grad_scale=1.0, defer=False, grad_per_tensor=False):
         """defer: False, True (defer the last micro-batch only) or a per-micro-batch
-        list of flags (deferred gradients then get buffers of their own)."""
+        list of flags (deferred gradients then get buffers of their own).
+        grad_per_tensor (LIST): every tensor's gradient gets a buffer of its
+        own, offset like its state, instead of a slice of one flat buffer."""
         self.wl = wl
         G = wl.gas
         if defer is True:
@@ -104,6 +106,9 @@ class GpuShard:
         nbuf = wl.gas if any(self.pattern[:-1]) else 1
         self.gbufs = [_alloc(wl.n, torch.int16, wl.misalign) for _ in range(nbuf)]
         self.gbuf = self.gbufs[0]
+        self.grad_per_tensor = bool(grad_per_tensor) and wl.mode != "flat"
+        self.tgrads = ([[_alloc(t.numel, torch.int16, wl.misalign) for t in wl.tensors] for _ in range(nbuf)]
+                       if self.grad_per_tensor else None)
 
     def grads_arg(self, buf=None):
         buf = self.gbuf if buf is None else buf
@@ -116,7 +121,14 @@ class GpuShard:
         for k in range(wl.gas):
             buf = self.gbufs[k % len(self.gbufs)]
             sgpu.fill_grad(wl, step, k, buf)
-            self.opt.accumulate(self.grads_arg(buf), first=(k == 0), last=(k == wl.gas - 1), defer=self.pattern[k])
+            if self.grad_per_tensor:
+                own = self.tgrads[k % len(self.gbufs)]
+                for dst, t, off in zip(own, wl.tensors, wl.offsets):
+                    dst.copy_(buf[off:off + t.numel])
+                arg = own
+            else:
+                arg = self.grads_arg(buf)
+            self.opt.accumulate(arg, first=(k == 0), last=(k == wl.gas - 1), defer=self.pattern[k])
         norm = self.opt.grad_norm(sync=True)
         self.opt.step()
         self.norms.append(norm)
@@ -135,7 +147,7 @@ class GpuShard:
         # state does.  LIST: tensor i's gradient is a slice at offsets[i] of one
         # buffer while its state is allocated on its own, so the bf16 offsets
         # agree modulo 16 bytes only where offsets[i] is a multiple of 8.
-        aligned = (self.wl.mode == "flat" or pending == 0 or
+        aligned = (self.wl.mode == "flat" or pending == 0 or self.grad_per_tensor or
                    all(off % 8 == 0 for t, off in zip(self.wl.tensors, self.wl.offsets) if t.numel))
         return C.BF16OPT_PATH_PIPELINE if quad_bytes <= 80 and aligned else C.BF16OPT_PATH_VECTOR
 

@@ -32,8 +32,8 @@ def _cleanup():
         torch.cuda.empty_cache()
 
 
-def dense_parity(wl, defer=False, grad_scale=1.0):
-    sh = GpuShard(wl, grad_scale=grad_scale, defer=defer)
+def dense_parity(wl, defer=False, grad_scale=1.0, grad_per_tensor=False):
+    sh = GpuShard(wl, grad_scale=grad_scale, defer=defer, grad_per_tensor=grad_per_tensor)
     sh.run(wl.steps)
     got = sh.states()
     norms = list(sh.norms)
@@ -129,6 +129,22 @@ def test_small_ragged_variants(case, mode, defer, step, monkeypatch):
     wl = workloads.custom(100 + case, sizes, decay=decay, gas=gas, steps=steps, grad_sigma=sigma, misalign=mis,
                           mode=mode)
     dense_parity(wl, defer=defer)
+
+
+@needs_cuda
+@pytest.mark.parametrize("pat", [[False, False, True], [False, True, True], [True, True, True, True],
+                                 [False, False, False], [True, False, True]])
+def test_list_pipeline_with_own_gradient_buffers(pat, monkeypatch):
+    """LIST tensors of ragged sizes whose gradients have buffers of their own,
+    offset like their state (so the bulk-copy pipeline applies whatever the
+    sizes), the pipeline forced: the later accumulates and the step fold the
+    gradients -- the deferred ones too -- through bulk copies, with scalar
+    heads and tails on every tensor, and equal the oracle over two steps."""
+    monkeypatch.setenv("BF16OPT_PIPE", "1")
+    monkeypatch.setenv("BF16OPT_SCHEDULE", "claim")
+    wl = workloads.custom(275, [20_000, 5, 16_385, 1200, 7, 65_539], decay=[True, False, True, False, True, True],
+                          gas=len(pat), steps=2, grad_sigma=0.05, misalign=3, mode="list")
+    dense_parity(wl, defer=pat, grad_per_tensor=True)
 
 
 @needs_cuda
