@@ -313,6 +313,14 @@ int for_each_launch(bf16opt_t *h, const FoldSet &fs, F &&launch) {
     return 0;
 }
 
+// Grid of a pipelined pass: one CTA per SM (its stages fill the SM's shared
+// memory), no more CTAs than units, within the BF16OPT_MAX_GRID cap.
+unsigned pipe_grid(const bf16opt_t *h, uint64_t units) {
+    uint64_t g = std::min<uint64_t>((uint64_t)h->sm_count, units);
+    if (h->max_grid > 0 && g > (uint64_t)h->max_grid) g = (uint64_t)h->max_grid;
+    return (unsigned)std::max<uint64_t>(1, g);
+}
+
 // The bulk-copy passes need every stream of a chunk's body 16-byte aligned at
 // one element: per segment, the FP32 pointers (master, m, v, the accumulator
 // if used) share their element index modulo 4, the bf16 ones (parameters,
@@ -356,10 +364,8 @@ int launch_accum_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st) {
                 cudaError_t e1 = kernel_attr_once(kp, h->device, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   (int)smem);
                 const uint32_t u0 = h->chunk_unit0[c0], u1 = h->chunk_unit0[c1];
-                uint64_t grid = std::min<uint64_t>((uint64_t)h->sm_count, u1 - u0);
-                if (h->max_grid > 0 && grid > (uint64_t)h->max_grid) grid = (uint64_t)h->max_grid;
                 if (e1 == cudaSuccess)
-                    e1 = launch_smem(h, kp, (unsigned)std::max<uint64_t>(1, grid), kPipeThreads, smem, st,
+                    e1 = launch_smem(h, kp, pipe_grid(h, u1 - u0), kPipeThreads, smem, st,
                                      (const Seg *)h->segs_d, (const Chunk *)h->chunks_d,
                                      (const PipeUnit *)h->units_d, u0, u1, gt, h->claim ? h->queue_d : nullptr);
                 if (e == cudaSuccess) e = e1;
@@ -416,10 +422,8 @@ int launch_step_k(bf16opt_t *h, const FoldSet &fs, cudaStream_t st, bool commit_
             cudaError_t e1 = kernel_attr_once(kp, h->device, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)kPipeSmem);   // the most any K of the variant takes
             const uint32_t u0 = h->chunk_unit0[c0], u1 = h->chunk_unit0[c1];
-            uint64_t grid = std::min<uint64_t>((uint64_t)h->sm_count, u1 - u0);
-            if (h->max_grid > 0 && grid > (uint64_t)h->max_grid) grid = (uint64_t)h->max_grid;
             if (e1 == cudaSuccess)
-                e1 = launch_smem(h, kp, (unsigned)std::max<uint64_t>(1, grid), kPipeThreads, smem, st,
+                e1 = launch_smem(h, kp, pipe_grid(h, u1 - u0), kPipeThreads, smem, st,
                                  (const Seg *)h->segs_d, (const Chunk *)h->chunks_d, (const PipeUnit *)h->units_d,
                                  u0, u1, gt, h->step_d, (const NormState *)h->norm_d, h->gscale,
                                  (commit_t && first) ? 1 : 0, h->claim ? h->queue_d : nullptr);
